@@ -1,0 +1,243 @@
+"""fp64 / exact-integer oracle for slot mapping, the KV write, block copy and
+paged decode attention.
+
+TEST INFRASTRUCTURE ONLY (see oracle/__init__.py). Arrays are numpy. Stored KV
+values keep their storage type: numpy float32, float16, or uint16 bit patterns
+for bfloat16 (numpy has no bfloat16); `upcast` turns any of them into float64
+exactly.
+
+Pool layout (a reading; the pages only say a block holds the K/V vectors of B
+tokens): key_cache and value_cache are [num_blocks, num_kv_heads, block_size,
+head_size]. A slot id s names block s // B, row s % B of that block.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+PAD_SLOT = -1
+
+
+# --------------------------------------------------------------------------
+# dtype handling
+# --------------------------------------------------------------------------
+def upcast(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact widening of stored values to float64.
+
+    bf16 is the upper half of an IEEE fp32 word, so its value is the fp32
+    whose high 16 bits are the stored pattern and low 16 bits are zero."""
+    if dtype == "f32":
+        assert a.dtype == np.float32
+        return a.astype(np.float64)
+    if dtype == "f16":
+        assert a.dtype == np.float16
+        return a.astype(np.float64)
+    if dtype == "bf16":
+        assert a.dtype in (np.uint16, np.int16)
+        bits = a.view(np.uint16).astype(np.uint32) << np.uint32(16)
+        return bits.view(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+# --------------------------------------------------------------------------
+# block arithmetic ([P4] "按 Block 分配"; [P2] block-size trade-off section)
+# --------------------------------------------------------------------------
+def blocks_needed(num_tokens: int, block_size: int) -> int:
+    """A sequence of T tokens without sharing holds ceil(T / B) blocks
+    ([P4] "按 Block 分配": 9 tokens, B=4 -> 3 blocks)."""
+    assert num_tokens >= 0 and block_size >= 1
+    return -(-num_tokens // block_size)
+
+
+def slots_allocated(num_tokens: int, block_size: int) -> int:
+    """B * ceil(T / B) token slots ([P4] "按 Block 分配": 12 slots)."""
+    return block_size * blocks_needed(num_tokens, block_size)
+
+
+def fragmentation(lengths, block_size: int):
+    """Tail waste of a batch, as the block-size section of [P2] defines it:
+    blocks = sum ceil(L/B), slots = blocks * B, empty = slots - sum L,
+    rate = empty / slots. Returns (blocks, slots, empty, rate)."""
+    blocks = sum(blocks_needed(L, block_size) for L in lengths)
+    slots = blocks * block_size
+    empty = slots - sum(lengths)
+    return blocks, slots, empty, (empty / slots if slots else 0.0)
+
+
+def kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_size: int,
+                       dtype_bytes: int) -> int:
+    """Per-token KV footprint: 2 (K and V) x layers x KV heads x head size x
+    bytes per element ([P3] §2.1; [P1] §1.1 memory formula; [P2] OPT-13B
+    example)."""
+    return 2 * num_layers * num_kv_heads * head_size * dtype_bytes
+
+
+def sharing_saving(tables) -> float:
+    """Block saving of a set of block tables as [P2]'s Figure-8 simulator
+    defines it: (logical mappings - distinct physical blocks) / logical
+    mappings."""
+    logical = sum(len(t) for t in tables)
+    unique = len({b for t in tables for b in t})
+    return (logical - unique) / logical if logical else 0.0
+
+
+# --------------------------------------------------------------------------
+# slot mapping ([P1] §2.3 BlockTable / slot-mapping kernel, single rank)
+# --------------------------------------------------------------------------
+def slot_mapping(query_start_loc, positions, block_table, block_size: int,
+                 num_tokens: int | None = None) -> np.ndarray:
+    """slot[t] for every token t of request r (query_start_loc[r] <= t <
+    query_start_loc[r+1]):
+
+        logical block  lb  = pos // B
+        physical block pb  = block_table[r, lb]
+        slot               = pb * B + (pos - lb * B)
+
+    This is the context-parallel-free case of [P1] §2.3 (world size 1, so
+    every token is local and no PAD is produced by the formula). Tokens that
+    belong to no request keep PAD_SLOT (-1).
+
+    Invalid input (negative position, logical block beyond the table row, or
+    an unassigned (negative) table entry) raises ValueError."""
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    pos = np.asarray(positions, dtype=np.int64)
+    tab = np.asarray(block_table, dtype=np.int64)
+    T = len(pos) if num_tokens is None else num_tokens
+    out = np.full(T, PAD_SLOT, dtype=np.int64)
+    B = int(block_size)
+    for r in range(len(qsl) - 1):
+        for t in range(int(qsl[r]), int(qsl[r + 1])):
+            if t < 0 or t >= T:
+                continue
+            p = int(pos[t])
+            if p < 0:
+                raise ValueError(f"negative position at token {t}")
+            lb = p // B
+            if lb >= tab.shape[1]:
+                raise ValueError(f"token {t}: logical block {lb} past the table")
+            pb = int(tab[r, lb])
+            if pb < 0:
+                raise ValueError(f"token {t}: table entry {lb} unassigned")
+            out[t] = pb * B + (p - lb * B)
+    return out
+
+
+# --------------------------------------------------------------------------
+# KV write and block copy (byte copies)
+# --------------------------------------------------------------------------
+def reshape_and_cache(k, v, slots, key_cache, value_cache, block_size: int):
+    """Write token t's K/V rows (every KV head) into the pool slot slots[t],
+    in place. A negative slot (PAD) is skipped. The slot names block
+    slot // B, row slot % B ([P1] §2.3: the slot mapping lets the attention
+    kernel address the pool directly)."""
+    B = int(block_size)
+    nb = key_cache.shape[0]
+    for t, s in enumerate(np.asarray(slots, dtype=np.int64)):
+        s = int(s)
+        if s < 0:
+            continue
+        blk, row = s // B, s % B
+        if blk >= nb:
+            raise ValueError(f"slot {s} outside the pool")
+        key_cache[blk, :, row, :] = k[t]
+        value_cache[blk, :, row, :] = v[t]
+
+
+def copy_blocks(key_caches, value_caches, src_dst_pairs):
+    """Block-level copy-on-write data movement: for each (src, dst) pair,
+    every layer's K and V block src is copied whole into block dst ([P2]
+    Figure 8: block 1's content is copied into block 3; [P4] COW figure:
+    P0 copied into P4). Destinations must be distinct and no destination may
+    also be a source."""
+    pairs = [(int(a), int(b)) for a, b in np.asarray(src_dst_pairs).reshape(-1, 2)]
+    dsts = [d for _, d in pairs]
+    srcs = {s for s, _ in pairs}
+    if len(set(dsts)) != len(dsts) or any(d in srcs for d in dsts):
+        raise ValueError("aliasing copy pairs")
+    for kc, vc in zip(key_caches, value_caches):
+        for s, d in pairs:
+            kc[d] = kc[s]
+            vc[d] = vc[s]
+
+
+# --------------------------------------------------------------------------
+# paged decode attention
+# --------------------------------------------------------------------------
+def gather_kv(cache, table_row, seq_len: int, kv_head: int, block_size: int,
+              dtype: str) -> np.ndarray:
+    """Contiguous fp64 copy of one sequence's K (or V) rows for one KV head,
+    token j read from physical block table_row[j // B], row j % B ([P4]
+    "按 Block 分配": token 8 -> logical block 2 -> P4, row 0)."""
+    j = np.arange(seq_len, dtype=np.int64)
+    blk = np.asarray(table_row, dtype=np.int64)[j // block_size]
+    if seq_len and (blk.min() < 0 or blk.max() >= cache.shape[0]):
+        raise ValueError("block id outside the pool")
+    rows = cache[blk, kv_head, j % block_size, :]
+    return upcast(np.ascontiguousarray(rows), dtype)
+
+
+def decode_attention_one(q_vec64, K64, V64, scale: float) -> np.ndarray:
+    """Textbook single-query softmax attention in fp64:
+        x_j = scale * <q, k_j>;  m = max_j x_j;  p_j = exp(x_j - m)
+        o   = sum_j p_j v_j / sum_j p_j
+    An empty context gives the zero vector (a reading: the pages always
+    attend over at least one token)."""
+    if K64.shape[0] == 0:
+        return np.zeros(V64.shape[1], dtype=np.float64)
+    x = scale * (K64 @ q_vec64)
+    m = x.max()
+    p = np.exp(x - m)
+    return (p @ V64) / p.sum()
+
+
+def decode_attention(q, key_cache, value_cache, block_tables, seq_lens,
+                     scale: float, num_kv_heads: int, block_size: int,
+                     dtype: str, seqs=None, heads=None) -> np.ndarray:
+    """Paged decode attention for every (sequence, query head), or for the
+    listed subsets. Query head h reads KV head h // (Hq / Hkv) (contiguous
+    groups; [P3] §2.1: 64 query heads share 8 KV heads).
+
+    The pages state that paging keeps dense attention semantics ([P4] last
+    section; [P2]: the kernel reads block by block, so blocks need not be
+    contiguous). The oracle therefore gathers each sequence's K and V through
+    its block table into contiguous arrays and runs dense attention on them.
+
+    Returns float64 [S, Hq, D] (rows outside `seqs`/`heads` stay zero)."""
+    S, Hq, D = q.shape
+    assert Hq % num_kv_heads == 0
+    g = Hq // num_kv_heads
+    q64 = upcast(q, dtype)
+    out = np.zeros((S, Hq, D), dtype=np.float64)
+    seqs = range(S) if seqs is None else seqs
+    heads = range(Hq) if heads is None else heads
+    for s in seqs:
+        L = int(seq_lens[s])
+        by_kv = {}
+        for h in heads:
+            kvh = h // g
+            if kvh not in by_kv:
+                by_kv[kvh] = (
+                    gather_kv(key_cache, block_tables[s], L, kvh, block_size, dtype),
+                    gather_kv(value_cache, block_tables[s], L, kvh, block_size, dtype))
+            K, V = by_kv[kvh]
+            out[s, h] = decode_attention_one(q64[s, h], K, V, scale)
+    return out
+
+
+def decode_step(q, k_new, v_new, key_cache, value_cache, block_tables,
+                context_lens, scale: float, num_kv_heads: int,
+                block_size: int, dtype: str, seqs=None, heads=None):
+    """One decode step as the build reads the pages' order: the new token's
+    slot is computed from its position (= cached context length), its K/V are
+    written there, then it attends over context + 1 tokens including itself.
+    Mutates the caches (caller passes copies). Returns (slots, out fp64)."""
+    S = q.shape[0]
+    qsl = np.arange(S + 1, dtype=np.int64)
+    pos = np.asarray(context_lens, dtype=np.int64)
+    slots = slot_mapping(qsl, pos, block_tables, block_size)
+    reshape_and_cache(k_new, v_new, slots, key_cache, value_cache, block_size)
+    seq_lens = pos + 1
+    out = decode_attention(q, key_cache, value_cache, block_tables, seq_lens,
+                           scale, num_kv_heads, block_size, dtype, seqs, heads)
+    return slots, out

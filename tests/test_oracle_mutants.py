@@ -1,0 +1,168 @@
+"""Planted mistakes: each mutant below is a plausible slip in the oracle (a
+dropped term, a wrong index, a transposed operand, floor for ceil, a missed
+reference-count update). The pins in test_oracle_pins.py and
+test_oracle_attention.py must catch every one of them. Mutants are planted in
+the oracle on the CPU only, through monkeypatching."""
+import numpy as np
+import pytest
+
+import oracle
+import oracle.paged_attention as opa
+import oracle.block_manager as obm
+import tests.test_oracle_attention as ta
+import tests.test_oracle_pins as tp
+
+
+def _slot_no_subtract(qsl, pos, tab, B, num_tokens=None):
+    tab = np.asarray(tab)
+    out = np.full(len(pos) if num_tokens is None else num_tokens, -1, np.int64)
+    for r in range(len(qsl) - 1):
+        for t in range(int(qsl[r]), int(qsl[r + 1])):
+            p = int(pos[t])
+            out[t] = int(tab[r, p // B]) * B + p          # offset not reduced
+    return out
+
+
+def _slot_offset_swapped(qsl, pos, tab, B, num_tokens=None):
+    tab = np.asarray(tab)
+    out = np.full(len(pos) if num_tokens is None else num_tokens, -1, np.int64)
+    for r in range(len(qsl) - 1):
+        for t in range(int(qsl[r]), int(qsl[r + 1])):
+            p = int(pos[t])
+            out[t] = int(tab[r, p % B if p % B < tab.shape[1] else 0]) * B + p // B
+    return out
+
+
+def _blocks_floor(T, B):
+    return T // B
+
+
+def _attn_no_max(q, K, V, scale):
+    if K.shape[0] == 0:
+        return np.zeros(V.shape[1])
+    p = np.exp(scale * (K @ q))
+    return (p @ V) / p.sum()
+
+
+def _attn_no_scale(q, K, V, scale):
+    if K.shape[0] == 0:
+        return np.zeros(V.shape[1])
+    x = K @ q
+    p = np.exp(x - x.max())
+    return (p @ V) / p.sum()
+
+
+def _attn_no_normalise(q, K, V, scale):
+    if K.shape[0] == 0:
+        return np.zeros(V.shape[1])
+    x = scale * (K @ q)
+    return np.exp(x - x.max()) @ V
+
+
+def _attn_keys_as_values(q, K, V, scale):
+    if K.shape[0] == 0:
+        return np.zeros(V.shape[1])
+    x = scale * (K @ q)
+    p = np.exp(x - x.max())
+    return (p @ K) / p.sum()
+
+
+def _gather_head_modulo(cache, table_row, L, kv_head, B, dtype):
+    # wrong row inside the block: j // B instead of j % B
+    j = np.arange(L)
+    blk = np.asarray(table_row)[j // B]
+    return opa.upcast(np.ascontiguousarray(cache[blk, kv_head, (j // B) % B, :]), dtype)
+
+
+def _upcast_bf16_wrong_shift(a, dtype):
+    if dtype == "bf16":
+        bits = a.view(np.uint16).astype(np.uint32) << np.uint32(15)
+        return bits.view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def _decode_gqa_modulo(q, kc, vc, tables, lens, scale, Hkv, B, dtype, seqs=None, heads=None):
+    S, Hq, D = q.shape
+    out = np.zeros((S, Hq, D))
+    q64 = opa.upcast(q, dtype)
+    for s in range(S):
+        for h in range(Hq):
+            kvh = h % Hkv                                  # wrong group map
+            K = opa.gather_kv(kc, tables[s], int(lens[s]), kvh, B, dtype)
+            V = opa.gather_kv(vc, tables[s], int(lens[s]), kvh, B, dtype)
+            out[s, h] = opa.decode_attention_one(q64[s, h], K, V, scale)
+    return out
+
+
+class _NoDecrementOnCow(obm.OracleBlockManager):
+    def _release(self, b):
+        pass
+
+
+class _CowAlways(obm.OracleBlockManager):
+    def append_slot(self, seq):
+        B = self.block_size
+        L = self.lens[seq]
+        table = self.tables[seq]
+        lb = L // B
+        cow = None
+        if lb == len(table):
+            table.append(self._take())
+        elif self.ref[table[lb]] >= 1:                     # copies even when sole holder
+            src, dst = table[lb], self._take()
+            self._release(src)
+            table[lb] = dst
+            cow = (src, dst)
+        self.lens[seq] = L + 1
+        return table[lb] * B + (L - lb * B), cow
+
+
+PIN_TESTS = [
+    tp.test_p4_block_table_example,
+    tp.test_p2_seven_token_prompt_on_demand_append,
+    tp.test_p2_fig8_copy_on_write_and_savings,
+    tp.test_p4_cow_figure_tables_refcounts_and_data,
+    tp.test_p2_fragmentation,
+    tp.test_p1_scenario_block_counts,
+    tp.test_kv_bytes_per_token_examples,
+    lambda: tp.test_slot_mapping_is_a_bijection_onto_owned_rows(4),
+    ta.test_bf16_upcast_is_exact,
+    ta.test_single_token_returns_its_value_exactly,
+    ta.test_equal_keys_give_the_mean_value,
+    ta.test_dominant_logit_selects_its_value_without_overflow,
+    lambda: ta.test_pure_python_brute_force(7, 8),
+    lambda: ta.test_oracle_matches_sdpa_fp64("gqa_small", "bf16", 8, 2, 8),
+    ta.test_decode_step_attends_to_the_new_token,
+    ta.test_gqa_query_head_reads_its_group_kv_head,
+]
+
+MUTANTS = {
+    "slot_no_subtract": [("slot_mapping", _slot_no_subtract)],
+    "slot_offset_swapped": [("slot_mapping", _slot_offset_swapped)],
+    "blocks_floor": [("blocks_needed", _blocks_floor)],
+    "attn_no_max": [("decode_attention_one", _attn_no_max)],
+    "attn_no_scale": [("decode_attention_one", _attn_no_scale)],
+    "attn_no_normalise": [("decode_attention_one", _attn_no_normalise)],
+    "attn_keys_as_values": [("decode_attention_one", _attn_keys_as_values)],
+    "gather_wrong_row": [("gather_kv", _gather_head_modulo)],
+    "bf16_wrong_shift": [("upcast", _upcast_bf16_wrong_shift)],
+    "gqa_modulo": [("decode_attention", _decode_gqa_modulo)],
+    "cow_no_decrement": [("OracleBlockManager", _NoDecrementOnCow)],
+    "cow_always": [("OracleBlockManager", _CowAlways)],
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, monkeypatch):
+    for attr, fn in MUTANTS[name]:
+        for mod in (oracle, opa, obm, tp):
+            if hasattr(mod, attr):
+                monkeypatch.setattr(mod, attr, fn)
+    caught = []
+    with np.errstate(all="ignore"):
+        for t in PIN_TESTS:
+            try:
+                t()
+            except Exception:
+                caught.append(getattr(t, "__name__", "lambda"))
+    assert caught, f"mutant {name} survived every pin"
