@@ -1,0 +1,496 @@
+"""Benchmark of the paged-KV decode step on GB300.
+
+One step = the whole hot path over one batch: slot mapping of the new tokens,
+the KV write (reshape_and_cache), and paged decode attention (with its split
+combine when the partitioning uses more than one partition). Copy-on-write
+block copies run only when a write hits a shared block, which the Llama-7B
+batch never does; the shared-prefix workload exercises them (--config
+shared_prefix).
+
+Prints one JSON line (rank 0). `value` is KV-read GB/s over the whole step
+(algorithmic bytes: sum_s L_s * 2 * Hkv * D * elt, valid tokens only) with
+inputs resident in HBM; `e2e` is the same metric with the per-step inputs
+copied from pinned host memory and the output copied back inside the timed
+region; `roofline` is for the attention launch alone.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                       [--impl ours|reference]
+For N > 1 launch under torch.distributed.run; each rank runs an independent
+replica of the workload (the decode step shards by sequence with no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn: KV-read GB/s vs HBM peak; seq-tokens/s at Llama-7B shape"
+FALLBACK_HBM_GBS = 6800.0
+ELT = {"f32": 4, "f16": 2, "bf16": 2}
+CSRC = os.path.join(ROOT, "paged_kv_cache_123_gb300", "csrc")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--config", default="llama7b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+def kv_read_bytes(seq_lens, num_kv_heads, head_size, elt):
+    """Algorithmic KV bytes one attention launch must read."""
+    return int(sum(int(L) for L in seq_lens)) * 2 * num_kv_heads * head_size * elt
+
+
+def kernel_sources_digest():
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    try:
+        rows = open(PROFILE_TRAFFIC).read().split("\n")
+    except OSError:
+        return None
+    digest = kernel_sources_digest()
+    for r in rows:
+        parts = r.split()
+        if len(parts) == 3 and parts[0] == config and parts[1] == digest:
+            return int(parts[2])
+    return None
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples tagged with host time, so the ones inside the timed
+    window can be picked out."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id is not None:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if len(inside) < 2:
+            inside = [s for t, s in self.samples if t <= t1]
+            window = "warmup+timed"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
+        mx = [num(s[1]) for s in inside if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4)
+                          if len(s) > 4 + i and s[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------- oracle (CPU) timing
+_ORC = {}
+
+
+def _orc_init(spec):
+    # runs in spawned worker processes: map the shared input files read-only
+    import numpy as np
+    for k, (path, shape, dt) in spec.items():
+        _ORC[k] = np.memmap(path, dtype=np.dtype(dt), mode="r", shape=shape)
+
+
+def _orc_run(job):
+    import oracle
+    seqs, scale, hkv, bs, dtype = job
+    A = _ORC
+    oracle.decode_attention(A["q"], A["kc"], A["vc"], A["tables"], A["lens"], scale, hkv, bs,
+                            dtype, seqs=seqs)
+    return len(seqs)
+
+
+class OracleTimer:
+    """The CPU oracle, as it stands, over a spawn pool of single-threaded
+    workers that map the inputs from files in a temporary directory. `arrays` are numpy
+    copies of the step's inputs taken before any kernel ran."""
+
+    def __init__(self, arrays, cfg, scale, workers):
+        import multiprocessing as mp
+        import tempfile
+
+        import numpy as np
+        self.cfg, self.scale, self.workers = cfg, scale, workers
+        self.lens = [int(x) for x in arrays["lens"].tolist()]
+        self.dir = tempfile.mkdtemp(prefix="pa_oracle_")
+        spec = {}
+        for k, a in arrays.items():
+            path = os.path.join(self.dir, k + ".bin")
+            mm = np.memmap(path, dtype=a.dtype, mode="w+", shape=a.shape)
+            mm[...] = a
+            mm.flush()
+            del mm
+            spec[k] = (path, a.shape, a.dtype.str)
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
+        self.pool = mp.get_context("spawn").Pool(workers, initializer=_orc_init, initargs=(spec,))
+        self.sample = None
+
+    def run(self, seqs):
+        cfg = self.cfg
+        chunks = [seqs[i::self.workers] for i in range(self.workers)]
+        jobs = [(c, self.scale, cfg.num_kv_heads, cfg.block_size, cfg.dtype)
+                for c in chunks if c]
+        t0 = time.perf_counter()
+        self.pool.map(_orc_run, jobs)
+        return time.perf_counter() - t0
+
+    def size_sample(self, budget_s):
+        """First n sequences whose oracle time is about budget_s."""
+        lens, w = self.lens, self.workers
+        probe = list(range(min(len(lens), w)))
+        self.run(probe)                      # warm the workers
+        dt = self.run(probe)
+        per_tok = dt * w / max(1, sum(lens[i] for i in probe))
+        want_tok = budget_s * w / max(per_tok, 1e-12)
+        n, tok = 0, 0
+        while n < len(lens) and (tok < want_tok or n < w):
+            tok += lens[n]
+            n += 1
+        self.sample = list(range(n))
+        return self.sample
+
+    def measure(self):
+        """(GB/s, seq-tokens/s, description, seconds) on the sized sample."""
+        cfg = self.cfg
+        dt = self.run(self.sample)
+        sl = [self.lens[i] for i in self.sample]
+        byts = kv_read_bytes(sl, cfg.num_kv_heads, cfg.head_size, ELT[cfg.dtype])
+        desc = (f"first {len(sl)} of {len(self.lens)} sequences of the {cfg.name} batch, "
+                f"all {cfg.num_q_heads} query heads ({sum(sl)} context tokens)")
+        return byts / dt / 1e9, sum(sl) / dt, desc, dt
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        import shutil
+        shutil.rmtree(self.dir, ignore_errors=True)
+
+
+def np_(t):
+    """Storage-typed numpy copy of a tensor (bf16 as uint16 bit patterns)."""
+    import numpy as np
+    import torch
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def oracle_arrays(inp):
+    return {"q": np_(inp.q), "kc": np_(inp.key_cache), "vc": np_(inp.value_cache),
+            "tables": np_(inp.block_tables), "lens": np_(inp.seq_lens)}
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------ distributed
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return dist.get_rank(), world
+    return 0, 1
+
+
+def max_over_ranks(x, world):
+    """Max of a host float over ranks (a timing reduction; the decode data
+    path itself has no exchange)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- arms
+def reference_arm(args):
+    """The oracle as the reference arm: CPU fp64, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from paged_kv_cache_123_gb300 import workloads
+    inp = workloads.make_decode_inputs(args.config, device="cpu")
+    workers = host_cores()
+    timer = OracleTimer(oracle_arrays(inp), inp.cfg, inp.scale, workers)
+    try:
+        timer.size_sample(max(0.5, 120.0 / max(1, args.steps + args.warmup)))
+        gbs_list, tps_list, dts = [], [], []
+        desc = ""
+        for i in range(args.warmup + args.steps):
+            gbs, tps, desc, dt = timer.measure()
+            if i >= args.warmup:
+                gbs_list.append(gbs)
+                tps_list.append(tps)
+                dts.append(dt)
+    finally:
+        timer.close()
+    value = statistics.median(gbs_list)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.median(dts), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "seq_tokens_per_s": round(statistics.median(tps_list), 1),
+        "config": {"workload": args.config, "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": workers,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def ours_arm(args):
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_123_gb300 as pa
+    from paged_kv_cache_123_gb300 import workloads
+
+    rank, world = dist_setup(args)
+    if world == 1:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    props = torch.cuda.get_device_properties(dev)
+    cfg = workloads.CONFIGS[args.config]
+    inp = workloads.make_decode_inputs(cfg, device=str(dev), seed=cfg.seed + rank)
+    B, Hkv, D = cfg.block_size, cfg.num_kv_heads, cfg.head_size
+    elt = inp.q.element_size()
+    S = cfg.num_seqs
+    lens = inp.seq_lens.cpu()
+    kv_bytes = kv_read_bytes(lens.tolist(), Hkv, D, elt)
+    tokens = int(lens.sum())
+    max_len = inp.max_seq_len
+    splits, ptoks = pa.pa_decode_partitioning(S, Hkv, B, max_len, 0)
+    ws_bytes = pa.pa_decode_workspace_bytes(S, cfg.num_q_heads, Hkv, D, B, max_len, 0)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(inp.q)
+    slots = torch.empty(S, dtype=torch.int64, device=dev)
+    g = dict(q=inp.q, k_new=inp.k_new, v_new=inp.v_new, tables=inp.block_tables,
+             lens=inp.seq_lens, pos=inp.positions, qsl=inp.query_start_loc)
+    stream = torch.cuda.current_stream()
+
+    def step(t, ev=None):
+        pa.pa_compute_slot_mapping(t["qsl"], t["pos"], t["tables"], B, slot_mapping=slots)
+        pa.pa_reshape_and_cache(t["k_new"], t["v_new"], slots, inp.key_cache, inp.value_cache)
+        if ev is not None:
+            ev[0].record(stream)
+        pa.pa_decode_attention(t["q"], inp.key_cache, inp.value_cache, t["tables"], t["lens"],
+                               inp.scale, Hkv, out, max_seq_len=max_len, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    launches_per_step = 3 + (1 if splits > 1 else 0)
+    # host copies for the CPU baseline, taken before any kernel touches the pools
+    orc_arrays = oracle_arrays(inp) if (rank == 0 and world == 1
+                                        and not args.no_cpu_baseline) else None
+    for _ in range(max(3, args.warmup)):
+        step(g)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_host0 = time.monotonic()
+    start.record(stream)
+    for i in range(args.steps):
+        step(g, evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.monotonic()
+    barrier(world)
+    if sampler is not None:
+        time.sleep(0.25)
+        sampler.stop()
+    ms_local = start.elapsed_time(stop)
+    ms_total = max_over_ranks(ms_local, world)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    assert pa.pa_get_device_error() == 0
+
+    # e2e: per-step inputs from pinned host memory, output back to host
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.cpu().pin_memory() for k, v in g.items()}
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dbuf = {k: torch.empty_like(v) for k, v in g.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            for k in host:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            step(dbuf)
+            out_host.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+        e2e = {"value": round(world * kv_bytes * args.steps / e2e_s / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "seq_tokens_per_s": round(world * tokens * args.steps / e2e_s, 1)}
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
+    step_s = ms_total * 1e-3 / args.steps
+    value = world * kv_bytes / step_s / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * step_s, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg.dtype, "accum_dtype": "f32", "data": "synthetic",
+        "seq_tokens_per_s": round(world * tokens / step_s, 1),
+        "config": {
+            "workload": cfg.name,
+            "shape": f"{S} seqs, ctx U[{cfg.ctx_lo},{cfg.ctx_hi}]+1 new token, "
+                     f"{cfg.num_q_heads}q/{Hkv}kv heads, D={D}, B={B}, {cfg.dtype}"
+            if cfg.ctx_fixed is None else f"{S} seqs x {cfg.ctx_fixed[0]}+1, "
+                                          f"{cfg.num_q_heads}q/{Hkv}kv heads, D={D}, B={B}",
+            "context_tokens": tokens, "kv_read_bytes_per_step": kv_bytes,
+            "pool_blocks": inp.num_blocks, "partitions": splits, "partition_tokens": ptoks,
+            "l2": "inputs larger than L2 (KV pool %.2f GB >> 129 MB L2), no flush" %
+                  (2 * inp.key_cache.numel() * elt / 1e9),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": {"bound": "hbm", "kernel": "pa_decode_attention",
+                     "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(cfg.name),
+                     "avg_launch_us": round(attn_ms * 1e3, 2),
+                     "algorithmic_bytes_per_launch": kv_bytes},
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e,
+        "clocks": sampler.summary(t_host0, t_host1) if sampler else None,
+        "device": props.name,
+    }
+    if orc_arrays is not None:
+        workers = host_cores()
+        timer = OracleTimer(orc_arrays, cfg, inp.scale, workers)
+        try:
+            timer.size_sample(args.cpu_baseline_seconds)
+            gbs, tps, desc, dt = timer.measure()
+        finally:
+            timer.close()
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": workers,
+                                "kind": "oracle", "sample": desc,
+                                "seq_tokens_per_s": round(tps, 1), "seconds": round(dt, 2)}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        ours_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,222 @@
+/*
+ * pagedattn.h — C ABI of libpagedattn.so, the paged-KV decode hot path for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method (PagedAttention): a sequence's key/value cache is cut into
+ * fixed-size blocks of B tokens that may sit anywhere in a preallocated
+ * physical pool; a per-request block table maps logical block i to its
+ * physical block, and the attention kernel reads the cache only through that
+ * table.  Sources, by page title:
+ *   [P1] "PagedAttention 核心创新深度分析" (openeuler.csdn.net)
+ *   [P2] "Visual reading: paged-attention-kv-cache" (blog.vllbc.top)
+ *   [P3] "vLLM 的 PagedAttention：显存管理如何撑起大模型推理" (deepsonar.com.cn)
+ *   [P4] "Infra: PagedAttention" (pufanyi.com)
+ *
+ * Conventions shared by every call
+ *   - All data pointers are DEVICE pointers unless a parameter says "host".
+ *     The caller owns every buffer; the library keeps no per-call state and
+ *     never allocates device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Every call is asynchronous on that stream; a return of PA_OK
+ *     means the arguments were valid and the kernels were launched.
+ *   - Tensors are dense row-major in the shapes given below.
+ *   - Physical KV pool layout (one pool for K, one for V):
+ *         cache[num_blocks][num_kv_heads][block_size][head_size]
+ *     A slot id s names block s / block_size, row s % block_size.  Every
+ *     (block, kv head) slice is one contiguous run of block_size*head_size
+ *     elements.
+ *   - dtype codes: PA_F32, PA_F16, PA_BF16. q, k, v, caches and out share
+ *     one dtype. Attention arithmetic is fp32.
+ *   - Supported shapes: slot mapping and the KV write take any block_size
+ *     >= 1 and any head_size whose row is a multiple of 16 bytes. Attention
+ *     takes head_size in {64, 128}, block_size a power of two in [1, 256],
+ *     and num_q_heads a multiple of num_kv_heads with group size
+ *     num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ *   - Device pointers must be 16-byte aligned (PA_ERR_ALIGN otherwise).
+ *   - Kernels check every index they read from device memory (block ids,
+ *     positions, slots, sequence lengths) before using it. A bad value is
+ *     never dereferenced: the affected item is skipped (slot mapping writes
+ *     -1; attention writes zeros for a sequence whose length is out of range
+ *     and leaves out a token whose block id is outside the pool) and an
+ *     error code is latched in a device-side word; read and clear it with
+ *     pa_get_device_error().
+ */
+#ifndef PAGEDATTN_H_
+#define PAGEDATTN_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ----------------------------------------------------- */
+#define PA_OK                0
+#define PA_ERR_NULL         (-1)  /* a required pointer is NULL */
+#define PA_ERR_SHAPE        (-2)  /* unsupported or inconsistent size */
+#define PA_ERR_DTYPE        (-3)  /* unknown dtype code */
+#define PA_ERR_WORKSPACE    (-4)  /* workspace missing or too small */
+#define PA_ERR_OUT_OF_RANGE (-5)  /* an index is outside its array */
+#define PA_ERR_CUDA         (-6)  /* a CUDA runtime call or launch failed */
+#define PA_ERR_ALIAS        (-7)  /* copy pairs overlap (dst repeated, or dst is a src) */
+#define PA_ERR_ALIGN        (-8)  /* a device pointer is not 16-byte aligned */
+#define PA_ERR_DEVICE       (-9)  /* no usable sm_103 device / kernel image */
+
+/* ---- dtype codes -------------------------------------------------------- */
+#define PA_F32  0
+#define PA_F16  1
+#define PA_BF16 2
+
+/* Human-readable name of a status code (static string, never NULL). */
+PA_API const char* pa_status_string(int status);
+
+/* Library ABI version; bumps whenever a signature or layout changes. */
+PA_API int pa_abi_version(void);
+
+/*
+ * pa_compute_slot_mapping — [P1] §2.3 BlockTable / slot-mapping kernel (the
+ * single-rank case: no context parallelism, so every token is local).
+ *
+ * For every token t of request r, i.e. query_start_loc[r] <= t <
+ * query_start_loc[r+1]:
+ *     lb = positions[t] / block_size                 (logical block)
+ *     slot_mapping[t] = block_table[r*block_table_stride + lb] * block_size
+ *                       + positions[t] % block_size
+ *
+ * query_start_loc    int32 [num_reqs + 1], non-decreasing, device.
+ * positions          int64 [num_tokens], device.
+ * block_table        int32 [num_reqs][block_table_stride], device; row r
+ *                    lists request r's physical block ids in logical order.
+ * slot_mapping       int64 [num_tokens], device, written.
+ * Tokens that belong to no request get -1 (PAD). A token whose position is
+ * negative, whose logical block is >= block_table_stride, or whose table
+ * entry is negative also gets -1 and latches PA_ERR_OUT_OF_RANGE on the
+ * device.  num_tokens == 0 or num_reqs == 0 is valid (no launch, or all PAD).
+ */
+PA_API int pa_compute_slot_mapping(const int32_t* query_start_loc, int num_reqs,
+                            const int64_t* positions, int64_t num_tokens,
+                            const int32_t* block_table,
+                            int64_t block_table_stride, int block_size,
+                            int64_t* slot_mapping, void* stream);
+
+/*
+ * pa_reshape_and_cache — write the new tokens' keys and values into the pool
+ * at the slots the slot mapping produced ([P1] §2.3: the slot mapping lets
+ * the attention kernel address the pool directly).
+ *
+ * k, v          [num_tokens][num_kv_heads][head_size], dtype, device.
+ * slot_mapping  int64 [num_tokens], device. slot < 0 (PAD) is skipped;
+ *               slot >= num_blocks*block_size is skipped and latches
+ *               PA_ERR_OUT_OF_RANGE.
+ * key_cache, value_cache  the pools (layout above), device, updated in place.
+ * Two tokens mapped to the same slot is a caller error (last writer is
+ * unspecified).
+ */
+PA_API int pa_reshape_and_cache(const void* k, const void* v, int64_t num_tokens,
+                         int num_kv_heads, int head_size, int dtype,
+                         const int64_t* slot_mapping, void* key_cache,
+                         void* value_cache, int64_t num_blocks,
+                         int block_size, void* stream);
+
+/*
+ * Scratch needed by pa_decode_attention for the same arguments
+ * (bytes; 0 means no workspace is needed and NULL may be passed).
+ * partition_size as in pa_decode_attention. Returns a negative status on
+ * invalid sizes.
+ */
+PA_API int64_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_size,
+                                  int block_size, int max_seq_len,
+                                  int partition_size);
+
+/*
+ * Number of context partitions ("splits") pa_decode_attention uses per
+ * sequence of length max_seq_len, and the partition length in tokens that
+ * it resolves partition_size to. Either output pointer (host) may be NULL.
+ */
+PA_API int pa_decode_partitioning(int num_seqs, int num_kv_heads, int block_size,
+                           int max_seq_len, int partition_size,
+                           int* num_splits_out, int* partition_tokens_out);
+
+/*
+ * pa_decode_attention — paged decode attention: one query token per sequence
+ * attends over that sequence's cached tokens, read block by block through
+ * its block table ([P2] block-wise attention and block table section; [P3]
+ * §2.2 and §2.6; [P4] "按 Block 分配"). Paging keeps dense semantics ([P4]
+ * closing section), so for each sequence s and query head h, with KV head
+ * kvh = h / (num_q_heads / num_kv_heads) and L = seq_lens[s]:
+ *     x_j = scale * <q[s,h], K_s[j]>          j < L
+ *     out[s,h] = sum_j softmax(x)_j * V_s[j]
+ * where K_s[j] is row j % B of KV head kvh in physical block
+ * block_tables[s*block_tables_stride + j / B].
+ *
+ * q, out        [num_seqs][num_q_heads][head_size], dtype, device.
+ * key_cache, value_cache  pools (layout above), device.
+ * block_tables  int32 [num_seqs][block_tables_stride], device.
+ * seq_lens      int32 [num_seqs], device; 0 <= seq_lens[s] <= max_seq_len and
+ *               <= block_tables_stride*block_size. A length outside that
+ *               range latches PA_ERR_OUT_OF_RANGE and yields zeros; a length
+ *               of 0 yields zeros (attention over nothing).
+ * max_seq_len   host upper bound of seq_lens, used to size the grid.
+ * partition_size  tokens per context partition (split-K over block ranges,
+ *               with a log-sum-exp combine), rounded up to a multiple of
+ *               max(64, block_size); 0 picks a size from the SM count and the
+ *               problem shape.
+ * workspace     device scratch of pa_decode_workspace_bytes(...) bytes (may
+ *               be NULL when that is 0). Contents on entry are ignored.
+ * Accumulation is fp32; out is rounded to nearest in the q dtype. Results
+ * are bitwise reproducible for fixed arguments and do not depend on where
+ * blocks sit in the pool.
+ */
+PA_API int pa_decode_attention(const void* q, const void* key_cache,
+                        const void* value_cache, const int32_t* block_tables,
+                        int64_t block_tables_stride, const int32_t* seq_lens,
+                        int num_seqs, int num_q_heads, int num_kv_heads,
+                        int head_size, int block_size, int64_t num_blocks,
+                        int dtype, float scale, int max_seq_len,
+                        int partition_size, void* out, void* workspace,
+                        int64_t workspace_bytes, void* stream);
+
+/*
+ * pa_copy_blocks — block-level copy-on-write data movement ([P2] Figure 8:
+ * "copy physical block 1's content to physical block 3"; [P4] copy-on-write
+ * figure). For every pair (src, dst) in src_dst_pairs and every layer l, the
+ * whole K block src of key_caches[l] is copied to block dst, and likewise for
+ * value_caches[l].
+ *
+ * key_caches, value_caches  HOST arrays of num_layers device pointers, one
+ *               pool per layer, each [num_blocks][...] with block_bytes bytes
+ *               per block (num_kv_heads*block_size*head_size*elt).
+ * src_dst_pairs int64 [num_pairs][2], device.
+ * src_dst_pairs_host  optional HOST copy of the same pairs (may be NULL). When
+ *               given, ids are range-checked and aliasing (a repeated dst, or
+ *               a dst that is also a src) is rejected with PA_ERR_ALIAS before
+ *               anything is launched. Without it the kernel range-checks each
+ *               pair (skipping and latching PA_ERR_OUT_OF_RANGE) and aliasing
+ *               is the caller's responsibility.
+ * block_bytes   a positive multiple of 16.
+ */
+PA_API int pa_copy_blocks(void* const* key_caches, void* const* value_caches,
+                   int num_layers, const int64_t* src_dst_pairs,
+                   const int64_t* src_dst_pairs_host, int64_t num_pairs,
+                   int64_t num_blocks, int64_t block_bytes, void* stream);
+
+/*
+ * Read (and clear) the device-side error word that the kernels latch on bad
+ * indices. Synchronises `stream` first. *code_out receives PA_OK or the
+ * first latched error (PA_ERR_OUT_OF_RANGE). The word is per device and
+ * shared by all streams.
+ */
+PA_API int pa_get_device_error(int* code_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H_ */

@@ -1,0 +1,15 @@
+"""paged_kv_cache_123_gb300 — PagedAttention's decode hot path on GB300.
+
+The KV cache lives in fixed-size blocks anywhere in a physical pool and each
+sequence reaches its blocks only through a block table. The work runs in
+hand-written CUDA kernels for sm_103a behind the C ABI of libpagedattn.so
+(include/pagedattn.h); this package is the thin Python binding (same names
+as the C entry points), the host-side block bookkeeping and the seeded input
+generators.
+"""
+from .ops import (  # noqa: F401
+    pa_compute_slot_mapping, pa_reshape_and_cache, pa_decode_workspace_bytes,
+    pa_decode_partitioning, pa_decode_attention, pa_copy_blocks, pa_get_device_error,
+)
+from ._lib import PagedAttnError, LIB_PATH, lib  # noqa: F401
+from .block_pool import BlockPool  # noqa: F401

@@ -1,0 +1,305 @@
+// C ABI of libpagedattn.so: argument validation, partition sizing and kernel
+// launch. Declarations and their contracts are in include/pagedattn.h.
+#include <algorithm>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "launchers.h"
+
+// Device-side error word latched by the kernels on bad indices.
+static __device__ int g_pa_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+int g_dev_status[kMaxDevices];
+
+// Per-device set-up, run once with that device current: the address of the
+// error word, its initial clear, and the SM count.
+int device_setup(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return PA_ERR_DEVICE;
+  std::call_once(g_dev_once[dev], [dev]() {
+    int st = PA_OK;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pa_device_error) != cudaSuccess) st = PA_ERR_DEVICE;
+    int zero = 0;
+    if (st == PA_OK && cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      st = PA_ERR_DEVICE;
+    int sms = 0;
+    if (st == PA_OK &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      st = PA_ERR_DEVICE;
+    g_err_ptr[dev] = static_cast<int*>(p);
+    g_sm_count[dev] = sms > 0 ? sms : 1;
+    g_dev_status[dev] = st;
+  });
+  *dev_out = dev;
+  return g_dev_status[dev];
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int elt_bytes(int dtype) {
+  switch (dtype) {
+    case PA_F32: return 4;
+    case PA_F16: return 2;
+    case PA_BF16: return 2;
+  }
+  return 0;
+}
+
+int check_launch(cudaError_t e) {
+  if (e == cudaSuccess) return PA_OK;
+  if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+    return PA_ERR_DEVICE;
+  return PA_ERR_CUDA;
+}
+
+// Tokens per context partition and the partition count for a batch whose
+// longest sequence is max_seq_len. Partitions are whole multiples of
+// max(64, block_size) tokens so every partition starts on a block boundary
+// and on a 64-token tile. With partition_size == 0 the count is chosen so
+// that (sequences x KV heads x partitions) gives several CTAs per SM, with
+// partitions no shorter than 512 tokens.
+void partitioning(int num_seqs, int num_kv_heads, int block_size, int max_seq_len,
+                  int partition_size, int sm_count, int* splits, int* tokens) {
+  const int64_t tile = block_size > 64 ? block_size : 64;
+  const int64_t len = max_seq_len > 0 ? max_seq_len : 1;
+  int64_t P;
+  if (partition_size > 0) {
+    P = ((int64_t)partition_size + tile - 1) / tile * tile;
+  } else {
+    const int64_t pairs = (int64_t)num_seqs * num_kv_heads;
+    const int64_t target = (int64_t)sm_count * 8;
+    int64_t want = pairs > 0 ? (target + pairs - 1) / pairs : 1;
+    if (want < 1) want = 1;
+    P = (len + want - 1) / want;
+    P = (P + tile - 1) / tile * tile;
+    const int64_t minP = (512 + tile - 1) / tile * tile;
+    if (P < minP) P = minP;
+  }
+  if (P > len) P = (len + tile - 1) / tile * tile;
+  if (P > (int64_t)1 << 30) P = (int64_t)1 << 30;
+  *tokens = (int)P;
+  *splits = (int)((len + P - 1) / P);
+}
+
+int64_t workspace_for(int num_seqs, int num_q_heads, int head_size, int splits) {
+  if (splits <= 1) return 0;
+  const int64_t n = (int64_t)num_seqs * num_q_heads * splits;
+  const int64_t acc = n * head_size * 4;
+  const int64_t ml = n * 2 * 4;
+  return ((acc + 255) / 256) * 256 + ml;
+}
+
+int check_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+                       int block_size, int max_seq_len) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0)
+    return PA_ERR_SHAPE;
+  if (head_size != 64 && head_size != 128) return PA_ERR_SHAPE;
+  if (!pow2(block_size) || block_size > 256) return PA_ERR_SHAPE;
+  if (num_q_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
+  const int g = num_q_heads / num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return PA_ERR_SHAPE;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_SHAPE;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL: return "a required pointer is NULL";
+    case PA_ERR_SHAPE: return "unsupported or inconsistent size";
+    case PA_ERR_DTYPE: return "unknown dtype code";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_OUT_OF_RANGE: return "an index is outside its array";
+    case PA_ERR_CUDA: return "CUDA runtime call or launch failed";
+    case PA_ERR_ALIAS: return "copy pairs overlap";
+    case PA_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case PA_ERR_DEVICE: return "no usable sm_103 device or kernel image";
+  }
+  return "unknown status";
+}
+
+int pa_abi_version(void) { return 1; }
+
+int pa_compute_slot_mapping(const int32_t* query_start_loc, int num_reqs,
+                            const int64_t* positions, int64_t num_tokens,
+                            const int32_t* block_table, int64_t block_table_stride,
+                            int block_size, int64_t* slot_mapping, void* stream) {
+  if (num_reqs < 0 || num_tokens < 0 || block_size <= 0 || block_table_stride < 0)
+    return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!query_start_loc || !positions || !slot_mapping) return PA_ERR_NULL;
+  if (num_reqs > 0 && !block_table) return PA_ERR_NULL;
+  int dev;
+  int st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  return check_launch(pa::launch_slot_mapping(
+      query_start_loc, num_reqs, positions, num_tokens, block_table,
+      block_table_stride, block_size, slot_mapping, (cudaStream_t)stream, g_err_ptr[dev]));
+}
+
+int pa_reshape_and_cache(const void* k, const void* v, int64_t num_tokens,
+                         int num_kv_heads, int head_size, int dtype,
+                         const int64_t* slot_mapping, void* key_cache,
+                         void* value_cache, int64_t num_blocks, int block_size,
+                         void* stream) {
+  const int eb = elt_bytes(dtype);
+  if (eb == 0) return PA_ERR_DTYPE;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
+      num_blocks < 0)
+    return PA_ERR_SHAPE;
+  if (((int64_t)head_size * eb) % 16 != 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !key_cache || !value_cache) return PA_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache))
+    return PA_ERR_ALIGN;
+  int dev;
+  int st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  return check_launch(pa::launch_reshape_and_cache(
+      k, v, num_tokens, num_kv_heads, head_size * eb, slot_mapping, key_cache,
+      value_cache, num_blocks, block_size, (cudaStream_t)stream, g_err_ptr[dev]));
+}
+
+int pa_decode_partitioning(int num_seqs, int num_kv_heads, int block_size,
+                           int max_seq_len, int partition_size,
+                           int* num_splits_out, int* partition_tokens_out) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || !pow2(block_size) || block_size > 256 ||
+      max_seq_len < 0 || partition_size < 0)
+    return PA_ERR_SHAPE;
+  int dev;
+  int st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  int splits, tokens;
+  partitioning(num_seqs, num_kv_heads, block_size, max_seq_len, partition_size,
+               g_sm_count[dev], &splits, &tokens);
+  if (num_splits_out) *num_splits_out = splits;
+  if (partition_tokens_out) *partition_tokens_out = tokens;
+  return PA_OK;
+}
+
+int64_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                  int head_size, int block_size, int max_seq_len,
+                                  int partition_size) {
+  int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size,
+                              block_size, max_seq_len);
+  if (st != PA_OK) return st;
+  if (partition_size < 0) return PA_ERR_SHAPE;
+  int splits, tokens;
+  st = pa_decode_partitioning(num_seqs, num_kv_heads, block_size, max_seq_len,
+                              partition_size, &splits, &tokens);
+  if (st != PA_OK) return st;
+  return workspace_for(num_seqs, num_q_heads, head_size, splits);
+}
+
+int pa_decode_attention(const void* q, const void* key_cache, const void* value_cache,
+                        const int32_t* block_tables, int64_t block_tables_stride,
+                        const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                        int num_kv_heads, int head_size, int block_size,
+                        int64_t num_blocks, int dtype, float scale, int max_seq_len,
+                        int partition_size, void* out, void* workspace,
+                        int64_t workspace_bytes, void* stream) {
+  if (elt_bytes(dtype) == 0) return PA_ERR_DTYPE;
+  int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size,
+                              block_size, max_seq_len);
+  if (st != PA_OK) return st;
+  if (partition_size < 0 || num_blocks < 0 || block_tables_stride < 0) return PA_ERR_SHAPE;
+  if ((int64_t)max_seq_len > block_tables_stride * block_size) return PA_ERR_OUT_OF_RANGE;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !key_cache || !value_cache || !block_tables || !seq_lens || !out)
+    return PA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) || !aligned16(out))
+    return PA_ERR_ALIGN;
+  int dev;
+  st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  pa::DecodeArgs a;
+  a.q = q; a.kc = key_cache; a.vc = value_cache;
+  a.tables = block_tables; a.table_stride = block_tables_stride; a.seq_lens = seq_lens;
+  a.num_seqs = num_seqs; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size; a.block_size = block_size; a.num_blocks = num_blocks;
+  a.dtype = dtype; a.scale = scale; a.max_seq_len = max_seq_len;
+  partitioning(num_seqs, num_kv_heads, block_size, max_seq_len, partition_size,
+               g_sm_count[dev], &a.num_splits, &a.partition);
+  const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);
+  a.ws_acc = nullptr; a.ws_ml = nullptr;
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PA_ERR_ALIGN;
+    const int64_t n = (int64_t)num_seqs * num_q_heads * a.num_splits;
+    a.ws_acc = static_cast<float*>(workspace);
+    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       ((n * head_size * 4 + 255) / 256) * 256);
+  }
+  a.out = out;
+  a.err = g_err_ptr[dev];
+  return check_launch(pa::launch_decode(a, (cudaStream_t)stream));
+}
+
+int pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
+                   const int64_t* src_dst_pairs, const int64_t* src_dst_pairs_host,
+                   int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
+                   void* stream) {
+  if (num_layers < 0 || num_pairs < 0 || num_blocks < 0) return PA_ERR_SHAPE;
+  if (block_bytes <= 0 || block_bytes % 16 != 0) return PA_ERR_SHAPE;
+  if (num_pairs == 0 || num_layers == 0) return PA_OK;
+  if (!key_caches || !value_caches || !src_dst_pairs) return PA_ERR_NULL;
+  for (int l = 0; l < num_layers; ++l) {
+    if (!key_caches[l] || !value_caches[l]) return PA_ERR_NULL;
+    if (!aligned16(key_caches[l]) || !aligned16(value_caches[l])) return PA_ERR_ALIGN;
+  }
+  if (src_dst_pairs_host) {
+    // ranges, then aliasing: sort-free O(P log P) via a sorted copy
+    std::vector<int64_t> d, s;
+    d.reserve(num_pairs); s.reserve(num_pairs);
+    for (int64_t i = 0; i < num_pairs; ++i) {
+      const int64_t a = src_dst_pairs_host[2 * i], b = src_dst_pairs_host[2 * i + 1];
+      if (a < 0 || a >= num_blocks || b < 0 || b >= num_blocks) return PA_ERR_OUT_OF_RANGE;
+      s.push_back(a); d.push_back(b);
+    }
+    std::sort(d.begin(), d.end());
+    std::sort(s.begin(), s.end());
+    for (int64_t i = 1; i < num_pairs; ++i)
+      if (d[i] == d[i - 1]) return PA_ERR_ALIAS;
+    for (int64_t x : d)
+      if (std::binary_search(s.begin(), s.end(), x)) return PA_ERR_ALIAS;
+  }
+  int dev;
+  int st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  return check_launch(pa::launch_copy_blocks(key_caches, value_caches, num_layers,
+                                             src_dst_pairs, num_pairs, num_blocks,
+                                             block_bytes, (cudaStream_t)stream,
+                                             g_err_ptr[dev]));
+}
+
+int pa_get_device_error(int* code_out, void* stream) {
+  if (!code_out) return PA_ERR_NULL;
+  int dev;
+  int st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  int v = 0, zero = 0;
+  if (cudaMemcpyAsync(&v, g_err_ptr[dev], sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaMemcpyAsync(g_err_ptr[dev], &zero, sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  *code_out = v;
+  return PA_OK;
+}
+
+}  // extern "C"

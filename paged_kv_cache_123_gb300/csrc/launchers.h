@@ -1,0 +1,52 @@
+// Host-side launchers for the kernels, one per translation unit. They assume
+// the arguments were validated by the C ABI layer (api.cu) and return a
+// cudaError_t from the launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+cudaError_t launch_slot_mapping(const int32_t* qsl, int num_reqs,
+                                const int64_t* positions, int64_t num_tokens,
+                                const int32_t* table, int64_t stride,
+                                int block_size, int64_t* slots,
+                                cudaStream_t st, int* err);
+
+cudaError_t launch_reshape_and_cache(const void* k, const void* v,
+                                     int64_t num_tokens, int num_kv_heads,
+                                     int row_bytes, const int64_t* slots,
+                                     void* kc, void* vc, int64_t num_blocks,
+                                     int block_size, cudaStream_t st, int* err);
+
+// Up to kCopyMaxLayers layers per launch.
+constexpr int kCopyMaxLayers = 64;
+cudaError_t launch_copy_blocks(void* const* kcs, void* const* vcs,
+                               int num_layers, const int64_t* pairs,
+                               int64_t num_pairs, int64_t num_blocks,
+                               int64_t block_bytes, cudaStream_t st, int* err);
+
+struct DecodeArgs {
+  const void* q;
+  const void* kc;
+  const void* vc;
+  const int32_t* tables;
+  int64_t table_stride;
+  const int32_t* seq_lens;
+  int num_seqs, num_q_heads, num_kv_heads, head_size, block_size;
+  int64_t num_blocks;
+  int dtype;
+  float scale;
+  int max_seq_len;
+  int partition;     // tokens per split (multiple of max(64, block_size))
+  int num_splits;    // ceil(max_seq_len / partition), >= 1
+  void* out;
+  float* ws_acc;     // [S][Hq][num_splits][D]   (num_splits > 1)
+  float* ws_ml;      // [S][Hq][num_splits][2]   (num_splits > 1)
+  int* err;
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+
+}  // namespace pa

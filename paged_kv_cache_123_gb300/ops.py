@@ -1,0 +1,153 @@
+"""Python entry points with the C ABI's names (include/pagedattn.h).
+
+Each function checks that tensors are on the GPU, contiguous and of the right
+integer type, then calls the library on torch's current stream. Shapes and
+sizes are validated by the library itself.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from ._lib import DTYPE_CODE, check, lib, ptr, stream_handle
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def pa_compute_slot_mapping(query_start_loc: torch.Tensor, positions: torch.Tensor,
+                            block_table: torch.Tensor, block_size: int,
+                            slot_mapping: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """slot[t] = block_table[r, pos // B] * B + pos % B for the tokens of each
+    request r; -1 for tokens of no request. Returns int64 [num_tokens]."""
+    _dev(query_start_loc, "query_start_loc", torch.int32)
+    _dev(positions, "positions", torch.int64)
+    _dev(block_table, "block_table", torch.int32)
+    T = positions.numel()
+    if slot_mapping is None:
+        slot_mapping = torch.empty(T, dtype=torch.int64, device=positions.device)
+    _dev(slot_mapping, "slot_mapping", torch.int64)
+    stride = block_table.shape[1] if block_table.dim() == 2 else 0
+    check("pa_compute_slot_mapping", lib().pa_compute_slot_mapping(
+        ptr(query_start_loc), query_start_loc.numel() - 1, ptr(positions), T,
+        ptr(block_table), stride, block_size, ptr(slot_mapping), stream_handle(stream)))
+    return slot_mapping
+
+
+def pa_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                         key_cache: torch.Tensor, value_cache: torch.Tensor,
+                         stream=None) -> None:
+    """Write k[t], v[t] ([T, Hkv, D]) into pool slot slot_mapping[t]; pools are
+    [num_blocks, Hkv, B, D]."""
+    for n, t in (("k", k), ("v", v), ("key_cache", key_cache), ("value_cache", value_cache)):
+        _dev(t, n)
+    _dev(slot_mapping, "slot_mapping", torch.int64)
+    NB, Hkv, B, D = key_cache.shape
+    if value_cache.shape != key_cache.shape or k.shape != v.shape:
+        raise ValueError("shape mismatch")
+    if k.shape[1:] != (Hkv, D) or k.dtype != key_cache.dtype:
+        raise ValueError("k/v must be [T, Hkv, D] in the cache dtype")
+    check("pa_reshape_and_cache", lib().pa_reshape_and_cache(
+        ptr(k), ptr(v), k.shape[0], Hkv, D, DTYPE_CODE[k.dtype], ptr(slot_mapping),
+        ptr(key_cache), ptr(value_cache), NB, B, stream_handle(stream)))
+
+
+def pa_decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                              head_size: int, block_size: int, max_seq_len: int,
+                              partition_size: int = 0) -> int:
+    n = lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                        block_size, max_seq_len, partition_size)
+    if n < 0:
+        check("pa_decode_workspace_bytes", int(n))
+    return int(n)
+
+
+def pa_decode_partitioning(num_seqs: int, num_kv_heads: int, block_size: int,
+                           max_seq_len: int, partition_size: int = 0):
+    """(num_splits, partition_tokens) the attention call will use."""
+    s, p = ctypes.c_int(0), ctypes.c_int(0)
+    check("pa_decode_partitioning", lib().pa_decode_partitioning(
+        num_seqs, num_kv_heads, block_size, max_seq_len, partition_size,
+        ctypes.byref(s), ctypes.byref(p)))
+    return s.value, p.value
+
+
+def pa_decode_attention(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                        block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                        num_kv_heads: int, out: Optional[torch.Tensor] = None, *,
+                        max_seq_len: int, partition_size: int = 0,
+                        workspace: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """Paged decode attention. q/out [S, Hq, D]; pools [NB, Hkv, B, D];
+    block_tables int32 [S, max_blocks]; seq_lens int32 [S]; max_seq_len is a
+    host upper bound of seq_lens."""
+    for n, t in (("q", q), ("key_cache", key_cache), ("value_cache", value_cache)):
+        _dev(t, n)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = key_cache.shape
+    if Hkv != num_kv_heads or Dk != D or value_cache.shape != key_cache.shape:
+        raise ValueError("pool shape does not match q / num_kv_heads")
+    if key_cache.dtype != q.dtype or value_cache.dtype != q.dtype:
+        raise ValueError("q and pools must share a dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out")
+    need = pa_decode_workspace_bytes(S, Hq, Hkv, D, B, max_seq_len, partition_size)
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check("pa_decode_attention", lib().pa_decode_attention(
+        ptr(q), ptr(key_cache), ptr(value_cache), ptr(block_tables), block_tables.shape[1],
+        ptr(seq_lens), S, Hq, Hkv, D, B, NB, DTYPE_CODE[q.dtype], float(scale),
+        int(max_seq_len), int(partition_size), ptr(out), ptr(workspace), ws_bytes,
+        stream_handle(stream)))
+    return out
+
+
+def pa_copy_blocks(key_caches: Sequence[torch.Tensor], value_caches: Sequence[torch.Tensor],
+                   src_dst_pairs: torch.Tensor,
+                   src_dst_pairs_host: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Copy whole blocks src -> dst in every layer's K and V pool.
+    src_dst_pairs: int64 [P, 2] on the GPU; src_dst_pairs_host: optional CPU
+    copy, which enables the aliasing check before launch."""
+    if len(key_caches) != len(value_caches) or not key_caches:
+        raise ValueError("need one K and one V pool per layer")
+    _dev(src_dst_pairs, "src_dst_pairs", torch.int64)
+    kc0 = key_caches[0]
+    for t in list(key_caches) + list(value_caches):
+        _dev(t, "cache")
+        if t.shape != kc0.shape or t.dtype != kc0.dtype:
+            raise ValueError("all pools must share shape and dtype")
+    nl = len(key_caches)
+    kp = (ctypes.c_void_p * nl)(*[t.data_ptr() for t in key_caches])
+    vp = (ctypes.c_void_p * nl)(*[t.data_ptr() for t in value_caches])
+    host = None
+    if src_dst_pairs_host is not None:
+        host = src_dst_pairs_host.to(torch.int64).contiguous()
+        if host.is_cuda or host.numel() != src_dst_pairs.numel():
+            raise ValueError("src_dst_pairs_host must be a CPU copy of the pairs")
+    NB = kc0.shape[0]
+    block_bytes = kc0[0].numel() * kc0.element_size()
+    check("pa_copy_blocks", lib().pa_copy_blocks(
+        kp, vp, nl, ptr(src_dst_pairs), None if host is None else host.data_ptr(),
+        src_dst_pairs.numel() // 2, NB, block_bytes, stream_handle(stream)))
+
+
+def pa_get_device_error(stream=None) -> int:
+    """Synchronise the stream, then read and clear the latched device error
+    (0 = none)."""
+    code = ctypes.c_int(0)
+    check("pa_get_device_error", lib().pa_get_device_error(ctypes.byref(code),
+                                                           stream_handle(stream)))
+    return code.value
