@@ -184,6 +184,43 @@ PA_API int pa_decode_attention(const void* q, const void* key_cache,
                         int64_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_attention_static — the same computation as pa_decode_attention,
+ * for callers that cannot allocate device memory and so cannot pass a
+ * workspace: for example a serving engine that reserved almost all of HBM
+ * for its KV block pool up front, or a host whose policy forbids cudaMalloc
+ * on the decode path (it can synchronise the device). The paper has no
+ * counterpart to this call; it is a convenience of this library.
+ *
+ * Arguments are those of pa_decode_attention without workspace and
+ * workspace_bytes. The split-partition scratch comes from a fixed array of
+ * PA_STATIC_SCRATCH_BYTES bytes inside the library, present on every device
+ * that loads the library until the process exits. The call allocates
+ * nothing.
+ *   - Sizes whose scratch (pa_decode_workspace_bytes) exceeds
+ *     PA_STATIC_SCRATCH_BYTES are refused with PA_ERR_WORKSPACE before any
+ *     launch; use pa_decode_attention with your own workspace for those.
+ *   - The first call on a device looks up that device's address of the
+ *     array (cudaGetSymbolAddress, with the device current); make that
+ *     first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps whatever the
+ *     last call left in it (nothing in it needs to start at zero). Calls
+ *     that may run at the same time on the GPU (different streams without
+ *     ordering between them) race on it: order them on one stream or use
+ *     pa_decode_attention with separate workspaces.
+ */
+#define PA_STATIC_SCRATCH_BYTES (32ll << 20)
+PA_API int pa_decode_attention_static(const void* q, const void* key_cache,
+                                      const void* value_cache,
+                                      const int32_t* block_tables,
+                                      int64_t block_tables_stride,
+                                      const int32_t* seq_lens, int num_seqs,
+                                      int num_q_heads, int num_kv_heads,
+                                      int head_size, int block_size,
+                                      int64_t num_blocks, int dtype, float scale,
+                                      int max_seq_len, int partition_size,
+                                      void* out, void* stream);
+
+/*
  * pa_copy_blocks — block-level copy-on-write data movement ([P2] Figure 8:
  * "copy physical block 1's content to physical block 3"; [P4] copy-on-write
  * figure). For every pair (src, dst) in src_dst_pairs and every layer l, the
