@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--partition", type=int, default=0,
+                    help="tokens per context partition (0 = the library's choice)")
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="use only the first N sequences (smaller profiling case)")
     return ap.parse_args()
 
 
@@ -342,6 +346,11 @@ def ours_arm(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     props = torch.cuda.get_device_properties(dev)
     cfg = workloads.CONFIGS[args.config]
+    if args.num_seqs:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, num_seqs=args.num_seqs, name=f"{cfg.name}_s{args.num_seqs}",
+                                  ctx_fixed=None if cfg.ctx_fixed is None
+                                  else cfg.ctx_fixed[:args.num_seqs])
     inp = workloads.make_decode_inputs(cfg, device=str(dev), seed=cfg.seed + rank)
     B, Hkv, D = cfg.block_size, cfg.num_kv_heads, cfg.head_size
     elt = inp.q.element_size()
@@ -350,8 +359,9 @@ def ours_arm(args):
     kv_bytes = kv_read_bytes(lens.tolist(), Hkv, D, elt)
     tokens = int(lens.sum())
     max_len = inp.max_seq_len
-    splits, ptoks = pa.pa_decode_partitioning(S, Hkv, B, max_len, 0)
-    ws_bytes = pa.pa_decode_workspace_bytes(S, cfg.num_q_heads, Hkv, D, B, max_len, 0)
+    P = args.partition
+    splits, ptoks = pa.pa_decode_partitioning(S, Hkv, B, max_len, P)
+    ws_bytes = pa.pa_decode_workspace_bytes(S, cfg.num_q_heads, Hkv, D, B, max_len, P)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     out = torch.empty_like(inp.q)
     slots = torch.empty(S, dtype=torch.int64, device=dev)
@@ -365,7 +375,8 @@ def ours_arm(args):
         if ev is not None:
             ev[0].record(stream)
         pa.pa_decode_attention(t["q"], inp.key_cache, inp.value_cache, t["tables"], t["lens"],
-                               inp.scale, Hkv, out, max_seq_len=max_len, workspace=ws)
+                               inp.scale, Hkv, out, max_seq_len=max_len, partition_size=P,
+                               workspace=ws)
         if ev is not None:
             ev[1].record(stream)
 

@@ -67,6 +67,7 @@ extern "C" {
 #define PA_ERR_ALIAS        (-7)  /* copy pairs overlap (dst repeated, or dst is a src) */
 #define PA_ERR_ALIGN        (-8)  /* a device pointer is not 16-byte aligned */
 #define PA_ERR_DEVICE       (-9)  /* no usable sm_103 device / kernel image */
+#define PA_ERR_TIMEOUT      (-10) /* a kernel gave up on a stuck asynchronous copy */
 
 /* ---- dtype codes -------------------------------------------------------- */
 #define PA_F32  0

@@ -19,7 +19,7 @@ PA_OK = 0
 STATUS_NAMES = {
     0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_DTYPE",
     -4: "PA_ERR_WORKSPACE", -5: "PA_ERR_OUT_OF_RANGE", -6: "PA_ERR_CUDA",
-    -7: "PA_ERR_ALIAS", -8: "PA_ERR_ALIGN", -9: "PA_ERR_DEVICE",
+    -7: "PA_ERR_ALIAS", -8: "PA_ERR_ALIGN", -9: "PA_ERR_DEVICE", -10: "PA_ERR_TIMEOUT",
 }
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 

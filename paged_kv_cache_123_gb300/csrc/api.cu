@@ -128,6 +128,7 @@ const char* pa_status_string(int status) {
     case PA_ERR_ALIAS: return "copy pairs overlap";
     case PA_ERR_ALIGN: return "device pointer not 16-byte aligned";
     case PA_ERR_DEVICE: return "no usable sm_103 device or kernel image";
+    case PA_ERR_TIMEOUT: return "a kernel gave up waiting on an asynchronous copy";
   }
   return "unknown status";
 }

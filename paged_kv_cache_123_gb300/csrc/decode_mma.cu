@@ -1,0 +1,480 @@
+// Paged decode attention on the tensor cores, for query-head groups (GQA).
+//
+// Same computation as decode_simt.cu ("Visual reading: paged-attention-kv-
+// cache", block-wise attention; "vLLM 的 PagedAttention：显存管理如何撑起大模
+// 型推理" §2.1: the query heads of a group share one KV head). With a group of
+// G query heads per KV head, the per-block work is a dense contraction:
+//     S^T[tokens x heads] = K_blk[tokens x D] * Q^T[D x heads]
+//     O^T[D x heads]     += V_blk^T[D x tokens] * P^T[tokens x heads]
+// so it runs on mma.sync m16n8k16 with the group as the N = 8 side (groups of
+// 2 or 4 are zero-padded) and 16 tokens or 16 head dims as the M side.
+//
+// Data movement: a producer warp walks the partition's block table and issues
+// one 3-D tiled TMA load (cp.async.bulk.tensor) per (block, 64-column half of
+// the head dim) for K and for V into a 3-stage ring of 64-token tiles, with
+// 128-byte swizzle so the ldmatrix reads are bank-conflict free. Four
+// consumer warps take 16 tokens of each tile each, keep their own running
+// softmax state (log2 domain), and free the stage through an mbarrier. Every
+// wait is bounded: a stuck barrier raises an abort flag, the CTA drains and
+// leaves, and PA_ERR_TIMEOUT is latched.
+//
+// Rows past the end of the sequence (the tail of the last block, blocks not
+// loaded) are masked to -inf in S and zeroed in the V tile before the P*V
+// product, so stale or uninitialised pool bytes cannot leak into the output.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "launchers.h"
+#include "tma.cuh"
+
+namespace pa {
+
+constexpr int kMmaConsumers = 4;
+constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
+constexpr int kTile = 64;
+constexpr int kStages = 3;
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+#define kNegInfM (-__int_as_float(0x7f800000))
+
+template <typename T> struct MmaOps;
+
+template <> struct MmaOps<__nv_bfloat16> {
+  static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  __device__ __forceinline__ static void mma(float* c, const uint32_t* a, uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  __device__ __forceinline__ static float2 unpack(uint32_t u) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
+  }
+};
+
+template <> struct MmaOps<__half> {
+  static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  __device__ __forceinline__ static void mma(float* c, const uint32_t* a, uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  __device__ __forceinline__ static float2 unpack(uint32_t u) {
+    return __half22float2(*reinterpret_cast<__half2*>(&u));
+  }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t* r, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t* r, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Address of 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte-swizzled
+// [rows][128 B] tile that starts on a 1024-byte boundary.
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
+  return base + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kMmaThreads, 2)
+decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV) {
+  constexpr int HALVES = D / 64;                 // 128-byte column halves per row
+  constexpr int HALF_BYTES = kTile * 128;        // one half of a 64-token tile
+  constexpr int KV_BYTES = HALVES * HALF_BYTES;  // K (or V) part of a stage
+  constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  constexpr int KSTEPS = D / 16;
+  static_assert(G == 2 || G == 4 || G == 8, "group");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * STAGE_BYTES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
+  // bit p set = piece p of the stage's tile was loaded (written by the
+  // producer before it arms the stage's full barrier)
+  unsigned* tile_mask = reinterpret_cast<unsigned*>(bars + 2 * kStages) + 1;
+  const uint32_t smem0 = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int st) { return bar0 + 8u * st; };
+  auto empty_bar = [&](int st) { return bar0 + 8u * (kStages + st); };
+
+  const int s = blockIdx.z, kvh = blockIdx.y, split = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
+  const int L = a.seq_lens[s];
+  const bool bad_len =
+      L < 0 || L > a.max_seq_len || (int64_t)L > a.table_stride * a.block_size;
+  if (bad_len || L == 0) {
+    if (split == 0) {
+      if (L != 0 && threadIdx.x == 0) latch(a.err, PA_ERR_OUT_OF_RANGE);
+      T* out = reinterpret_cast<T*>(a.out);
+      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+        out[((int64_t)s * Hq + (int64_t)kvh * G) * D + i] = Vec<T>::cvt_out(0.f);
+    }
+    return;
+  }
+  const int t0 = split * a.partition;
+  if (t0 >= L) return;
+  const int t1 = min(L, t0 + a.partition);
+  const int nsplit = (L + a.partition - 1) / a.partition;
+  const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+  const int B = a.block_size;
+  const int bshift = __ffs(B) - 1;
+  const int R = B < kTile ? B : kTile;           // rows per TMA box
+  const int32_t* trow = a.tables + (int64_t)s * a.table_stride;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(full_bar(st), 1);
+      mbar_init(empty_bar(st), kMmaConsumers);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  // merge state, per consumer warp; heads 2c and 2c+1 of this lane
+  float m0 = kNegInfM, m1 = kNegInfM, l0 = 0.f, l1 = 0.f;
+  float o[KSTEPS][4];
+#pragma unroll
+  for (int i = 0; i < KSTEPS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  if (warp == kMmaConsumers) {
+    // ---------------- producer warp: lane p owns piece p (R rows of one
+    // block) of each tile; the table entries of a tile are read in parallel
+    // before waiting for the stage, and each lane issues its own TMA loads.
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
+    const int npieces = kTile / R;             // <= 8 (R >= 8)
+    int issued = 0;
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % kStages;
+      const int ts = t0 + i * kTile;
+      const int te = min(t1, ts + kTile);
+      const int tok = ts + lane * R;
+      int64_t blk = -1;
+      bool mine = false;
+      if (lane < npieces && tok < te) {
+        blk = trow[tok >> bshift];
+        mine = blk >= 0 && blk < a.num_blocks;
+        if (!mine) latch(a.err, PA_ERR_OUT_OF_RANGE);
+      }
+      const unsigned pm = __ballot_sync(0xffffffffu, mine);
+      int ok = 1;
+      if (lane == 0) {
+        if (i >= kStages)
+          ok = mbar_wait_bounded(empty_bar(st), ((i / kStages) - 1) & 1, abort_flag, kWaitCycles);
+        if (ok) {
+          tile_mask[st] = pm;
+          mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * HALVES * R * 128u);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (mine) {
+        const uint32_t kdst = smem0 + st * STAGE_BYTES + lane * R * 128;
+        const uint32_t vdst = kdst + KV_BYTES;
+        const int z = (int)(blk * Hkv + kvh);
+        const int y = tok & (B - 1);
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h) {
+          tma_load_3d(kdst + h * HALF_BYTES, &tmK, h * 64, y, z, full_bar(st));
+          tma_load_3d(vdst + h * HALF_BYTES, &tmV, h * 64, y, z, full_bar(st));
+        }
+      }
+      issued = i + 1;
+    }
+    // let the loads this CTA issued land before it can leave
+    if (lane == 0)
+      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+        mbar_wait_bounded(full_bar(j % kStages), (j / kStages) & 1, abort_flag, kWaitCycles);
+  } else {
+    // ---------------- consumers
+    const int n = lane >> 2, c = lane & 3;
+    uint32_t qf[KSTEPS][2];
+    {
+      const T* qb = reinterpret_cast<const T*>(a.q) + ((int64_t)s * Hq + (int64_t)kvh * G) * D;
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        if (n < G) {
+          qf[ks][0] = *reinterpret_cast<const uint32_t*>(qb + n * D + ks * 16 + 2 * c);
+          qf[ks][1] = *reinterpret_cast<const uint32_t*>(qb + n * D + ks * 16 + 8 + 2 * c);
+        } else {
+          qf[ks][0] = qf[ks][1] = 0u;
+        }
+      }
+    }
+    const float sl2 = a.scale * kLog2e;
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % kStages;
+      if (!mbar_wait_bounded(full_bar(st), (i / kStages) & 1, abort_flag, kWaitCycles)) break;
+      const int ts = t0 + i * kTile;
+      const int te = min(t1, ts + kTile);
+      const int r0 = ts + warp * 16;   // first token of this warp's 16 rows
+      const uint32_t kst = smem0 + st * STAGE_BYTES;
+      const uint32_t vst = kst + KV_BYTES;
+      if (r0 < te) {
+        bool row_ok = false;
+        {
+          const int r = warp * 16 + (lane & 15);   // row inside the tile
+          row_ok = (ts + r < te) && ((tile_mask[st] >> (r / R)) & 1u);
+        }
+        const unsigned okm = __ballot_sync(0xffffffffu, row_ok) & 0xffffu;
+        if (okm != 0xffffu) {
+          const int r = lane & 15, h = lane >> 4;
+          if (h < HALVES && !((okm >> r) & 1u)) {
+            uint4* p = reinterpret_cast<uint4*>(smem + (vst - smem0) + h * HALF_BYTES +
+                                                (warp * 16 + r) * 128);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) p[j] = make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+        }
+        // S^T = K * Q^T for this warp's 16 tokens
+        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const int j = lane >> 3;
+          const int row = warp * 16 + (j & 1) * 8 + (lane & 7);
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            const int dch = ks * 2 + (j >> 1);
+            uint32_t af[4];
+            ldsm_x4(af, swz(kst + (dch >> 3) * HALF_BYTES, row, dch & 7));
+            MmaOps<T>::mma(sacc, af, qf[ks][0], qf[ks][1]);
+          }
+        }
+        const bool okA = (okm >> n) & 1u, okB = (okm >> (n + 8)) & 1u;
+        const float x0 = okA ? sacc[0] * sl2 : kNegInfM;   // row n,   head 2c
+        const float x1 = okA ? sacc[1] * sl2 : kNegInfM;   // row n,   head 2c+1
+        const float x2 = okB ? sacc[2] * sl2 : kNegInfM;   // row n+8, head 2c
+        const float x3 = okB ? sacc[3] * sl2 : kNegInfM;   // row n+8, head 2c+1
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const bool live0 = mn0 != kNegInfM, live1 = mn1 != kNegInfM;
+        const float al0 = live0 ? exp2f(m0 - mn0) : 1.f;
+        const float al1 = live1 ? exp2f(m1 - mn1) : 1.f;
+        const float p0 = live0 ? exp2f(x0 - mn0) : 0.f;
+        const float p2 = live0 ? exp2f(x2 - mn0) : 0.f;
+        const float p1 = live1 ? exp2f(x1 - mn1) : 0.f;
+        const float p3 = live1 ? exp2f(x3 - mn1) : 0.f;
+        const uint32_t cA = MmaOps<T>::pack(p0, p1);
+        const uint32_t cB = MmaOps<T>::pack(p2, p3);
+        // the denominator sums the same rounded weights the MMA multiplies
+        const float2 fA = MmaOps<T>::unpack(cA), fB = MmaOps<T>::unpack(cB);
+        l0 = l0 * al0 + fA.x + fB.x;
+        l1 = l1 * al1 + fA.y + fB.y;
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+          o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+        }
+        const uint32_t pb0 = movmatrix_trans(cA);
+        const uint32_t pb1 = movmatrix_trans(cB);
+        // O^T += V^T * P^T
+        {
+          const int j = lane >> 3;
+          const int row = warp * 16 + (j >> 1) * 8 + (lane & 7);
+#pragma unroll
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            const int dch = mt * 2 + (j & 1);
+            uint32_t af[4];
+            ldsm_x4_trans(af, swz(vst + (dch >> 3) * HALF_BYTES, row, dch & 7));
+            MmaOps<T>::mma(o[mt], af, pb0, pb1);
+          }
+        }
+        if (okm != 0xffffu) fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(st));
+    }
+    // sum the per-lane denominators over the 8 lanes that share a head pair
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+  }
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) latch(a.err, PA_ERR_TIMEOUT);
+    return;
+  }
+
+  // merge the four consumer warps through shared memory (the stage ring is
+  // free now)
+  float* sm_o = reinterpret_cast<float*>(smem);                  // [4][8][D]
+  float* sm_m = sm_o + kMmaConsumers * 8 * D;                    // [4][8]
+  float* sm_l = sm_m + kMmaConsumers * 8;                        // [4][8]
+  if (warp < kMmaConsumers) {
+    const int n = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int mt = 0; mt < KSTEPS; ++mt) {
+      float* base = sm_o + warp * 8 * D;
+      base[(2 * c) * D + mt * 16 + n] = o[mt][0];
+      base[(2 * c + 1) * D + mt * 16 + n] = o[mt][1];
+      base[(2 * c) * D + mt * 16 + n + 8] = o[mt][2];
+      base[(2 * c + 1) * D + mt * 16 + n + 8] = o[mt][3];
+    }
+    if (n == 0) {
+      sm_m[warp * 8 + 2 * c] = m0;
+      sm_m[warp * 8 + 2 * c + 1] = m1;
+      sm_l[warp * 8 + 2 * c] = l0;
+      sm_l[warp * 8 + 2 * c + 1] = l1;
+    }
+  }
+  __syncthreads();
+  T* out = reinterpret_cast<T*>(a.out);
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int g = idx / D, d = idx - g * D;
+    float M = kNegInfM;
+#pragma unroll
+    for (int w = 0; w < kMmaConsumers; ++w) M = fmaxf(M, sm_m[w * 8 + g]);
+    float Ls = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMmaConsumers; ++w) {
+      const float mw = sm_m[w * 8 + g];
+      const float wt = (mw == kNegInfM) ? 0.f : exp2f(mw - M);
+      Ls += sm_l[w * 8 + g] * wt;
+      O += sm_o[(w * 8 + g) * D + d] * wt;
+    }
+    const int h = kvh * G + g;
+    if (nsplit == 1) {
+      out[((int64_t)s * Hq + h) * D + d] = Vec<T>::cvt_out(Ls > 0.f ? O / Ls : 0.f);
+    } else {
+      const int64_t slot = ((int64_t)s * Hq + h) * a.num_splits + split;
+      a.ws_acc[slot * D + d] = O;
+      if (d == 0) { a.ws_ml[2 * slot] = M; a.ws_ml[2 * slot + 1] = Ls; }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// Pool [NB][Hkv][B][D] seen as a 3-D tensor {D, B, NB*Hkv}; one box is 64
+// columns x min(B, 64) rows of one (block, kv head) slice.
+bool encode_pool_map(CUtensorMap* map, const void* base, CUtensorMapDataType type,
+                     const DecodeArgs& a) {
+  const uint64_t D = a.head_size, B = a.block_size;
+  const uint64_t planes = (uint64_t)a.num_blocks * a.num_kv_heads;
+  if (planes == 0 || planes > 0x7fffffffull) return false;  // signed 32-bit coordinates
+  cuuint64_t dims[3] = {D, B, planes};
+  cuuint64_t strides[2] = {D * 2, B * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)(B < 64 ? B : 64), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+constexpr int mma_smem_bytes() {
+  return 1024 + kStages * 2 * (D / 64) * kTile * 128 + 2 * kStages * 8 + 4 + 4 * kStages + 16;
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_mma_tdg(const DecodeArgs& a, cudaStream_t st) {
+  if (!get_encode()) return cudaErrorNotSupported;
+  CUtensorMap tk, tv;
+  if (!encode_pool_map(&tk, a.kc, MmaOps<T>::kTmaType, a) ||
+      !encode_pool_map(&tv, a.vc, MmaOps<T>::kTmaType, a))
+    return cudaErrorInvalidValue;
+  constexpr int smem = mma_smem_bytes<D>();
+  static_assert(smem >= kMmaConsumers * 8 * D * 4 + 2 * kMmaConsumers * 8 * 4 + 1024,
+                "merge area must fit in the stage ring");
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, []() {
+    attr_err = cudaFuncSetAttribute(decode_mma_kernel<T, D, G>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  dim3 grid(a.num_splits, a.num_kv_heads, a.num_seqs);
+  decode_mma_kernel<T, D, G><<<grid, kMmaThreads, smem, st>>>(a, tk, tv);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_combine(a, st);
+}
+
+template <typename T, int D>
+cudaError_t launch_mma_td(const DecodeArgs& a, cudaStream_t st) {
+  switch (a.num_q_heads / a.num_kv_heads) {
+    case 2: return launch_mma_tdg<T, D, 2>(a, st);
+    case 4: return launch_mma_tdg<T, D, 4>(a, st);
+    case 8: return launch_mma_tdg<T, D, 8>(a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t launch_mma_t(const DecodeArgs& a, cudaStream_t st) {
+  if (a.head_size == 64) return launch_mma_td<T, 64>(a, st);
+  if (a.head_size == 128) return launch_mma_td<T, 128>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool mma_path_applies(const DecodeArgs& a) {
+  const int g = a.num_q_heads / a.num_kv_heads;
+  return (a.dtype == PA_F16 || a.dtype == PA_BF16) && (g == 2 || g == 4 || g == 8) &&
+         a.block_size >= 8 && (a.head_size == 64 || a.head_size == 128);
+}
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st) {
+  if (a.dtype == PA_BF16) return launch_mma_t<__nv_bfloat16>(a, st);
+  if (a.dtype == PA_F16) return launch_mma_t<__half>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

@@ -233,11 +233,27 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a) {
 }
 
 template <typename T, int D>
-cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st) {
+cudaError_t launch_combine_td(const DecodeArgs& a, cudaStream_t st) {
   if (a.num_splits <= 1) return cudaSuccess;
   dim3 grid(a.num_q_heads, a.num_seqs);
   combine_kernel<T, D><<<grid, D, 0, st>>>(a);
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_combine_t(const DecodeArgs& a, cudaStream_t st) {
+  if (a.head_size == 64) return launch_combine_td<T, 64>(a, st);
+  if (a.head_size == 128) return launch_combine_td<T, 128>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st) {
+  switch (a.dtype) {
+    case PA_F32: return launch_combine_t<float>(a, st);
+    case PA_F16: return launch_combine_t<__half>(a, st);
+    case PA_BF16: return launch_combine_t<__nv_bfloat16>(a, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <typename T, int D, int G>
@@ -247,7 +263,7 @@ cudaError_t launch_simt_tg(const DecodeArgs& a, cudaStream_t st) {
   decode_simt_kernel<T, D, G, U><<<grid, kSimtWarps * 32, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_combine<T, D>(a, st);
+  return launch_combine_td<T, D>(a, st);
 }
 
 template <typename T, int D>
@@ -278,6 +294,7 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
+  if (mma_path_applies(a)) return launch_decode_mma(a, st);
   return launch_decode_simt(a, st);
 }
 

@@ -47,6 +47,14 @@ struct DecodeArgs {
   int* err;
 };
 
+// Attention dispatch: the tensor-core kernel (decode_mma.cu) for 16-bit
+// query-head groups of 2, 4 or 8 with blocks of at least 8 tokens, the
+// CUDA-core kernel (decode_simt.cu) otherwise; then the split combine.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+bool mma_path_applies(const DecodeArgs& a);
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
+// log-sum-exp combine of the partitions (no-op when num_splits == 1)
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st);
 
 }  // namespace pa

@@ -177,3 +177,44 @@ def test_workspace_too_small_is_rejected():
                                g["seq_lens"], inp.scale, 2, max_seq_len=inp.max_seq_len,
                                partition_size=256, workspace=small)
     assert e.value.status == -4
+
+
+@pytest.mark.parametrize("dtype,G", [("bf16", 8), ("f16", 4), ("f16", 1), ("f32", 2)])
+def test_garbage_outside_the_sequence_never_reaches_the_output(dtype, G):
+    """Pool rows that belong to no token (the tail of each last block, and
+    every unassigned block) hold NaN; the result must still match the oracle,
+    which reads only the rows the block tables name."""
+    cfg = workloads.DecodeConfig("nan", 5, 2 * G, 2, 128, 16, dtype, seed=31)
+    inp = workloads.make_decode_inputs(cfg, context_lens=[0, 5, 70, 200, 333])
+    nan = float("nan")
+    used = torch.zeros(inp.num_blocks, 16, dtype=torch.bool)
+    for s, L in enumerate(inp.seq_lens.tolist()):
+        for j in range(L):
+            used[int(inp.block_tables[s, j // 16]), j % 16] = True
+    # the new token's row is written by the step itself, so it counts as used
+    for cache in (inp.key_cache, inp.value_cache):
+        c = cache.permute(0, 2, 1, 3)            # [NB, B, Hkv, D] view
+        c[~used] = nan
+    _, out_o, _, _ = oracle_step(inp)
+    _, out, _ = run_step(inp, partition_size=64)
+    assert torch.isfinite(out.float()).all()
+    assert max_abs_err(out, out_o) <= TOL[dtype]
+
+
+def test_tensor_core_path_edge_rows():
+    """Group-of-8 bf16 (tensor-core kernel): a zero-length sequence gives
+    zeros, a sequence with a block id outside the pool latches the error, and
+    the other sequences are unaffected."""
+    cfg = workloads.DecodeConfig("edge", 3, 16, 2, 128, 16, "bf16", seed=8)
+    inp = workloads.make_decode_inputs(cfg, context_lens=[40, 40, 40])
+    _, out_o, _, _ = oracle_step(inp)
+    g = to_dev(inp)
+    slots = pa.pa_compute_slot_mapping(g["query_start_loc"], g["positions"], g["block_tables"], 16)
+    pa.pa_reshape_and_cache(g["k_new"], g["v_new"], slots, g["key_cache"], g["value_cache"])
+    g["seq_lens"][0] = 0
+    g["block_tables"][1, 1] = inp.num_blocks + 3
+    out = pa.pa_decode_attention(g["q"], g["key_cache"], g["value_cache"], g["block_tables"],
+                                 g["seq_lens"], inp.scale, 2, max_seq_len=41)
+    assert pa.pa_get_device_error() == -5
+    assert out[0].eq(0).all()
+    assert max_abs_err(out[2:], out_o[2:]) <= TOL["bf16"]
