@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the step's kernels eagerly instead of replaying a CUDA graph")
     ap.add_argument("--partition", type=int, default=0,
                     help="tokens per context partition (0 = the library's choice)")
     ap.add_argument("--num-seqs", type=int, default=0,
@@ -210,7 +212,8 @@ class OracleTimer:
         return time.perf_counter() - t0
 
     def size_sample(self, budget_s):
-        """First n sequences whose oracle time is about budget_s."""
+        """A sample worth about budget_s of oracle time: the first n
+        sequences, or the whole batch repeated when one pass is shorter."""
         lens, w = self.lens, self.workers
         probe = list(range(min(len(lens), w)))
         self.run(probe)                      # warm the workers
@@ -222,17 +225,23 @@ class OracleTimer:
             tok += lens[n]
             n += 1
         self.sample = list(range(n))
+        self.repeats = 1
+        if n == len(lens) and tok < want_tok:
+            self.repeats = max(1, int(round(want_tok / max(1, tok))))
         return self.sample
 
     def measure(self):
         """(GB/s, seq-tokens/s, description, seconds) on the sized sample."""
         cfg = self.cfg
-        dt = self.run(self.sample)
+        dt = 0.0
+        for _ in range(self.repeats):
+            dt += self.run(self.sample)
         sl = [self.lens[i] for i in self.sample]
-        byts = kv_read_bytes(sl, cfg.num_kv_heads, cfg.head_size, ELT[cfg.dtype])
+        byts = self.repeats * kv_read_bytes(sl, cfg.num_kv_heads, cfg.head_size, ELT[cfg.dtype])
         desc = (f"first {len(sl)} of {len(self.lens)} sequences of the {cfg.name} batch, "
-                f"all {cfg.num_q_heads} query heads ({sum(sl)} context tokens)")
-        return byts / dt / 1e9, sum(sl) / dt, desc, dt
+                f"all {cfg.num_q_heads} query heads ({sum(sl)} context tokens)"
+                + (f", {self.repeats} passes" if self.repeats > 1 else ""))
+        return byts / dt / 1e9, self.repeats * sum(sl) / dt, desc, dt
 
     def close(self):
         self.pool.close()
@@ -360,7 +369,7 @@ def ours_arm(args):
     tokens = int(lens.sum())
     max_len = inp.max_seq_len
     P = args.partition
-    splits, ptoks = pa.pa_decode_partitioning(S, Hkv, B, max_len, P)
+    splits, ptoks = pa.pa_decode_partitioning(S, cfg.num_q_heads, Hkv, B, max_len, P)
     ws_bytes = pa.pa_decode_workspace_bytes(S, cfg.num_q_heads, Hkv, D, B, max_len, P)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     out = torch.empty_like(inp.q)
@@ -397,40 +406,94 @@ def ours_arm(args):
     sampler = ClockSampler(uuid) if rank == 0 else None
     if sampler is not None:
         time.sleep(0.3)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    # the step as one CUDA graph (the decode step is graph-captured in the
+    # serving engine the pages describe); --no-graph launches it eagerly
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step(g)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(g)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pa.pa_get_device_error() == 0
+
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t_host0 = time.monotonic()
     start.record(stream)
     for i in range(args.steps):
-        step(g, evs[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            step(g)
     stop.record(stream)
     torch.cuda.synchronize()
     t_host1 = time.monotonic()
     barrier(world)
+    ms_local = start.elapsed_time(stop)
+    ms_total = max_over_ranks(ms_local, world)
+    assert pa.pa_get_device_error() == 0
+
+    # per-launch attention time: the same K steps launched eagerly, with
+    # events on the launching stream around every attention call
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_host2 = time.monotonic()
+    for i in range(args.steps):
+        step(g, evs[i])
+    torch.cuda.synchronize()
+    t_host3 = time.monotonic()
     if sampler is not None:
         time.sleep(0.25)
         sampler.stop()
-    ms_local = start.elapsed_time(stop)
-    ms_total = max_over_ranks(ms_local, world)
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    eager_ms = (t_host3 - t_host2) * 1e3
     assert pa.pa_get_device_error() == 0
 
     # e2e: per-step inputs from pinned host memory, output back to host
     e2e = None
     if not args.no_e2e:
-        host = {k: v.cpu().pin_memory() for k, v in g.items()}
+        # every per-step input lives in one pinned staging buffer and one
+        # device buffer, so a step costs one host-to-device copy
+        names = list(g)
+        offs, total = {}, 0
+        for k in names:
+            offs[k] = total
+            total += (g[k].numel() * g[k].element_size() + 255) // 256 * 256
+        host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+
+        def view(buf, k):
+            n = g[k].numel() * g[k].element_size()
+            return buf[offs[k]:offs[k] + n].view(g[k].dtype).view(g[k].shape)
+        for k in names:
+            view(host_buf, k).copy_(g[k].cpu())
+        dbuf = {k: view(dev_buf, k) for k in names}
         out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        dbuf = {k: torch.empty_like(v) for k, v in g.items()}
-        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        h2d = total
         d2h = out_host.numel() * out_host.element_size()
+        dev_buf.copy_(host_buf)
+        graph_e2e = None
+        if graph is not None:
+            step(dbuf)
+            torch.cuda.synchronize()
+            graph_e2e = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_e2e):
+                step(dbuf)
 
         def e2e_step():
-            for k in host:
-                dbuf[k].copy_(host[k], non_blocking=True)
-            step(dbuf)
+            dev_buf.copy_(host_buf, non_blocking=True)
+            if graph_e2e is not None:
+                graph_e2e.replay()
+            else:
+                step(dbuf)
             out_host.copy_(out, non_blocking=True)
 
         for _ in range(3):
@@ -478,7 +541,9 @@ def ours_arm(args):
                      "algorithmic_bytes_per_launch": kv_bytes},
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
-        "clocks": sampler.summary(t_host0, t_host1) if sampler else None,
+        "clocks": sampler.summary(t_host0, t_host3) if sampler else None,
+        "launch": "cuda graph per step" if graph is not None else "eager",
+        "ms_per_step_eager_host": round(eager_ms / args.steps, 4),
         "device": props.name,
     }
     if orc_arrays is not None:

@@ -141,7 +141,8 @@ PA_API int64_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads,
  * sequence of length max_seq_len, and the partition length in tokens that
  * it resolves partition_size to. Either output pointer (host) may be NULL.
  */
-PA_API int pa_decode_partitioning(int num_seqs, int num_kv_heads, int block_size,
+PA_API int pa_decode_partitioning(int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int block_size,
                            int max_seq_len, int partition_size,
                            int* num_splits_out, int* partition_tokens_out);
 

@@ -31,7 +31,7 @@ SIGNATURES = {
     "pa_reshape_and_cache": ([_c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_p,
                               _c_i64, _c_i32, _c_p], _c_i32),
     "pa_decode_workspace_bytes": ([_c_i32] * 7, _c_i64),
-    "pa_decode_partitioning": ([_c_i32] * 5 + [_c_p, _c_p], _c_i32),
+    "pa_decode_partitioning": ([_c_i32] * 6 + [_c_p, _c_p], _c_i32),
     "pa_decode_attention": ([_c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32, _c_i32,
                              _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32, _c_i32, _c_p,
                              _c_p, _c_i64, _c_p], _c_i32),

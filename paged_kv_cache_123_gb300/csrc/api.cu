@@ -65,27 +65,35 @@ int check_launch(cudaError_t e) {
 // Tokens per context partition and the partition count for a batch whose
 // longest sequence is max_seq_len. Partitions are whole multiples of
 // max(64, block_size) tokens so every partition starts on a block boundary
-// and on a 64-token tile. With partition_size == 0 the count is chosen so
-// that (sequences x KV heads x partitions) gives several CTAs per SM, with
-// partitions no shorter than 512 tokens.
-void partitioning(int num_seqs, int num_kv_heads, int block_size, int max_seq_len,
-                  int partition_size, int sm_count, int* splits, int* tokens) {
+// and on a 64-token tile. With partition_size == 0 the length is chosen so
+// that (sequences x KV heads x partitions) fills two waves of resident CTAs
+// even for the longest sequence, then capped: 2048 tokens for the
+// tensor-core kernel's shape class (group >= 2, block >= 8; two 100 KB CTAs
+// per SM) and 512 for the CUDA-core kernel (many small CTAs per SM, where
+// shorter partitions even out ragged lengths). Both caps were the fastest of
+// 512..4096 on the Llama-7B and GQA batches on GB300.
+void partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
+                  int max_seq_len, int partition_size, int sm_count, int* splits,
+                  int* tokens) {
   const int64_t tile = block_size > 64 ? block_size : 64;
   const int64_t len = max_seq_len > 0 ? max_seq_len : 1;
+  auto round_up = [tile](int64_t x) { return (x + tile - 1) / tile * tile; };
   int64_t P;
   if (partition_size > 0) {
-    P = ((int64_t)partition_size + tile - 1) / tile * tile;
+    P = round_up(partition_size);
   } else {
+    const int g = num_q_heads / num_kv_heads;
+    const bool tc = g >= 2 && block_size >= 8;
+    const int64_t per_sm = tc ? 2 : 8;
+    const int64_t cap = round_up(tc ? 2048 : 512);
     const int64_t pairs = (int64_t)num_seqs * num_kv_heads;
-    const int64_t target = (int64_t)sm_count * 8;
-    int64_t want = pairs > 0 ? (target + pairs - 1) / pairs : 1;
-    if (want < 1) want = 1;
-    P = (len + want - 1) / want;
-    P = (P + tile - 1) / tile * tile;
-    const int64_t minP = (512 + tile - 1) / tile * tile;
-    if (P < minP) P = minP;
+    const int64_t target = 2 * (int64_t)sm_count * per_sm;
+    P = round_up((len * (pairs > 0 ? pairs : 1) + target - 1) / target);
+    const int64_t floor_p = round_up(256);
+    if (P < floor_p) P = floor_p;
+    if (P > cap) P = cap;
   }
-  if (P > len) P = (len + tile - 1) / tile * tile;
+  if (P > len) P = round_up(len);
   if (P > (int64_t)1 << 30) P = (int64_t)1 << 30;
   *tokens = (int)P;
   *splits = (int)((len + P - 1) / P);
@@ -133,7 +141,7 @@ const char* pa_status_string(int status) {
   return "unknown status";
 }
 
-int pa_abi_version(void) { return 1; }
+int pa_abi_version(void) { return 2; }
 
 int pa_compute_slot_mapping(const int32_t* query_start_loc, int num_reqs,
                             const int64_t* positions, int64_t num_tokens,
@@ -175,17 +183,18 @@ int pa_reshape_and_cache(const void* k, const void* v, int64_t num_tokens,
       value_cache, num_blocks, block_size, (cudaStream_t)stream, g_err_ptr[dev]));
 }
 
-int pa_decode_partitioning(int num_seqs, int num_kv_heads, int block_size,
+int pa_decode_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
                            int max_seq_len, int partition_size,
                            int* num_splits_out, int* partition_tokens_out) {
-  if (num_seqs < 0 || num_kv_heads <= 0 || !pow2(block_size) || block_size > 256 ||
+  if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 ||
+      num_q_heads % num_kv_heads != 0 || !pow2(block_size) || block_size > 256 ||
       max_seq_len < 0 || partition_size < 0)
     return PA_ERR_SHAPE;
   int dev;
   int st = device_setup(&dev);
   if (st != PA_OK) return st;
   int splits, tokens;
-  partitioning(num_seqs, num_kv_heads, block_size, max_seq_len, partition_size,
+  partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size,
                g_sm_count[dev], &splits, &tokens);
   if (num_splits_out) *num_splits_out = splits;
   if (partition_tokens_out) *partition_tokens_out = tokens;
@@ -200,7 +209,7 @@ int64_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
   if (st != PA_OK) return st;
   if (partition_size < 0) return PA_ERR_SHAPE;
   int splits, tokens;
-  st = pa_decode_partitioning(num_seqs, num_kv_heads, block_size, max_seq_len,
+  st = pa_decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len,
                               partition_size, &splits, &tokens);
   if (st != PA_OK) return st;
   return workspace_for(num_seqs, num_q_heads, head_size, splits);
@@ -233,7 +242,7 @@ int pa_decode_attention(const void* q, const void* key_cache, const void* value_
   a.num_seqs = num_seqs; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
   a.head_size = head_size; a.block_size = block_size; a.num_blocks = num_blocks;
   a.dtype = dtype; a.scale = scale; a.max_seq_len = max_seq_len;
-  partitioning(num_seqs, num_kv_heads, block_size, max_seq_len, partition_size,
+  partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size,
                g_sm_count[dev], &a.num_splits, &a.partition);
   const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);
   a.ws_acc = nullptr; a.ws_ml = nullptr;

@@ -10,9 +10,10 @@
 // 2 or 4 are zero-padded) and 16 tokens or 16 head dims as the M side.
 //
 // Data movement: a producer warp walks the partition's block table and issues
-// one 3-D tiled TMA load (cp.async.bulk.tensor) per (block, 64-column half of
-// the head dim) for K and for V into a 3-stage ring of 64-token tiles, with
-// 128-byte swizzle so the ldmatrix reads are bank-conflict free. Four
+// one 4-D tiled TMA load (cp.async.bulk.tensor) per block (up to 64 whole
+// token rows, one contiguous run in HBM) for K and for V into a 3-stage ring
+// of 64-token tiles, with the 128-byte swizzle so ldmatrix reads hit at most
+// two rows per bank group. Four
 // consumer warps take 16 tokens of each tile each, keep their own running
 // softmax state (log2 domain), and free the stage through an mbarrier. Every
 // wait is bounded: a stuck barrier raises an abort flag, the CTA drains and
@@ -94,19 +95,23 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
-// Address of 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte-swizzled
-// [rows][128 B] tile that starts on a 1024-byte boundary.
-__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
-  return base + row * 128 + ((chunk ^ (row & 7)) << 4);
+// Shared-memory address of 16-byte chunk `dch` (0 .. D/8-1) of token row
+// `row` in a tile of whole rows stored as 128-byte lines (HALVES lines per
+// row), with the TMA 128-byte swizzle: the 16-byte chunk index inside a line
+// is XORed with the line index mod 8. The tile starts on a 1024-byte boundary.
+template <int HALVES>
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int dch) {
+  const int line = row * HALVES + (dch >> 3);
+  return base + line * 128 + (((dch & 7) ^ (line & 7)) << 4);
 }
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
-  constexpr int HALVES = D / 64;                 // 128-byte column halves per row
-  constexpr int HALF_BYTES = kTile * 128;        // one half of a 64-token tile
-  constexpr int KV_BYTES = HALVES * HALF_BYTES;  // K (or V) part of a stage
+  constexpr int HALVES = D / 64;                 // 128-byte lines per token row
+  constexpr int ROW_BYTES = HALVES * 128;        // one token row (D * 2 bytes)
+  constexpr int KV_BYTES = kTile * ROW_BYTES;    // K (or V) part of a stage
   constexpr int STAGE_BYTES = 2 * KV_BYTES;
   constexpr int KSTEPS = D / 16;
   static_assert(G == 2 || G == 4 || G == 8, "group");
@@ -194,21 +199,18 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           ok = mbar_wait_bounded(empty_bar(st), ((i / kStages) - 1) & 1, abort_flag, kWaitCycles);
         if (ok) {
           tile_mask[st] = pm;
-          mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * HALVES * R * 128u);
+          mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * ROW_BYTES);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if (mine) {
-        const uint32_t kdst = smem0 + st * STAGE_BYTES + lane * R * 128;
+        const uint32_t kdst = smem0 + st * STAGE_BYTES + lane * R * ROW_BYTES;
         const uint32_t vdst = kdst + KV_BYTES;
         const int z = (int)(blk * Hkv + kvh);
         const int y = tok & (B - 1);
-#pragma unroll
-        for (int h = 0; h < HALVES; ++h) {
-          tma_load_3d(kdst + h * HALF_BYTES, &tmK, h * 64, y, z, full_bar(st));
-          tma_load_3d(vdst + h * HALF_BYTES, &tmV, h * 64, y, z, full_bar(st));
-        }
+        tma_load_4d(kdst, &tmK, 0, 0, y, z, full_bar(st));
+        tma_load_4d(vdst, &tmV, 0, 0, y, z, full_bar(st));
       }
       issued = i + 1;
     }
@@ -251,8 +253,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         if (okm != 0xffffu) {
           const int r = lane & 15, h = lane >> 4;
           if (h < HALVES && !((okm >> r) & 1u)) {
-            uint4* p = reinterpret_cast<uint4*>(smem + (vst - smem0) + h * HALF_BYTES +
-                                                (warp * 16 + r) * 128);
+            uint4* p = reinterpret_cast<uint4*>(smem + (vst - smem0) +
+                                                (warp * 16 + r) * ROW_BYTES + h * 128);
 #pragma unroll
             for (int j = 0; j < 8; ++j) p[j] = make_uint4(0, 0, 0, 0);
           }
@@ -267,7 +269,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           for (int ks = 0; ks < KSTEPS; ++ks) {
             const int dch = ks * 2 + (j >> 1);
             uint32_t af[4];
-            ldsm_x4(af, swz(kst + (dch >> 3) * HALF_BYTES, row, dch & 7));
+            ldsm_x4(af, swz<HALVES>(kst, row, dch));
             MmaOps<T>::mma(sacc, af, qf[ks][0], qf[ks][1]);
           }
         }
@@ -312,7 +314,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           for (int mt = 0; mt < KSTEPS; ++mt) {
             const int dch = mt * 2 + (j & 1);
             uint32_t af[4];
-            ldsm_x4_trans(af, swz(vst + (dch >> 3) * HALF_BYTES, row, dch & 7));
+            ldsm_x4_trans(af, swz<HALVES>(vst, row, dch));
             MmaOps<T>::mma(o[mt], af, pb0, pb1);
           }
         }
@@ -400,18 +402,19 @@ bool get_encode() {
   return g_encode != nullptr;
 }
 
-// Pool [NB][Hkv][B][D] seen as a 3-D tensor {D, B, NB*Hkv}; one box is 64
-// columns x min(B, 64) rows of one (block, kv head) slice.
+// Pool [NB][Hkv][B][D] seen as a 4-D tensor {64, D/64, B, NB*Hkv}: a row of
+// D elements split into 128-byte lines. One box is min(B, 64) whole rows of
+// one (block, kv head) slice, i.e. one contiguous run of global memory.
 bool encode_pool_map(CUtensorMap* map, const void* base, CUtensorMapDataType type,
                      const DecodeArgs& a) {
   const uint64_t D = a.head_size, B = a.block_size;
   const uint64_t planes = (uint64_t)a.num_blocks * a.num_kv_heads;
   if (planes == 0 || planes > 0x7fffffffull) return false;  // signed 32-bit coordinates
-  cuuint64_t dims[3] = {D, B, planes};
-  cuuint64_t strides[2] = {D * 2, B * D * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)(B < 64 ? B : 64), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return g_encode(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
+  cuuint64_t dims[4] = {64, D / 64, B, planes};
+  cuuint64_t strides[3] = {128, D * 2, B * D * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)(D / 64), (cuuint32_t)(B < 64 ? B : 64), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode(map, type, 4, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

@@ -71,12 +71,12 @@ def pa_decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int
     return int(n)
 
 
-def pa_decode_partitioning(num_seqs: int, num_kv_heads: int, block_size: int,
-                           max_seq_len: int, partition_size: int = 0):
+def pa_decode_partitioning(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                           block_size: int, max_seq_len: int, partition_size: int = 0):
     """(num_splits, partition_tokens) the attention call will use."""
     s, p = ctypes.c_int(0), ctypes.c_int(0)
     check("pa_decode_partitioning", lib().pa_decode_partitioning(
-        num_seqs, num_kv_heads, block_size, max_seq_len, partition_size,
+        num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size,
         ctypes.byref(s), ctypes.byref(p)))
     return s.value, p.value
 

@@ -93,7 +93,7 @@ def test_forced_partitions(partition, dtype, G):
     inp = workloads.make_decode_inputs(cfg, context_lens=[447, 1, 130, 900])
     _, out_o, _, _ = oracle_step(inp)
     _, out, _ = run_step(inp, partition_size=partition)
-    splits, ptoks = pa.pa_decode_partitioning(4, 2, 16, inp.max_seq_len, partition)
+    splits, ptoks = pa.pa_decode_partitioning(4, 2 * G, 2, 16, inp.max_seq_len, partition)
     assert ptoks % 64 == 0 and splits == math.ceil(inp.max_seq_len / ptoks)
     assert max_abs_err(out, out_o) <= TOL[dtype]
 
