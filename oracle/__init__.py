@@ -21,6 +21,6 @@ from .paged_attention import (  # noqa: F401
     upcast, slot_mapping, reshape_and_cache, copy_blocks, gather_kv,
     decode_attention, decode_attention_one, decode_step, blocks_needed,
     slots_allocated,
-    fragmentation, kv_bytes_per_token, sharing_saving,
+    fragmentation, kv_bytes_per_token, sharing_saving, map_to_kernel_blocks,
 )
 from .block_manager import OracleBlockManager  # noqa: F401

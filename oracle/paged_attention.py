@@ -241,3 +241,21 @@ def decode_step(q, k_new, v_new, key_cache, value_cache, block_tables,
     out = decode_attention(q, key_cache, value_cache, block_tables, seq_lens,
                            scale, num_kv_heads, block_size, dtype, seqs, heads)
     return slots, out
+
+
+# --------------------------------------------------------------------------
+# hybrid block sizes ([P1] §3.4 map_to_kernel_blocks)
+# --------------------------------------------------------------------------
+def map_to_kernel_blocks(manager_ids, blocks_per_kv_block: int) -> np.ndarray:
+    """Each allocator ("manager") block of r = blocks_per_kv_block kernel
+    blocks expands to kernel ids k*r, k*r + 1, ..., k*r + r - 1, in order
+    ([P1] §3.4: ids [0, 1, 2] with r = 2 give [0, 1, 2, 3, 4, 5]). A negative
+    (unassigned) manager id expands to r entries of -1."""
+    r = int(blocks_per_kv_block)
+    assert r >= 1
+    out = []
+    for k in np.asarray(manager_ids, dtype=np.int64).reshape(-1):
+        k = int(k)
+        for i in range(r):
+            out.append(-1 if k < 0 else k * r + i)
+    return np.asarray(out, dtype=np.int64)

@@ -249,3 +249,30 @@ def test_block_manager_invariants_random_walk():
         assert sorted(bm.free) == [b for b in range(NB) if counts[b] == 0]
         for s, t in bm.tables.items():
             assert len(t) == oracle.blocks_needed(bm.lens[s], B)
+
+
+def test_p1_map_to_kernel_blocks_example():
+    g = load("p1_map_to_kernel_blocks.json")
+    r = g["blocks_per_kv_block"]
+    assert r == g["manager_block_tokens"] // g["kernel_block_tokens"]
+    assert oracle.map_to_kernel_blocks(g["manager_ids"], r).tolist() == g["kernel_ids"]
+    for k, ids in g["per_manager_block"].items():
+        assert oracle.map_to_kernel_blocks([int(k)], r).tolist() == ids
+
+
+def test_map_to_kernel_blocks_preserves_token_addresses():
+    """Brute force: a token at position p of a sequence whose manager table
+    uses blocks of B*r tokens lands at the same (kernel block, row) whether
+    addressed through the expanded kernel table with block size B, or as
+    row p % (B*r) of manager block k split into r kernel blocks."""
+    rng = np.random.default_rng(5)
+    for r in (1, 2, 4):
+        B = 4
+        mids = rng.permutation(10)[:4]
+        kt = oracle.map_to_kernel_blocks(mids, r)
+        for p in range(4 * B * r):
+            k = mids[p // (B * r)]
+            off = p % (B * r)
+            want = (k * r + off // B, off % B)
+            s = oracle.slot_mapping([0, 1], [p], kt.reshape(1, -1), B)[0]
+            assert (s // B, s % B) == want
