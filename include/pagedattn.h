@@ -247,6 +247,28 @@ PA_API int pa_copy_blocks(void* const* key_caches, void* const* value_caches,
                    int64_t num_blocks, int64_t block_bytes, void* stream);
 
 /*
+ * pa_map_to_kernel_blocks — hybrid block sizes ([P1] §3.4,
+ * map_to_kernel_blocks): when the allocator's block holds r kernel blocks,
+ * its block k owns kernel blocks k*r, k*r+1, ..., k*r+r-1, and a table of
+ * allocator ids expands to a table the attention kernels read with block
+ * size B = allocator block tokens / r. Example from [P1]: ids [0, 1, 2] with
+ * r = 2 give [0, 1, 2, 3, 4, 5].
+ *
+ * manager_table  int32 [num_rows][manager_stride], device; the first
+ *                num_cols entries of each row are expanded; a negative id
+ *                expands to r entries of -1.
+ * kernel_table   int32 [num_rows][kernel_stride], device, written in its
+ *                first num_cols*r entries of each row;
+ *                kernel_stride >= num_cols * r.
+ * blocks_per_kv_block  r >= 1. An expanded id above INT32_MAX is written as
+ *                -1 and latches PA_ERR_OUT_OF_RANGE.
+ */
+PA_API int pa_map_to_kernel_blocks(const int32_t* manager_table, int64_t num_rows,
+                                   int64_t manager_stride, int64_t num_cols,
+                                   int blocks_per_kv_block, int32_t* kernel_table,
+                                   int64_t kernel_stride, void* stream);
+
+/*
  * Read (and clear) the device-side error word that the kernels latch on bad
  * indices. Synchronises `stream` first. *code_out receives PA_OK or the
  * first latched error (PA_ERR_OUT_OF_RANGE). The word is per device and

@@ -296,6 +296,22 @@ int pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_l
                                              g_err_ptr[dev]));
 }
 
+int pa_map_to_kernel_blocks(const int32_t* manager_table, int64_t num_rows,
+                            int64_t manager_stride, int64_t num_cols, int blocks_per_kv_block,
+                            int32_t* kernel_table, int64_t kernel_stride, void* stream) {
+  if (num_rows < 0 || num_cols < 0 || blocks_per_kv_block < 1 || manager_stride < num_cols ||
+      kernel_stride < num_cols * blocks_per_kv_block)
+    return PA_ERR_SHAPE;
+  if (num_rows == 0 || num_cols == 0) return PA_OK;
+  if (!manager_table || !kernel_table) return PA_ERR_NULL;
+  int dev;
+  int st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  return check_launch(pa::launch_map_to_kernel_blocks(
+      manager_table, num_rows, manager_stride, num_cols, blocks_per_kv_block, kernel_table,
+      kernel_stride, (cudaStream_t)stream, g_err_ptr[dev]));
+}
+
 int pa_get_device_error(int* code_out, void* stream) {
   if (!code_out) return PA_ERR_NULL;
   int dev;

@@ -164,3 +164,48 @@ cudaError_t launch_copy_blocks(void* const* kcs, void* const* vcs,
 }
 
 }  // namespace pa
+
+namespace pa {
+
+// Hybrid block sizes ("PagedAttention 核心创新深度分析" §3.4,
+// map_to_kernel_blocks): the allocator hands out blocks of r kernel blocks;
+// its block k owns kernel blocks k*r .. k*r + r - 1. One thread per output
+// entry of the expanded table; a negative (unassigned) id stays -1.
+__global__ void map_to_kernel_blocks_kernel(const int32_t* __restrict__ mtab, int64_t rows,
+                                            int64_t mstride, int64_t cols, int r,
+                                            int32_t* __restrict__ ktab, int64_t kstride,
+                                            int* err) {
+  const int64_t per_row = cols * r;
+  const int64_t n = rows * per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / per_row;
+    const int64_t j = i - row * per_row;
+    const int64_t c = j / r;
+    const int64_t k = mtab[row * mstride + c];
+    int64_t v = -1;
+    if (k >= 0) {
+      v = k * r + (j - c * r);
+      if (v > 0x7fffffffLL) {
+        latch(err, PA_ERR_OUT_OF_RANGE);
+        v = -1;
+      }
+    }
+    ktab[row * kstride + j] = (int32_t)v;
+  }
+}
+
+cudaError_t launch_map_to_kernel_blocks(const int32_t* mtab, int64_t rows, int64_t mstride,
+                                        int64_t cols, int r, int32_t* ktab, int64_t kstride,
+                                        cudaStream_t st, int* err) {
+  const int64_t n = rows * cols * r;
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = (n + threads - 1) / threads;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  map_to_kernel_blocks_kernel<<<(unsigned)blocks, threads, 0, st>>>(
+      mtab, rows, mstride, cols, r, ktab, kstride, err);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

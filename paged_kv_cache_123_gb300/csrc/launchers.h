@@ -27,6 +27,10 @@ cudaError_t launch_copy_blocks(void* const* kcs, void* const* vcs,
                                int64_t num_pairs, int64_t num_blocks,
                                int64_t block_bytes, cudaStream_t st, int* err);
 
+cudaError_t launch_map_to_kernel_blocks(const int32_t* mtab, int64_t rows, int64_t mstride,
+                                        int64_t cols, int r, int32_t* ktab, int64_t kstride,
+                                        cudaStream_t st, int* err);
+
 struct DecodeArgs {
   const void* q;
   const void* kc;

@@ -151,3 +151,22 @@ def pa_get_device_error(stream=None) -> int:
     check("pa_get_device_error", lib().pa_get_device_error(ctypes.byref(code),
                                                            stream_handle(stream)))
     return code.value
+
+
+def pa_map_to_kernel_blocks(manager_table: torch.Tensor, blocks_per_kv_block: int,
+                            kernel_table: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """Expand an int32 [rows, cols] table of allocator block ids (each owning
+    r = blocks_per_kv_block kernel blocks) into an int32 [rows, cols * r]
+    table of kernel block ids."""
+    _dev(manager_table, "manager_table", torch.int32)
+    rows, cols = manager_table.shape
+    r = int(blocks_per_kv_block)
+    if kernel_table is None:
+        kernel_table = torch.empty((rows, cols * r), dtype=torch.int32,
+                                   device=manager_table.device)
+    _dev(kernel_table, "kernel_table", torch.int32)
+    check("pa_map_to_kernel_blocks", lib().pa_map_to_kernel_blocks(
+        ptr(manager_table), rows, cols, cols, r, ptr(kernel_table), kernel_table.shape[1],
+        stream_handle(stream)))
+    return kernel_table

@@ -93,3 +93,11 @@ def test_copy_blocks_host_alias_and_range_checks(lib):
     assert run([(0, 9)]) == -5                  # outside the pool
     assert run([(0, 1)], block_bytes=24) == -2  # not a multiple of 16
     assert lib.pa_copy_blocks(arr, arr, 1, p, None, 0, 8, 256, None) == 0  # no pairs
+
+
+def test_map_to_kernel_blocks_host_checks(lib):
+    p = ctypes.c_void_p(16)
+    assert lib.pa_map_to_kernel_blocks(p, 2, 3, 3, 0, p, 6, None) == -2     # r < 1
+    assert lib.pa_map_to_kernel_blocks(p, 2, 3, 3, 2, p, 5, None) == -2     # stride too small
+    assert lib.pa_map_to_kernel_blocks(None, 2, 3, 3, 2, p, 6, None) == -1
+    assert lib.pa_map_to_kernel_blocks(p, 0, 3, 3, 2, p, 6, None) == 0      # nothing to do
