@@ -22,5 +22,6 @@ from .paged_attention import (  # noqa: F401
     decode_attention, decode_attention_one, decode_step, blocks_needed,
     slots_allocated,
     fragmentation, kv_bytes_per_token, sharing_saving, map_to_kernel_blocks,
+    multi_query_attention,
 )
 from .block_manager import OracleBlockManager  # noqa: F401

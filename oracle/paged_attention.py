@@ -259,3 +259,40 @@ def map_to_kernel_blocks(manager_ids, blocks_per_kv_block: int) -> np.ndarray:
         for i in range(r):
             out.append(-1 if k < 0 else k * r + i)
     return np.asarray(out, dtype=np.int64)
+
+
+# --------------------------------------------------------------------------
+# several new tokens per sequence (chunked prefill / speculative tokens)
+# --------------------------------------------------------------------------
+def multi_query_attention(q, key_cache, value_cache, block_tables, query_start_loc,
+                          seq_lens, scale: float, num_kv_heads: int, block_size: int,
+                          dtype: str) -> np.ndarray:
+    """Causal paged attention for n_s = qsl[s+1] - qsl[s] new tokens of each
+    sequence, whose K/V are already in the pool ([P3] §2.5: the scheduler
+    gives each request a token budget that covers chunked prefill and
+    speculative tokens alike; the slot mapping of [P1] §2.3 handles many
+    tokens per request). Sequence s holds L_s = seq_lens[s] tokens including
+    the new ones, so new token i sits at position L_s - n_s + i and attends to
+    positions 0 .. L_s - n_s + i. With n_s = 1 this is decode attention.
+    q: [T, Hq, D] with T = qsl[-1]. Returns float64 [T, Hq, D]."""
+    T, Hq, D = q.shape
+    g = Hq // num_kv_heads
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    q64 = upcast(q, dtype)
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    for s in range(len(qsl) - 1):
+        n = int(qsl[s + 1] - qsl[s])
+        L = int(seq_lens[s])
+        if n == 0:
+            continue
+        if n > L:
+            raise ValueError(f"sequence {s}: {n} new tokens but length {L}")
+        for kvh in range(num_kv_heads):
+            K = gather_kv(key_cache, block_tables[s], L, kvh, block_size, dtype)
+            V = gather_kv(value_cache, block_tables[s], L, kvh, block_size, dtype)
+            for i in range(n):
+                last = L - n + i
+                for h in range(kvh * g, (kvh + 1) * g):
+                    out[qsl[s] + i, h] = decode_attention_one(
+                        q64[qsl[s] + i, h], K[:last + 1], V[:last + 1], scale)
+    return out
