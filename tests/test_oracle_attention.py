@@ -183,3 +183,47 @@ def test_gqa_query_head_reads_its_group_kv_head():
                                   1.0, Hkv, B, "f32")
     for h in range(Hq):
         assert np.all(out[0, h] == h // g + 1.0)
+
+
+def _mq_inputs(dtype, n_new, ctx, hq, hkv, B, seed):
+    cfg = workloads.DecodeConfig("mq", len(ctx), hq, hkv, 64, B, dtype, seed=seed)
+    lens = [c + n for c, n in zip(ctx, n_new)]
+    inp = workloads.make_decode_inputs(cfg, context_lens=[L - 1 for L in lens])
+    qsl = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int64)
+    gen = torch.Generator().manual_seed(seed + 1)
+    q = torch.empty(int(qsl[-1]), hq, 64, dtype=workloads.DTYPES[dtype])
+    workloads.randn_into(q, gen)
+    return inp, q, qsl, np.array(lens)
+
+
+def test_multi_query_with_one_new_token_is_decode():
+    inp, q, qsl, lens = _mq_inputs("bf16", [1, 1, 1], [5, 17, 40], 8, 2, 8, 3)
+    a = oracle.multi_query_attention(_np(q), _np(inp.key_cache), _np(inp.value_cache),
+                                     inp.block_tables.numpy(), qsl, lens, 0.125, 2, 8, "bf16")
+    b = oracle.decode_attention(_np(q), _np(inp.key_cache), _np(inp.value_cache),
+                                inp.block_tables.numpy(), lens, 0.125, 2, 8, "bf16")
+    assert np.array_equal(a, b)
+
+
+def test_multi_query_matches_sdpa_with_causal_offset_mask():
+    n_new, ctx = [3, 0, 6, 1], [4, 9, 0, 30]
+    inp, q, qsl, lens = _mq_inputs("f16", n_new, ctx, 8, 2, 4, 9)
+    got = oracle.multi_query_attention(_np(q), _np(inp.key_cache), _np(inp.value_cache),
+                                       inp.block_tables.numpy(), qsl, lens, 0.2, 2, 4, "f16")
+    kc64 = oracle.upcast(_np(inp.key_cache), "f16")
+    vc64 = oracle.upcast(_np(inp.value_cache), "f16")
+    q64 = oracle.upcast(_np(q), "f16")
+    for s, (n, L) in enumerate(zip(n_new, lens)):
+        if n == 0:
+            continue
+        row = inp.block_tables[s].numpy()
+        # query i may see key j iff j <= L - n + i
+        mask = torch.from_numpy(np.arange(L)[None, :] <= (L - n + np.arange(n))[:, None])
+        for kvh in range(2):
+            K = torch.from_numpy(_block_concat(kc64, row, L, kvh))
+            V = torch.from_numpy(_block_concat(vc64, row, L, kvh))
+            for h in range(kvh * 4, kvh * 4 + 4):
+                Q = torch.from_numpy(q64[qsl[s]:qsl[s] + n, h])
+                o = torch.nn.functional.scaled_dot_product_attention(
+                    Q[None], K[None], V[None], attn_mask=mask[None], scale=0.2)[0]
+                assert np.allclose(got[qsl[s]:qsl[s] + n, h], o.numpy(), atol=1e-12, rtol=0)

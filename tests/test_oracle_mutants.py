@@ -94,6 +94,25 @@ def _decode_gqa_modulo(q, kc, vc, tables, lens, scale, Hkv, B, dtype, seqs=None,
     return out
 
 
+def _mq_sees_one_future_token(q, kc, vc, tables, qsl, lens, scale, Hkv, B, dtype):
+    T, Hq, D = q.shape
+    g = Hq // Hkv
+    q64 = opa.upcast(q, dtype)
+    out = np.zeros((T, Hq, D))
+    for s in range(len(qsl) - 1):
+        n, L = int(qsl[s + 1] - qsl[s]), int(lens[s])
+        for kvh in range(Hkv):
+            K = opa.gather_kv(kc, tables[s], L, kvh, B, dtype)
+            V = opa.gather_kv(vc, tables[s], L, kvh, B, dtype)
+            for i in range(n):
+                last = min(L - 1, L - n + i + 1)           # one token too far
+                for h in range(kvh * g, (kvh + 1) * g):
+                    out[qsl[s] + i, h] = opa.decode_attention_one(q64[qsl[s] + i, h],
+                                                                  K[:last + 1], V[:last + 1],
+                                                                  scale)
+    return out
+
+
 class _NoDecrementOnCow(obm.OracleBlockManager):
     def _release(self, b):
         pass
@@ -134,6 +153,8 @@ PIN_TESTS = [
     lambda: ta.test_oracle_matches_sdpa_fp64("gqa_small", "bf16", 8, 2, 8),
     ta.test_decode_step_attends_to_the_new_token,
     ta.test_gqa_query_head_reads_its_group_kv_head,
+    ta.test_multi_query_with_one_new_token_is_decode,
+    ta.test_multi_query_matches_sdpa_with_causal_offset_mask,
 ]
 
 MUTANTS = {
@@ -149,6 +170,7 @@ MUTANTS = {
     "gqa_modulo": [("decode_attention", _decode_gqa_modulo)],
     "cow_no_decrement": [("OracleBlockManager", _NoDecrementOnCow)],
     "cow_always": [("OracleBlockManager", _CowAlways)],
+    "mq_future_token": [("multi_query_attention", _mq_sees_one_future_token)],
 }
 
 
