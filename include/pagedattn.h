@@ -223,6 +223,39 @@ PA_API int pa_decode_attention_static(const void* q, const void* key_cache,
                                       void* out, void* stream);
 
 /*
+ * pa_multi_query_attention — causal paged attention for several new tokens
+ * per sequence in one step: a prefill chunk or speculative candidates ([P3]
+ * §2.5: one token budget per request covers chunked prefill and speculative
+ * tokens; [P1] §2.3: the slot mapping places any number of tokens per
+ * request). Sequence s has n_s = query_start_loc[s+1] - query_start_loc[s]
+ * new tokens whose K/V are already in the pool (pa_reshape_and_cache) and
+ * L_s = seq_lens[s] tokens in total; new token i is at position
+ * L_s - n_s + i and attends to positions 0 .. L_s - n_s + i:
+ *     out[t, h] = sum_{j <= L_s - n_s + i} softmax_j(scale <q[t,h], K_s[j]>) V_s[j]
+ * with t = query_start_loc[s] + i and KV head h / (num_q_heads/num_kv_heads).
+ * With n_s = 1 this is pa_decode_attention.
+ *
+ * q, out           [num_tokens][num_q_heads][head_size], dtype, device;
+ *                  num_tokens = query_start_loc[num_seqs].
+ * query_start_loc  int32 [num_seqs + 1], non-decreasing, device.
+ * seq_lens         int32 [num_seqs], device; n_s <= L_s <= max_seq_len.
+ * max_query_len    host upper bound of n_s (sizes the grid).
+ * Other arguments as in pa_decode_attention. Supported: fp16/bf16,
+ * head_size 64/128, block_size a power of two in [8, 256], group size
+ * 1/2/4/8 (PA_ERR_SHAPE / PA_ERR_DTYPE otherwise). A sequence whose lengths
+ * break these bounds is skipped (its rows are not written) and latches
+ * PA_ERR_OUT_OF_RANGE. No workspace is needed.
+ */
+PA_API int pa_multi_query_attention(const void* q, const int32_t* query_start_loc,
+                                    int num_seqs, const void* key_cache,
+                                    const void* value_cache, const int32_t* block_tables,
+                                    int64_t block_tables_stride, const int32_t* seq_lens,
+                                    int num_q_heads, int num_kv_heads, int head_size,
+                                    int block_size, int64_t num_blocks, int dtype,
+                                    float scale, int max_query_len, int max_seq_len,
+                                    void* out, void* stream);
+
+/*
  * pa_copy_blocks — block-level copy-on-write data movement ([P2] Figure 8:
  * "copy physical block 1's content to physical block 3"; [P4] copy-on-write
  * figure). For every pair (src, dst) in src_dst_pairs and every layer l, the

@@ -259,6 +259,39 @@ int pa_decode_attention(const void* q, const void* key_cache, const void* value_
   return check_launch(pa::launch_decode(a, (cudaStream_t)stream));
 }
 
+int pa_multi_query_attention(const void* q, const int32_t* query_start_loc, int num_seqs,
+                             const void* key_cache, const void* value_cache,
+                             const int32_t* block_tables, int64_t block_tables_stride,
+                             const int32_t* seq_lens, int num_q_heads, int num_kv_heads,
+                             int head_size, int block_size, int64_t num_blocks, int dtype,
+                             float scale, int max_query_len, int max_seq_len, void* out,
+                             void* stream) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return elt_bytes(dtype) ? PA_ERR_SHAPE : PA_ERR_DTYPE;
+  int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                              max_seq_len);
+  if (st != PA_OK) return st;
+  if (block_size < 8 || max_query_len < 0 || num_blocks < 0 || block_tables_stride < 0)
+    return PA_ERR_SHAPE;
+  if ((int64_t)max_seq_len > block_tables_stride * block_size) return PA_ERR_OUT_OF_RANGE;
+  if (num_seqs == 0 || max_query_len == 0) return PA_OK;
+  if (!q || !query_start_loc || !key_cache || !value_cache || !block_tables || !seq_lens || !out)
+    return PA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) || !aligned16(out))
+    return PA_ERR_ALIGN;
+  int dev;
+  st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  pa::MultiQueryArgs a;
+  a.q = q; a.qsl = query_start_loc; a.num_seqs = num_seqs;
+  a.kc = key_cache; a.vc = value_cache; a.tables = block_tables;
+  a.table_stride = block_tables_stride; a.seq_lens = seq_lens;
+  a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads; a.head_size = head_size;
+  a.block_size = block_size; a.num_blocks = num_blocks; a.dtype = dtype; a.scale = scale;
+  a.max_query_len = max_query_len; a.max_seq_len = max_seq_len; a.out = out;
+  a.err = g_err_ptr[dev];
+  return check_launch(pa::launch_multi_query(a, (cudaStream_t)stream));
+}
+
 int pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                    const int64_t* src_dst_pairs, const int64_t* src_dst_pairs_host,
                    int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,

@@ -3,6 +3,7 @@
 // cudaError_t from the launch.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -60,5 +61,31 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
 // log-sum-exp combine of the partitions (no-op when num_splits == 1)
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st);
+
+// TMA descriptor of a KV pool [num_blocks][num_kv_heads][block_size][head_size]
+// (16-bit dtype): boxes of min(block_size, 64) whole rows of one slice.
+bool encode_kv_pool_map(CUtensorMap* map, const void* base, int dtype, int64_t num_blocks,
+                        int num_kv_heads, int block_size, int head_size);
+
+// Several new tokens per sequence (chunked prefill, speculative tokens):
+// causal paged attention, tensor-core kernel (prefill_mma.cu).
+struct MultiQueryArgs {
+  const void* q;
+  const int32_t* qsl;
+  int num_seqs;
+  const void* kc;
+  const void* vc;
+  const int32_t* tables;
+  int64_t table_stride;
+  const int32_t* seq_lens;
+  int num_q_heads, num_kv_heads, head_size, block_size;
+  int64_t num_blocks;
+  int dtype;
+  float scale;
+  int max_query_len, max_seq_len;
+  void* out;
+  int* err;
+};
+cudaError_t launch_multi_query(const MultiQueryArgs& a, cudaStream_t st);
 
 }  // namespace pa

@@ -170,3 +170,31 @@ def pa_map_to_kernel_blocks(manager_table: torch.Tensor, blocks_per_kv_block: in
         ptr(manager_table), rows, cols, cols, r, ptr(kernel_table), kernel_table.shape[1],
         stream_handle(stream)))
     return kernel_table
+
+
+def pa_multi_query_attention(q: torch.Tensor, query_start_loc: torch.Tensor,
+                             key_cache: torch.Tensor, value_cache: torch.Tensor,
+                             block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                             num_kv_heads: int, out: Optional[torch.Tensor] = None, *,
+                             max_query_len: int, max_seq_len: int,
+                             stream=None) -> torch.Tensor:
+    """Causal paged attention of several new tokens per sequence.
+    q/out [T, Hq, D] with T = query_start_loc[-1]; pools [NB, Hkv, B, D]."""
+    for n, t in (("q", q), ("key_cache", key_cache), ("value_cache", value_cache)):
+        _dev(t, n)
+    _dev(query_start_loc, "query_start_loc", torch.int32)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    T, Hq, D = q.shape
+    NB, Hkv, B, Dk = key_cache.shape
+    if Hkv != num_kv_heads or Dk != D or value_cache.shape != key_cache.shape:
+        raise ValueError("pool shape does not match q / num_kv_heads")
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out")
+    check("pa_multi_query_attention", lib().pa_multi_query_attention(
+        ptr(q), ptr(query_start_loc), query_start_loc.numel() - 1, ptr(key_cache),
+        ptr(value_cache), ptr(block_tables), block_tables.shape[1], ptr(seq_lens), Hq, Hkv, D,
+        B, NB, DTYPE_CODE[q.dtype], float(scale), int(max_query_len), int(max_seq_len),
+        ptr(out), stream_handle(stream)))
+    return out

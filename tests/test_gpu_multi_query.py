@@ -1,0 +1,124 @@
+"""Several new tokens per sequence (prefill chunks, speculative tokens):
+slot mapping of all new tokens, their KV write, then causal paged attention
+through the C ABI, element by element against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_123_gb300 as pa
+from paged_kv_cache_123_gb300 import workloads
+from tests.helpers import TOL, max_abs_err, np_
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def make_batch(dtype, D, hq, hkv, B, ctx, n_new, seed):
+    gen = torch.Generator().manual_seed(seed)
+    dt = workloads.DTYPES[dtype]
+    lens = [c + n for c, n in zip(ctx, n_new)]
+    nblk = [-(-L // B) for L in lens]
+    NB = sum(nblk) + 5
+    perm = torch.randperm(NB, generator=gen)
+    tables = torch.full((len(lens), max(nblk)), -1, dtype=torch.int32)
+    off = 0
+    for s, k in enumerate(nblk):
+        tables[s, :k] = perm[off:off + k].to(torch.int32)
+        off += k
+    T = sum(n_new)
+    kc = torch.empty(NB, hkv, B, D, dtype=dt)
+    vc = torch.empty_like(kc)
+    q = torch.empty(T, hq, D, dtype=dt)
+    kn = torch.empty(T, hkv, D, dtype=dt)
+    vn = torch.empty_like(kn)
+    for t in (kc, vc, q, kn, vn):
+        workloads.randn_into(t, gen)
+    qsl = torch.tensor(np.concatenate([[0], np.cumsum(n_new)]), dtype=torch.int32)
+    pos = torch.tensor([p for c, n in zip(ctx, n_new) for p in range(c, c + n)],
+                       dtype=torch.int64)
+    return dict(kc=kc, vc=vc, q=q, kn=kn, vn=vn, qsl=qsl, pos=pos, tables=tables,
+                lens=torch.tensor(lens, dtype=torch.int32), B=B, hkv=hkv, dtype=dtype,
+                scale=D ** -0.5, max_q=max(n_new), max_len=max(lens))
+
+
+def run_both(b):
+    kco, vco = np_(b["kc"]), np_(b["vc"])
+    slots_o = oracle.slot_mapping(b["qsl"].numpy(), b["pos"].numpy(), b["tables"].numpy(), b["B"])
+    oracle.reshape_and_cache(np_(b["kn"]), np_(b["vn"]), slots_o, kco, vco, b["B"])
+    want = oracle.multi_query_attention(np_(b["q"]), kco, vco, b["tables"].numpy(),
+                                        b["qsl"].numpy(), b["lens"].numpy(), b["scale"],
+                                        b["hkv"], b["B"], b["dtype"])
+    g = {k: v.to(DEV) for k, v in b.items() if isinstance(v, torch.Tensor)}
+    slots = pa.pa_compute_slot_mapping(g["qsl"], g["pos"], g["tables"], b["B"])
+    pa.pa_reshape_and_cache(g["kn"], g["vn"], slots, g["kc"], g["vc"])
+    out = pa.pa_multi_query_attention(g["q"], g["qsl"], g["kc"], g["vc"], g["tables"], g["lens"],
+                                      b["scale"], b["hkv"], max_query_len=b["max_q"],
+                                      max_seq_len=b["max_len"])
+    torch.cuda.synchronize()
+    assert np.array_equal(slots.cpu().numpy(), slots_o)
+    return out, want, g
+
+
+CASES = []
+for dtype in ("bf16", "f16"):
+    for D in (64, 128):
+        for G in (1, 2, 4, 8):
+            CASES.append((dtype, D, G, 16))
+for B in (8, 32, 64, 128, 256):
+    CASES.append(("bf16", 128, 8, B))
+    CASES.append(("f16", 128, 1, B))
+
+
+@pytest.mark.parametrize("dtype,D,G,B", CASES)
+def test_multi_query_matches_oracle(dtype, D, G, B):
+    ctx = [0, 5, 100, 300, 0, 64]
+    n_new = [1, 3, 17, 70, 130, 64]
+    seed = 500 + 17 * D + 7 * G + B + (1000 if dtype == "f16" else 0)
+    b = make_batch(dtype, D, 2 * G, 2, B, ctx, n_new, seed)
+    out, want, _ = run_both(b)
+    assert torch.isfinite(out.float()).all()
+    err = max_abs_err(out, want)
+    assert err <= TOL[dtype], err
+    assert pa.pa_get_device_error() == 0
+
+
+def test_one_new_token_matches_decode_kernel():
+    b = make_batch("bf16", 128, 16, 2, 16, [10, 500, 2000], [1, 1, 1], 31)
+    out, want, g = run_both(b)
+    dec = pa.pa_decode_attention(g["q"], g["kc"], g["vc"], g["tables"], g["lens"], b["scale"], 2,
+                                 max_seq_len=b["max_len"])
+    assert (out.float() - dec.float()).abs().max().item() <= TOL["bf16"]
+    assert max_abs_err(out, want) <= TOL["bf16"]
+
+
+def test_garbage_pool_rows_do_not_leak():
+    b = make_batch("bf16", 128, 16, 2, 16, [3, 40], [5, 9], 41)
+    used = torch.zeros(b["kc"].shape[0], 16, dtype=torch.bool)
+    for s, L in enumerate(b["lens"].tolist()):
+        for j in range(L):
+            used[int(b["tables"][s, j // 16]), j % 16] = True
+    for cache in (b["kc"], b["vc"]):
+        cache.permute(0, 2, 1, 3)[~used] = float("nan")
+    out, want, _ = run_both(b)
+    assert torch.isfinite(out.float()).all()
+    assert max_abs_err(out, want) <= TOL["bf16"]
+
+
+def test_more_new_tokens_than_length_is_rejected_on_device():
+    b = make_batch("f16", 64, 4, 4, 16, [0, 8], [4, 4], 51)
+    g = {k: v.to(DEV) for k, v in b.items() if isinstance(v, torch.Tensor)}
+    g["lens"][0] = 2                          # 4 new tokens but length 2
+    pa.pa_get_device_error()
+    pa.pa_multi_query_attention(g["q"], g["qsl"], g["kc"], g["vc"], g["tables"], g["lens"],
+                                b["scale"], 4, max_query_len=4, max_seq_len=12)
+    assert pa.pa_get_device_error() == -5
+
+
+def test_unsupported_dtype_and_block_are_refused():
+    b = make_batch("f16", 64, 4, 4, 4, [0], [2], 61)
+    g = {k: v.to(DEV) for k, v in b.items() if isinstance(v, torch.Tensor)}
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.pa_multi_query_attention(g["q"], g["qsl"], g["kc"], g["vc"], g["tables"], g["lens"],
+                                    b["scale"], 4, max_query_len=2, max_seq_len=2)
+    assert e.value.status == -2               # block size 4 < 8
