@@ -240,20 +240,37 @@ PA_API int pa_decode_attention_static(const void* q, const void* key_cache,
  * query_start_loc  int32 [num_seqs + 1], non-decreasing, device.
  * seq_lens         int32 [num_seqs], device; n_s <= L_s <= max_seq_len.
  * max_query_len    host upper bound of n_s (sizes the grid).
+ * num_tokens       host: rows of q (= query_start_loc[num_seqs]).
+ * partition_size   tokens per KV partition (split-K with a log-sum-exp
+ *                  combine); 0 splits only short query runs (every
+ *                  sequence's rows fit one 64-row tile), sized from the SM
+ *                  count. workspace as sized by pa_multi_query_workspace_bytes.
  * Other arguments as in pa_decode_attention. Supported: fp16/bf16,
  * head_size 64/128, block_size a power of two in [8, 256], group size
  * 1/2/4/8 (PA_ERR_SHAPE / PA_ERR_DTYPE otherwise). A sequence whose lengths
  * break these bounds is skipped (its rows are not written) and latches
- * PA_ERR_OUT_OF_RANGE. No workspace is needed.
+ * PA_ERR_OUT_OF_RANGE.
  */
 PA_API int pa_multi_query_attention(const void* q, const int32_t* query_start_loc,
-                                    int num_seqs, const void* key_cache,
-                                    const void* value_cache, const int32_t* block_tables,
+                                    int num_seqs, int64_t num_tokens,
+                                    const void* key_cache, const void* value_cache,
+                                    const int32_t* block_tables,
                                     int64_t block_tables_stride, const int32_t* seq_lens,
                                     int num_q_heads, int num_kv_heads, int head_size,
                                     int block_size, int64_t num_blocks, int dtype,
                                     float scale, int max_query_len, int max_seq_len,
-                                    void* out, void* stream);
+                                    int partition_size, void* out, void* workspace,
+                                    int64_t workspace_bytes, void* stream);
+
+/*
+ * Scratch bytes pa_multi_query_attention needs for these sizes (0: none,
+ * NULL may be passed); negative status on invalid sizes.
+ */
+PA_API int64_t pa_multi_query_workspace_bytes(int64_t num_tokens, int num_seqs,
+                                              int num_q_heads, int num_kv_heads,
+                                              int head_size, int block_size,
+                                              int max_query_len, int max_seq_len,
+                                              int partition_size);
 
 /*
  * pa_copy_blocks — block-level copy-on-write data movement ([P2] Figure 8:

@@ -38,9 +38,10 @@ SIGNATURES = {
     "pa_decode_attention_static": ([_c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32,
                                     _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32,
                                     _c_i32, _c_p, _c_p], _c_i32),
-    "pa_multi_query_attention": ([_c_p, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32,
-                                  _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32,
-                                  _c_i32, _c_p, _c_p], _c_i32),
+    "pa_multi_query_attention": ([_c_p, _c_p, _c_i32, _c_i64, _c_p, _c_p, _c_p, _c_i64, _c_p,
+                                  _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f,
+                                  _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i64, _c_p], _c_i32),
+    "pa_multi_query_workspace_bytes": ([_c_i64] + [_c_i32] * 8, _c_i64),
     "pa_copy_blocks": ([_c_p, _c_p, _c_i32, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p], _c_i32),
     "pa_get_device_error": ([_c_p, _c_p], _c_i32),
     "pa_map_to_kernel_blocks": ([_c_p, _c_i64, _c_i64, _c_i64, _c_i32, _c_p, _c_i64, _c_p],

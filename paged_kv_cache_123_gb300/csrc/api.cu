@@ -259,21 +259,78 @@ int pa_decode_attention(const void* q, const void* key_cache, const void* value_
   return check_launch(pa::launch_decode(a, (cudaStream_t)stream));
 }
 
-int pa_multi_query_attention(const void* q, const int32_t* query_start_loc, int num_seqs,
-                             const void* key_cache, const void* value_cache,
-                             const int32_t* block_tables, int64_t block_tables_stride,
-                             const int32_t* seq_lens, int num_q_heads, int num_kv_heads,
-                             int head_size, int block_size, int64_t num_blocks, int dtype,
-                             float scale, int max_query_len, int max_seq_len, void* out,
-                             void* stream) {
-  if (dtype != PA_F16 && dtype != PA_BF16) return elt_bytes(dtype) ? PA_ERR_SHAPE : PA_ERR_DTYPE;
+// Context partitions of the multi-query kernel. Only short query runs
+// (every sequence's rows fit one 64-row tile) are split: long prefill chunks
+// already give many row tiles. The length is picked as for the decode
+// tensor-core kernel (two waves of resident CTAs, 256..2048 tokens).
+static void mq_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
+                     int max_query_len, int max_seq_len, int partition_size, int sm_count,
+                     int* splits, int* tokens) {
+  const int g = num_q_heads / num_kv_heads;
+  const int64_t tile = block_size > 64 ? block_size : 64;
+  const int64_t len = max_seq_len > 0 ? max_seq_len : 1;
+  auto round_up = [tile](int64_t x) { return (x + tile - 1) / tile * tile; };
+  int64_t P;
+  if (partition_size > 0) {
+    P = round_up(partition_size);
+  } else if ((int64_t)max_query_len * g > 64) {
+    P = round_up(len);
+  } else {
+    const int64_t ctas = (int64_t)num_seqs * num_kv_heads;
+    const int64_t target = 2 * (int64_t)sm_count * 2;
+    P = round_up((len * (ctas > 0 ? ctas : 1) + target - 1) / target);
+    if (P < round_up(256)) P = round_up(256);
+    if (P > round_up(2048)) P = round_up(2048);
+  }
+  if (P > len) P = round_up(len);
+  *tokens = (int)P;
+  *splits = (int)((len + P - 1) / P);
+}
+
+static int check_mq_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+                   int block_size, int max_query_len, int max_seq_len) {
   int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
                               max_seq_len);
   if (st != PA_OK) return st;
-  if (block_size < 8 || max_query_len < 0 || num_blocks < 0 || block_tables_stride < 0)
+  if (block_size < 8 || max_query_len < 0) return PA_ERR_SHAPE;
+  if ((int64_t)max_query_len * (num_q_heads / num_kv_heads) > 0x7fffffffll) return PA_ERR_SHAPE;
+  return PA_OK;
+}
+
+int64_t pa_multi_query_workspace_bytes(int64_t num_tokens, int num_seqs, int num_q_heads,
+                                       int num_kv_heads, int head_size, int block_size,
+                                       int max_query_len, int max_seq_len, int partition_size) {
+  int st = check_mq_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                          max_query_len, max_seq_len);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0 || partition_size < 0) return PA_ERR_SHAPE;
+  int dev;
+  st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  int splits, tokens;
+  mq_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_query_len, max_seq_len,
+                  partition_size, g_sm_count[dev], &splits, &tokens);
+  if (splits <= 1) return 0;
+  const int64_t n = num_tokens * num_q_heads * splits;
+  return ((n * head_size * 4 + 255) / 256) * 256 + n * 2 * 4;
+}
+
+int pa_multi_query_attention(const void* q, const int32_t* query_start_loc, int num_seqs,
+                             int64_t num_tokens, const void* key_cache, const void* value_cache,
+                             const int32_t* block_tables, int64_t block_tables_stride,
+                             const int32_t* seq_lens, int num_q_heads, int num_kv_heads,
+                             int head_size, int block_size, int64_t num_blocks, int dtype,
+                             float scale, int max_query_len, int max_seq_len,
+                             int partition_size, void* out, void* workspace,
+                             int64_t workspace_bytes, void* stream) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return elt_bytes(dtype) ? PA_ERR_SHAPE : PA_ERR_DTYPE;
+  int st = check_mq_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                          max_query_len, max_seq_len);
+  if (st != PA_OK) return st;
+  if (num_blocks < 0 || block_tables_stride < 0 || num_tokens < 0 || partition_size < 0)
     return PA_ERR_SHAPE;
   if ((int64_t)max_seq_len > block_tables_stride * block_size) return PA_ERR_OUT_OF_RANGE;
-  if (num_seqs == 0 || max_query_len == 0) return PA_OK;
+  if (num_seqs == 0 || max_query_len == 0 || num_tokens == 0) return PA_OK;
   if (!q || !query_start_loc || !key_cache || !value_cache || !block_tables || !seq_lens || !out)
     return PA_ERR_NULL;
   if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) || !aligned16(out))
@@ -282,12 +339,23 @@ int pa_multi_query_attention(const void* q, const int32_t* query_start_loc, int 
   st = device_setup(&dev);
   if (st != PA_OK) return st;
   pa::MultiQueryArgs a;
-  a.q = q; a.qsl = query_start_loc; a.num_seqs = num_seqs;
+  a.q = q; a.qsl = query_start_loc; a.num_seqs = num_seqs; a.num_tokens = num_tokens;
   a.kc = key_cache; a.vc = value_cache; a.tables = block_tables;
   a.table_stride = block_tables_stride; a.seq_lens = seq_lens;
   a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads; a.head_size = head_size;
   a.block_size = block_size; a.num_blocks = num_blocks; a.dtype = dtype; a.scale = scale;
   a.max_query_len = max_query_len; a.max_seq_len = max_seq_len; a.out = out;
+  mq_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_query_len, max_seq_len,
+                  partition_size, g_sm_count[dev], &a.num_splits, &a.partition);
+  a.ws_acc = nullptr; a.ws_ml = nullptr;
+  if (a.num_splits > 1) {
+    const int64_t n = num_tokens * num_q_heads * a.num_splits;
+    const int64_t acc = ((n * head_size * 4 + 255) / 256) * 256;
+    if (!workspace || workspace_bytes < acc + n * 8) return PA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PA_ERR_ALIGN;
+    a.ws_acc = static_cast<float*>(workspace);
+    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc);
+  }
   a.err = g_err_ptr[dev];
   return check_launch(pa::launch_multi_query(a, (cudaStream_t)stream));
 }

@@ -83,7 +83,12 @@ struct MultiQueryArgs {
   int dtype;
   float scale;
   int max_query_len, max_seq_len;
+  int64_t num_tokens;  // rows of q / out
+  int partition;       // tokens per KV partition
+  int num_splits;      // ceil(max_seq_len / partition)
   void* out;
+  float* ws_acc;       // [num_tokens][Hq][num_splits][D]   (num_splits > 1)
+  float* ws_ml;        // [num_tokens][Hq][num_splits][2]
   int* err;
 };
 cudaError_t launch_multi_query(const MultiQueryArgs& a, cudaStream_t st);

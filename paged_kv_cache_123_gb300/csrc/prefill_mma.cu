@@ -41,8 +41,8 @@ constexpr long long kMqWaitCycles = 4000000000LL;
 // kv head): lane p issues the TMA loads of the tile's block-piece p.
 template <int ROW_BYTES, int KV_BYTES, int STAGE_BYTES>
 __device__ void mq_produce(const MultiQueryArgs& a, const CUtensorMap* tmK,
-                           const CUtensorMap* tmV, const int32_t* trow, int kvh, int kv_end,
-                           int ntiles, uint32_t smem0, uint32_t bar0, unsigned* tile_mask,
+                           const CUtensorMap* tmV, const int32_t* trow, int kvh, int kv_lo,
+                           int kv_end, int ntiles, uint32_t smem0, uint32_t bar0, unsigned* tile_mask,
                            volatile int* abort_flag, int lane) {
   const int B = a.block_size;
   const int bshift = __ffs(B) - 1;
@@ -55,7 +55,7 @@ __device__ void mq_produce(const MultiQueryArgs& a, const CUtensorMap* tmK,
   int issued = 0;
   for (int i = 0; i < ntiles; ++i) {
     const int st = i % kMqStages;
-    const int ts = i * kMqTile;
+    const int ts = kv_lo + i * kMqTile;
     const int te = min(kv_end, ts + kMqTile);
     const int tok = ts + lane * R;
     int64_t blk = -1;
@@ -113,7 +113,9 @@ multi_query_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMap t
   const uint32_t smem0 = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
 
-  const int s = blockIdx.z, kvh = blockIdx.y, qt = blockIdx.x;
+  const int s = blockIdx.z, kvh = blockIdx.y;
+  const int row_tiles = (a.max_query_len * G + kMqTile - 1) / kMqTile;
+  const int qt = blockIdx.x % row_tiles, split = blockIdx.x / row_tiles;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = a.num_q_heads;
   const int q0 = a.qsl[s];
@@ -121,14 +123,17 @@ multi_query_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMap t
   const int L = a.seq_lens[s];
   if (n < 0 || n > a.max_query_len || L < n || L > a.max_seq_len ||
       (int64_t)L > a.table_stride * a.block_size || q0 < 0) {
-    if (qt == 0 && kvh == 0 && threadIdx.x == 0) latch(a.err, PA_ERR_OUT_OF_RANGE);
+    if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) latch(a.err, PA_ERR_OUT_OF_RANGE);
     return;
   }
   const int r0 = qt * kMqTile;                       // first row of this CTA
   if (r0 >= n * G) return;
   const int i_last = min(n - 1, (r0 + kMqTile - 1) / G);
-  const int kv_end = L - n + i_last + 1;             // keys any row here may see
-  const int ntiles = (kv_end + kMqTile - 1) / kMqTile;
+  const int kv_all = L - n + i_last + 1;             // keys any row here may see
+  const int kv_lo = split * a.partition;             // this CTA's partition
+  if (kv_lo >= kv_all) return;
+  const int kv_end = min(kv_all, kv_lo + a.partition);
+  const int ntiles = (kv_end - kv_lo + kMqTile - 1) / kMqTile;
   const int32_t* trow = a.tables + (int64_t)s * a.table_stride;
 
   if (threadIdx.x == 0) {
@@ -142,7 +147,7 @@ multi_query_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMap t
   __syncthreads();
 
   if (warp == kMqConsumers) {
-    mq_produce<ROW_BYTES, KV_BYTES, STAGE_BYTES>(a, &tmK, &tmV, trow, kvh, kv_end, ntiles,
+    mq_produce<ROW_BYTES, KV_BYTES, STAGE_BYTES>(a, &tmK, &tmV, trow, kvh, kv_lo, kv_end, ntiles,
                                                  smem0, bar0, tile_mask, abort_flag, lane);
     __syncthreads();
     if (*abort_flag && lane == 0) latch(a.err, PA_ERR_TIMEOUT);
@@ -200,7 +205,7 @@ multi_query_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMap t
     const int st = i % kMqStages;
     if (!mbar_wait_bounded(bar0 + 8u * st, (i / kMqStages) & 1, abort_flag, kMqWaitCycles))
       break;
-    const int ts = i * kMqTile;
+    const int ts = kv_lo + i * kMqTile;
     const int te = min(kv_end, ts + kMqTile);
     const uint32_t kst = smem0 + st * STAGE_BYTES;
     const uint32_t vst = kst + KV_BYTES;
@@ -307,14 +312,64 @@ multi_query_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMap t
   for (int h = 0; h < 2; ++h) {
     if (!rv[h]) continue;
     const int r = rw0 + n8 + 8 * h;
-    const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
-    T* op = out + ((int64_t)(q0 + r / G) * Hq + (int64_t)kvh * G + r % G) * D;
+    const int64_t t = q0 + r / G;
+    const int head = kvh * G + r % G;
+    const int count = (pos[h] + a.partition) / a.partition;   // partitions holding its keys
+    if (count == 1) {
+      if (split != 0) continue;
+      const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+      T* op = out + (t * Hq + head) * D;
 #pragma unroll
-    for (int j = 0; j < DN; ++j) {
-      const uint32_t v = MmaOps<T>::pack(o[j][2 * h] * inv, o[j][2 * h + 1] * inv);
-      *reinterpret_cast<uint32_t*>(op + j * 8 + 2 * c) = v;
+      for (int j = 0; j < DN; ++j) {
+        const uint32_t v = MmaOps<T>::pack(o[j][2 * h] * inv, o[j][2 * h + 1] * inv);
+        *reinterpret_cast<uint32_t*>(op + j * 8 + 2 * c) = v;
+      }
+    } else if (split < count) {
+      const int64_t slot = (t * Hq + head) * a.num_splits + split;
+      float* acc = a.ws_acc + slot * D;
+#pragma unroll
+      for (int j = 0; j < DN; ++j)
+        *reinterpret_cast<float2*>(acc + j * 8 + 2 * c) = make_float2(o[j][2 * h], o[j][2 * h + 1]);
+      if (c == 0) {
+        a.ws_ml[2 * slot] = m[h];
+        a.ws_ml[2 * slot + 1] = l[h];
+      }
     }
   }
+}
+
+// Log-sum-exp merge of the partitions of one (new token, query head) row;
+// rows whose keys fit one partition were written by the attention kernel.
+template <typename T, int D>
+__global__ void __launch_bounds__(D) mq_combine_kernel(const MultiQueryArgs a) {
+  const int64_t t = blockIdx.x;
+  const int head = blockIdx.y, d = threadIdx.x;
+  int lo = 0, hi = a.num_seqs + 1;              // owning sequence of row t
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)a.qsl[mid] <= t) lo = mid + 1; else hi = mid;
+  }
+  const int s = lo - 1;
+  if (s < 0 || s >= a.num_seqs) return;
+  const int q0 = a.qsl[s], n = a.qsl[s + 1] - q0, L = a.seq_lens[s];
+  if (n < 0 || n > a.max_query_len || L < n || L > a.max_seq_len ||
+      (int64_t)L > a.table_stride * a.block_size || q0 < 0)
+    return;
+  const int pos = L - n + (int)(t - q0);
+  const int count = (pos + a.partition) / a.partition;
+  if (count <= 1) return;
+  const int64_t base = (t * a.num_q_heads + head) * a.num_splits;
+  float M = kNegInfQ;
+  for (int p = 0; p < count; ++p) M = fmaxf(M, a.ws_ml[2 * (base + p)]);
+  float Ls = 0.f, O = 0.f;
+  for (int p = 0; p < count; ++p) {
+    const float mp = a.ws_ml[2 * (base + p)];
+    const float w = (mp == kNegInfQ) ? 0.f : exp2f(mp - M);
+    Ls += a.ws_ml[2 * (base + p) + 1] * w;
+    O += a.ws_acc[(base + p) * D + d] * w;
+  }
+  T* out = reinterpret_cast<T*>(a.out);
+  out[(t * a.num_q_heads + head) * D + d] = Vec<T>::cvt_out(Ls > 0.f ? O / Ls : 0.f);
 }
 
 }  // namespace
@@ -346,8 +401,13 @@ cudaError_t launch_mq_tdg(const MultiQueryArgs& a, cudaStream_t st) {
   const int64_t rows = (int64_t)a.max_query_len * G;
   const int64_t tiles = (rows + kMqTile - 1) / kMqTile;
   if (tiles == 0 || a.num_seqs == 0) return cudaSuccess;
-  dim3 grid((unsigned)tiles, a.num_kv_heads, a.num_seqs);
+  dim3 grid((unsigned)(tiles * a.num_splits), a.num_kv_heads, a.num_seqs);
   multi_query_kernel<T, D, G><<<grid, kMqThreads, smem, st>>>(a, tk, tv);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.num_splits <= 1) return e;
+  if (a.num_tokens > 0x7fffffffLL) return cudaErrorInvalidValue;
+  dim3 cgrid((unsigned)a.num_tokens, a.num_q_heads);
+  mq_combine_kernel<T, D><<<cgrid, D, 0, st>>>(a);
   return cudaGetLastError();
 }
 

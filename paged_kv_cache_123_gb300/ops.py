@@ -172,11 +172,24 @@ def pa_map_to_kernel_blocks(manager_table: torch.Tensor, blocks_per_kv_block: in
     return kernel_table
 
 
+def pa_multi_query_workspace_bytes(num_tokens: int, num_seqs: int, num_q_heads: int,
+                                   num_kv_heads: int, head_size: int, block_size: int,
+                                   max_query_len: int, max_seq_len: int,
+                                   partition_size: int = 0) -> int:
+    n = lib().pa_multi_query_workspace_bytes(num_tokens, num_seqs, num_q_heads, num_kv_heads,
+                                             head_size, block_size, max_query_len,
+                                             max_seq_len, partition_size)
+    if n < 0:
+        check("pa_multi_query_workspace_bytes", int(n))
+    return int(n)
+
+
 def pa_multi_query_attention(q: torch.Tensor, query_start_loc: torch.Tensor,
                              key_cache: torch.Tensor, value_cache: torch.Tensor,
                              block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
                              num_kv_heads: int, out: Optional[torch.Tensor] = None, *,
-                             max_query_len: int, max_seq_len: int,
+                             max_query_len: int, max_seq_len: int, partition_size: int = 0,
+                             workspace: Optional[torch.Tensor] = None,
                              stream=None) -> torch.Tensor:
     """Causal paged attention of several new tokens per sequence.
     q/out [T, Hq, D] with T = query_start_loc[-1]; pools [NB, Hkv, B, D]."""
@@ -192,9 +205,15 @@ def pa_multi_query_attention(q: torch.Tensor, query_start_loc: torch.Tensor,
     if out is None:
         out = torch.empty_like(q)
     _dev(out, "out")
+    S = query_start_loc.numel() - 1
+    need = pa_multi_query_workspace_bytes(T, S, Hq, Hkv, D, B, max_query_len, max_seq_len,
+                                          partition_size)
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     check("pa_multi_query_attention", lib().pa_multi_query_attention(
-        ptr(q), ptr(query_start_loc), query_start_loc.numel() - 1, ptr(key_cache),
-        ptr(value_cache), ptr(block_tables), block_tables.shape[1], ptr(seq_lens), Hq, Hkv, D,
-        B, NB, DTYPE_CODE[q.dtype], float(scale), int(max_query_len), int(max_seq_len),
-        ptr(out), stream_handle(stream)))
+        ptr(q), ptr(query_start_loc), S, T, ptr(key_cache), ptr(value_cache), ptr(block_tables),
+        block_tables.shape[1], ptr(seq_lens), Hq, Hkv, D, B, NB, DTYPE_CODE[q.dtype],
+        float(scale), int(max_query_len), int(max_seq_len), int(partition_size), ptr(out),
+        ptr(workspace), ws_bytes, stream_handle(stream)))
     return out

@@ -42,7 +42,7 @@ def make_batch(dtype, D, hq, hkv, B, ctx, n_new, seed):
                 scale=D ** -0.5, max_q=max(n_new), max_len=max(lens))
 
 
-def run_both(b):
+def run_both(b, partition=0):
     kco, vco = np_(b["kc"]), np_(b["vc"])
     slots_o = oracle.slot_mapping(b["qsl"].numpy(), b["pos"].numpy(), b["tables"].numpy(), b["B"])
     oracle.reshape_and_cache(np_(b["kn"]), np_(b["vn"]), slots_o, kco, vco, b["B"])
@@ -54,7 +54,7 @@ def run_both(b):
     pa.pa_reshape_and_cache(g["kn"], g["vn"], slots, g["kc"], g["vc"])
     out = pa.pa_multi_query_attention(g["q"], g["qsl"], g["kc"], g["vc"], g["tables"], g["lens"],
                                       b["scale"], b["hkv"], max_query_len=b["max_q"],
-                                      max_seq_len=b["max_len"])
+                                      max_seq_len=b["max_len"], partition_size=partition)
     torch.cuda.synchronize()
     assert np.array_equal(slots.cpu().numpy(), slots_o)
     return out, want, g
@@ -122,3 +122,26 @@ def test_unsupported_dtype_and_block_are_refused():
         pa.pa_multi_query_attention(g["q"], g["qsl"], g["kc"], g["vc"], g["tables"], g["lens"],
                                     b["scale"], 4, max_query_len=2, max_seq_len=2)
     assert e.value.status == -2               # block size 4 < 8
+
+
+@pytest.mark.parametrize("partition", [64, 192, 1024])
+@pytest.mark.parametrize("dtype,G,n_new", [("bf16", 8, [4, 1, 3, 2]), ("f16", 1, [7, 1, 30, 2]),
+                                           ("bf16", 4, [40, 1, 100, 9])])
+def test_split_partitions_with_combine(partition, dtype, G, n_new):
+    """KV split into partitions, partials merged by log-sum-exp; rows whose
+    visible keys fit one partition bypass the merge."""
+    b = make_batch(dtype, 128, 2 * G, 2, 16, [900, 0, 2000, 63], n_new, 71)
+    out, want, _ = run_both(b, partition)
+    need = pa.pa_multi_query_workspace_bytes(sum(n_new), 4, 2 * G, 2, 128, 16, b["max_q"],
+                                             b["max_len"], partition)
+    assert need > 0
+    assert max_abs_err(out, want) <= TOL[dtype]
+    assert pa.pa_get_device_error() == 0
+
+
+def test_short_query_runs_split_automatically():
+    b = make_batch("bf16", 128, 16, 2, 16, [3000, 5000, 100], [4, 4, 4], 81)
+    need = pa.pa_multi_query_workspace_bytes(12, 3, 16, 2, 128, 16, 4, b["max_len"], 0)
+    assert need > 0                      # few CTAs without splits: the library splits
+    out, want, _ = run_both(b)
+    assert max_abs_err(out, want) <= TOL["bf16"]
