@@ -22,6 +22,7 @@ from .paged_attention import (  # noqa: F401
     decode_attention, decode_attention_one, decode_step, blocks_needed,
     slots_allocated,
     fragmentation, kv_bytes_per_token, sharing_saving, map_to_kernel_blocks,
-    multi_query_attention,
+    multi_query_attention, e4m3_decode, e4m3_encode, quantize_e4m3, reshape_and_cache_fp8,
+    decode_attention_fp8,
 )
 from .block_manager import OracleBlockManager  # noqa: F401

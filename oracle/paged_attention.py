@@ -296,3 +296,87 @@ def multi_query_attention(q, key_cache, value_cache, block_tables, query_start_l
                     out[qsl[s] + i, h] = decode_attention_one(
                         q64[qsl[s] + i, h], K[:last + 1], V[:last + 1], scale)
     return out
+
+
+# --------------------------------------------------------------------------
+# fp8 (e4m3) KV blocks ([P1] §3.5 AttentionSpec.kv_quant_mode; §7 outlook on
+# quantisation-aware blocks). The pages fix no format; the reading taken is
+# OCP FP8 E4M3 codes with one fp32 scale per pool (K and V each):
+#     code = e4m3(x / scale) with round-to-nearest-even and saturation to
+#            +-448; value = decode(code) * scale.
+# --------------------------------------------------------------------------
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of E4M3 codes (sign, 4 exponent bits with bias 7, 3 mantissa
+    bits; exponent 0 is subnormal m * 2^-9; S.1111.111 is NaN)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = sign * val
+    return np.where((c & 0x7F) == 0x7F, np.nan, val)
+
+
+def e4m3_encode(x32) -> np.ndarray:
+    """Nearest E4M3 code of float32 values, ties to the even code, values
+    beyond the largest finite magnitude (448) saturate to it, NaN -> 0x7F."""
+    x = np.asarray(x32, dtype=np.float32).astype(np.float64)
+    out = np.zeros(x.shape, dtype=np.uint8)
+    flat, res = x.reshape(-1), out.reshape(-1)
+    for idx, v in enumerate(flat):
+        if np.isnan(v):
+            res[idx] = 0x7F
+            continue
+        s = 0x80 if np.signbit(v) else 0
+        a = abs(v)
+        if a >= 448.0:
+            res[idx] = s | 0x7E
+            continue
+        if a < 2.0 ** -6:                           # subnormal range
+            q = int(np.rint(a / 2.0 ** -9))         # 8 becomes the smallest normal
+            res[idx] = s | q
+            continue
+        mant, exp = np.frexp(a)                     # a = mant * 2^exp, mant in [0.5, 1)
+        e = exp - 1                                 # a = (2 * mant) * 2^e
+        q = int(np.rint((2.0 * mant - 1.0) * 8.0))
+        if q == 8:
+            e, q = e + 1, 0
+        code = ((e + 7) << 3) | q
+        res[idx] = s | min(code, 0x7E)
+    return out
+
+
+def quantize_e4m3(x, dtype: str, scale: float) -> np.ndarray:
+    """Codes for stored values x: widened exactly to fp32, divided by the fp32
+    scale with fp32 rounding, then encoded."""
+    x32 = upcast(x, dtype).astype(np.float32)
+    return e4m3_encode(x32 / np.float32(scale))
+
+
+def reshape_and_cache_fp8(k, v, slots, key_cache8, value_cache8, block_size: int,
+                          dtype: str, k_scale: float, v_scale: float):
+    """KV write into e4m3 pools: quantise, then the same slot placement as
+    reshape_and_cache."""
+    reshape_and_cache(quantize_e4m3(k, dtype, k_scale), quantize_e4m3(v, dtype, v_scale),
+                      slots, key_cache8, value_cache8, block_size)
+
+
+def decode_attention_fp8(q, key_cache8, value_cache8, block_tables, seq_lens, scale: float,
+                         num_kv_heads: int, block_size: int, dtype: str, k_scale: float,
+                         v_scale: float, seqs=None, heads=None) -> np.ndarray:
+    """Decode attention over e4m3 pools: K = decode(code) * k_scale and
+    V = decode(code) * v_scale exactly in fp64, then decode_attention."""
+    S, Hq, D = q.shape
+    g = Hq // num_kv_heads
+    q64 = upcast(q, dtype)
+    out = np.zeros((S, Hq, D), dtype=np.float64)
+    for s in (range(S) if seqs is None else seqs):
+        L = int(seq_lens[s])
+        j = np.arange(L)
+        blk = np.asarray(block_tables[s], dtype=np.int64)[j // block_size]
+        for h in (range(Hq) if heads is None else heads):
+            kvh = h // g
+            K = e4m3_decode(key_cache8[blk, kvh, j % block_size, :]) * np.float64(np.float32(k_scale))
+            V = e4m3_decode(value_cache8[blk, kvh, j % block_size, :]) * np.float64(np.float32(v_scale))
+            out[s, h] = decode_attention_one(q64[s, h], K, V, scale)
+    return out
