@@ -273,6 +273,39 @@ PA_API int64_t pa_multi_query_workspace_bytes(int64_t num_tokens, int num_seqs,
                                               int partition_size);
 
 /*
+ * fp8 KV pools ([P1] §3.5: an attention layer's KV spec carries a
+ * quantisation mode; §7 outlook: quantisation-aware blocks). The pages fix no
+ * format; this library stores OCP FP8 E4M3 codes (1 byte, same pool layout)
+ * with one fp32 scale per pool:
+ *     code  = e4m3(x / scale)   nearest even, saturated to +-448, NaN -> NaN
+ *     value = code * scale
+ *
+ * pa_reshape_and_cache_fp8 — pa_reshape_and_cache into fp8 pools: k, v of
+ * `dtype` (fp32/fp16/bf16) are divided by k_scale / v_scale in fp32 and
+ * converted; head_size a multiple of 16; scales > 0.
+ */
+PA_API int pa_reshape_and_cache_fp8(const void* k, const void* v, int64_t num_tokens,
+                                    int num_kv_heads, int head_size, int dtype,
+                                    const int64_t* slot_mapping, void* key_cache,
+                                    void* value_cache, int64_t num_blocks, int block_size,
+                                    float k_scale, float v_scale, void* stream);
+
+/*
+ * pa_decode_attention_fp8 — pa_decode_attention over fp8 pools: q and out of
+ * `dtype`, K = code * k_scale, V = code * v_scale. Same partitioning and
+ * workspace as pa_decode_attention (pa_decode_workspace_bytes applies).
+ * Runs on the CUDA cores for every group size.
+ */
+PA_API int pa_decode_attention_fp8(const void* q, const void* key_cache,
+                                   const void* value_cache, const int32_t* block_tables,
+                                   int64_t block_tables_stride, const int32_t* seq_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_size, int block_size, int64_t num_blocks,
+                                   int dtype, float scale, float k_scale, float v_scale,
+                                   int max_seq_len, int partition_size, void* out,
+                                   void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
  * pa_copy_blocks — block-level copy-on-write data movement ([P2] Figure 8:
  * "copy physical block 1's content to physical block 3"; [P4] copy-on-write
  * figure). For every pair (src, dst) in src_dst_pairs and every layer l, the

@@ -42,6 +42,11 @@ SIGNATURES = {
                                   _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f,
                                   _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i64, _c_p], _c_i32),
     "pa_multi_query_workspace_bytes": ([_c_i64] + [_c_i32] * 8, _c_i64),
+    "pa_reshape_and_cache_fp8": ([_c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_p,
+                                  _c_i64, _c_i32, _c_f, _c_f, _c_p], _c_i32),
+    "pa_decode_attention_fp8": ([_c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32, _c_i32,
+                                 _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_f, _c_f, _c_i32,
+                                 _c_i32, _c_p, _c_p, _c_i64, _c_p], _c_i32),
     "pa_copy_blocks": ([_c_p, _c_p, _c_i32, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p], _c_i32),
     "pa_get_device_error": ([_c_p, _c_p], _c_i32),
     "pa_map_to_kernel_blocks": ([_c_p, _c_i64, _c_i64, _c_i64, _c_i32, _c_p, _c_i64, _c_p],

@@ -360,6 +360,71 @@ int pa_multi_query_attention(const void* q, const int32_t* query_start_loc, int 
   return check_launch(pa::launch_multi_query(a, (cudaStream_t)stream));
 }
 
+int pa_reshape_and_cache_fp8(const void* k, const void* v, int64_t num_tokens, int num_kv_heads,
+                             int head_size, int dtype, const int64_t* slot_mapping,
+                             void* key_cache, void* value_cache, int64_t num_blocks,
+                             int block_size, float k_scale, float v_scale, void* stream) {
+  if (elt_bytes(dtype) == 0) return PA_ERR_DTYPE;
+  if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks < 0 ||
+      head_size <= 0 || head_size % 16 != 0)
+    return PA_ERR_SHAPE;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f)) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !key_cache || !value_cache) return PA_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache))
+    return PA_ERR_ALIGN;
+  int dev;
+  int st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  return check_launch(pa::launch_reshape_and_cache_fp8(
+      k, v, num_tokens, num_kv_heads, head_size, dtype, slot_mapping, key_cache, value_cache,
+      num_blocks, block_size, k_scale, v_scale, (cudaStream_t)stream, g_err_ptr[dev]));
+}
+
+int pa_decode_attention_fp8(const void* q, const void* key_cache, const void* value_cache,
+                            const int32_t* block_tables, int64_t block_tables_stride,
+                            const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                            int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+                            int dtype, float scale, float k_scale, float v_scale,
+                            int max_seq_len, int partition_size, void* out, void* workspace,
+                            int64_t workspace_bytes, void* stream) {
+  if (elt_bytes(dtype) == 0) return PA_ERR_DTYPE;
+  int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                              max_seq_len);
+  if (st != PA_OK) return st;
+  if (partition_size < 0 || num_blocks < 0 || block_tables_stride < 0) return PA_ERR_SHAPE;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f)) return PA_ERR_SHAPE;
+  if ((int64_t)max_seq_len > block_tables_stride * block_size) return PA_ERR_OUT_OF_RANGE;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !key_cache || !value_cache || !block_tables || !seq_lens || !out) return PA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) || !aligned16(out))
+    return PA_ERR_ALIGN;
+  int dev;
+  st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  pa::DecodeArgs a;
+  a.q = q; a.kc = key_cache; a.vc = value_cache;
+  a.tables = block_tables; a.table_stride = block_tables_stride; a.seq_lens = seq_lens;
+  a.num_seqs = num_seqs; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size; a.block_size = block_size; a.num_blocks = num_blocks;
+  a.dtype = dtype; a.scale = scale; a.max_seq_len = max_seq_len;
+  partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size,
+               g_sm_count[dev], &a.num_splits, &a.partition);
+  const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);
+  a.ws_acc = nullptr; a.ws_ml = nullptr;
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PA_ERR_ALIGN;
+    const int64_t n = (int64_t)num_seqs * num_q_heads * a.num_splits;
+    a.ws_acc = static_cast<float*>(workspace);
+    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       ((n * head_size * 4 + 255) / 256) * 256);
+  }
+  a.out = out;
+  a.err = g_err_ptr[dev];
+  return check_launch(pa::launch_decode_fp8(a, k_scale, v_scale, (cudaStream_t)stream));
+}
+
 int pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                    const int64_t* src_dst_pairs, const int64_t* src_dst_pairs_host,
                    int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,

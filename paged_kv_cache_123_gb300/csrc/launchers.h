@@ -56,6 +56,15 @@ struct DecodeArgs {
 // query-head groups of 2, 4 or 8 with blocks of at least 8 tokens, the
 // CUDA-core kernel (decode_simt.cu) otherwise; then the split combine.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+// fp8 (E4M3) pools: quantising KV write, and decode attention (q/out dtype
+// in a.dtype, caches of 1-byte codes)
+cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, int64_t num_tokens,
+                                         int num_kv_heads, int head_size, int dtype,
+                                         const int64_t* slots, void* kc, void* vc,
+                                         int64_t num_blocks, int block_size, float k_scale,
+                                         float v_scale, cudaStream_t st, int* err);
+cudaError_t launch_decode_fp8(const DecodeArgs& a, float k_scale, float v_scale,
+                              cudaStream_t st);
 bool mma_path_applies(const DecodeArgs& a);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);

@@ -217,3 +217,49 @@ def pa_multi_query_attention(q: torch.Tensor, query_start_loc: torch.Tensor,
         float(scale), int(max_query_len), int(max_seq_len), int(partition_size), ptr(out),
         ptr(workspace), ws_bytes, stream_handle(stream)))
     return out
+
+
+def pa_reshape_and_cache_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                             key_cache: torch.Tensor, value_cache: torch.Tensor,
+                             k_scale: float, v_scale: float, stream=None) -> None:
+    """KV write into E4M3 pools (uint8 [NB, Hkv, B, D]): code = e4m3(x / scale)."""
+    for n, t in (("k", k), ("v", v), ("key_cache", key_cache), ("value_cache", value_cache)):
+        _dev(t, n)
+    _dev(slot_mapping, "slot_mapping", torch.int64)
+    if key_cache.dtype != torch.uint8 or value_cache.dtype != torch.uint8:
+        raise ValueError("fp8 pools are uint8 tensors of E4M3 codes")
+    NB, Hkv, B, D = key_cache.shape
+    check("pa_reshape_and_cache_fp8", lib().pa_reshape_and_cache_fp8(
+        ptr(k), ptr(v), k.shape[0], Hkv, D, DTYPE_CODE[k.dtype], ptr(slot_mapping),
+        ptr(key_cache), ptr(value_cache), NB, B, float(k_scale), float(v_scale),
+        stream_handle(stream)))
+
+
+def pa_decode_attention_fp8(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                            num_kv_heads: int, k_scale: float, v_scale: float,
+                            out: Optional[torch.Tensor] = None, *, max_seq_len: int,
+                            partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """Decode attention over E4M3 pools; q/out in fp32/fp16/bf16."""
+    for n, t in (("q", q), ("key_cache", key_cache), ("value_cache", value_cache)):
+        _dev(t, n)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = key_cache.shape
+    if Hkv != num_kv_heads or Dk != D or key_cache.dtype != torch.uint8:
+        raise ValueError("pools must be uint8 [NB, Hkv, B, D] matching q")
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out")
+    need = pa_decode_workspace_bytes(S, Hq, Hkv, D, B, max_seq_len, partition_size)
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check("pa_decode_attention_fp8", lib().pa_decode_attention_fp8(
+        ptr(q), ptr(key_cache), ptr(value_cache), ptr(block_tables), block_tables.shape[1],
+        ptr(seq_lens), S, Hq, Hkv, D, B, NB, DTYPE_CODE[q.dtype], float(scale), float(k_scale),
+        float(v_scale), int(max_seq_len), int(partition_size), ptr(out), ptr(workspace),
+        ws_bytes, stream_handle(stream)))
+    return out

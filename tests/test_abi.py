@@ -101,3 +101,26 @@ def test_map_to_kernel_blocks_host_checks(lib):
     assert lib.pa_map_to_kernel_blocks(p, 2, 3, 3, 2, p, 5, None) == -2     # stride too small
     assert lib.pa_map_to_kernel_blocks(None, 2, 3, 3, 2, p, 6, None) == -1
     assert lib.pa_map_to_kernel_blocks(p, 0, 3, 3, 2, p, 6, None) == 0      # nothing to do
+
+
+def test_fp8_and_multi_query_host_checks(lib):
+    p = ctypes.c_void_p(16)
+    f = ctypes.c_float
+    # fp8 write: bad scale, head size not a multiple of 16, unknown dtype
+    assert lib.pa_reshape_and_cache_fp8(p, p, 1, 1, 64, 1, p, p, p, 4, 4, f(0.0), f(1.0), None) == -2
+    assert lib.pa_reshape_and_cache_fp8(p, p, 1, 1, 72, 1, p, p, p, 4, 4, f(1.0), f(1.0), None) == -2
+    assert lib.pa_reshape_and_cache_fp8(p, p, 1, 1, 64, 9, p, p, p, 4, 4, f(1.0), f(1.0), None) == -3
+    # fp8 decode: negative scale, table too short
+    st = lib.pa_decode_attention_fp8(p, p, p, p, 4, p, 2, 4, 4, 64, 4, 8, 1, f(1.0), f(-1.0),
+                                     f(1.0), 16, 0, p, None, 0, None)
+    assert st == -2
+    st = lib.pa_decode_attention_fp8(p, p, p, p, 4, p, 2, 4, 4, 64, 4, 8, 1, f(1.0), f(1.0),
+                                     f(1.0), 17, 0, p, None, 0, None)
+    assert st == -5
+    # multi-query: fp32 refused, block size below 8 refused, nothing to do
+    args = lambda dt, B, mq: (p, p, 2, 4, p, p, p, 4, p, 4, 4, 64, B, 8, dt, f(1.0), mq, 16, 0,
+                              p, None, 0, None)
+    assert lib.pa_multi_query_attention(*args(0, 16, 2)) == -2
+    assert lib.pa_multi_query_attention(*args(1, 4, 2)) == -2
+    assert lib.pa_multi_query_attention(*args(1, 16, 0)) == 0
+    assert lib.pa_multi_query_workspace_bytes(8, 2, 48, 3, 128, 16, 4, 100, 0) == -2

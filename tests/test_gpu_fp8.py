@@ -1,0 +1,99 @@
+"""fp8 (E4M3) KV pools through the C ABI: the quantising KV write must give
+the oracle's codes bit for bit; decode attention over the codes must match the
+oracle's fp64 attention on the dequantised values."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_123_gb300 as pa
+from paged_kv_cache_123_gb300 import workloads
+from tests.helpers import TOL, max_abs_err, np_
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def fp8_pool(shape, scale, gen):
+    x = torch.randn(shape, generator=gen) / scale
+    return x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (1 / 64, 0.037), (3.3, 0.002)])
+def test_quantising_kv_write_bit_exact(dtype, k_scale, v_scale):
+    cfg = workloads.DecodeConfig("q8", 30, 8, 4, 128, 16, dtype, ctx_lo=0, ctx_hi=100, seed=9)
+    inp = workloads.make_decode_inputs(cfg)
+    gen = torch.Generator().manual_seed(3)
+    kc = fp8_pool((inp.num_blocks, 4, 16, 128), 1 / 64, gen)
+    vc = fp8_pool((inp.num_blocks, 4, 16, 128), 1 / 64, gen)
+    # include saturating inputs and exact zeros
+    k = inp.k_new.clone()
+    k[0, 0, :4] = torch.tensor([1e4, -1e4, 0.0, -0.0]).to(k.dtype)
+    slots = oracle.slot_mapping(inp.query_start_loc.numpy(), inp.positions.numpy(),
+                                inp.block_tables.numpy(), 16)
+    slots[3] = -1
+    ko, vo = kc.numpy().copy(), vc.numpy().copy()
+    oracle.reshape_and_cache_fp8(np_(k), np_(inp.v_new), slots, ko, vo, 16, dtype,
+                                 k_scale, v_scale)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    pa.pa_reshape_and_cache_fp8(k.to(DEV), inp.v_new.to(DEV), torch.from_numpy(slots).to(DEV),
+                                kd, vd, k_scale, v_scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(kd.cpu().numpy(), ko)
+    assert np.array_equal(vd.cpu().numpy(), vo)
+    assert pa.pa_get_device_error() == 0
+
+
+CASES = [(dt, G, 16, 0) for dt in ("f32", "f16", "bf16") for G in (1, 2, 4, 8)]
+CASES += [("bf16", 8, 1, 0), ("bf16", 8, 128, 0), ("f16", 1, 64, 192), ("bf16", 4, 16, 64)]
+
+
+@pytest.mark.parametrize("dtype,G,B,partition", CASES)
+def test_fp8_decode_matches_oracle(dtype, G, B, partition):
+    Hkv = 2
+    cfg = workloads.DecodeConfig("a8", 5, Hkv * G, Hkv, 128, B, dtype, seed=17 + G + B)
+    inp = workloads.make_decode_inputs(cfg, context_lens=[0, 15, 63, 200, 700])
+    gen = torch.Generator().manual_seed(G * 7 + B)
+    ks, vs = 1 / 48, 1 / 40
+    kc = fp8_pool((inp.num_blocks, Hkv, B, 128), ks, gen)
+    vc = fp8_pool((inp.num_blocks, Hkv, B, 128), vs, gen)
+    want = oracle.decode_attention_fp8(np_(inp.q), kc.numpy(), vc.numpy(),
+                                       inp.block_tables.numpy(), inp.seq_lens.numpy(),
+                                       inp.scale, Hkv, B, dtype, ks, vs)
+    out = pa.pa_decode_attention_fp8(inp.q.to(DEV), kc.to(DEV), vc.to(DEV),
+                                     inp.block_tables.to(DEV), inp.seq_lens.to(DEV), inp.scale,
+                                     Hkv, ks, vs, max_seq_len=inp.max_seq_len,
+                                     partition_size=partition)
+    torch.cuda.synchronize()
+    err = max_abs_err(out, want)
+    assert err <= TOL[dtype], err
+    assert pa.pa_get_device_error() == 0
+
+
+def test_fp8_full_step_against_oracle():
+    """slot mapping, quantising write of the new token, fp8 attention that
+    includes it."""
+    cfg = workloads.DecodeConfig("s8", 6, 32, 8, 128, 16, "bf16", ctx_lo=1, ctx_hi=3000, seed=23)
+    inp = workloads.make_decode_inputs(cfg)
+    gen = torch.Generator().manual_seed(5)
+    ks, vs = 1 / 50, 1 / 50
+    kc = fp8_pool((inp.num_blocks, 8, 16, 128), ks, gen)
+    vc = fp8_pool((inp.num_blocks, 8, 16, 128), vs, gen)
+    ko, vo = kc.numpy().copy(), vc.numpy().copy()
+    slots_o = oracle.slot_mapping(inp.query_start_loc.numpy(), inp.positions.numpy(),
+                                  inp.block_tables.numpy(), 16)
+    oracle.reshape_and_cache_fp8(np_(inp.k_new), np_(inp.v_new), slots_o, ko, vo, 16, "bf16",
+                                 ks, vs)
+    want = oracle.decode_attention_fp8(np_(inp.q), ko, vo, inp.block_tables.numpy(),
+                                       inp.seq_lens.numpy(), inp.scale, 8, 16, "bf16", ks, vs)
+    g = {k: getattr(inp, k).to(DEV) for k in ("q", "k_new", "v_new", "block_tables", "seq_lens",
+                                              "positions", "query_start_loc")}
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    slots = pa.pa_compute_slot_mapping(g["query_start_loc"], g["positions"], g["block_tables"], 16)
+    pa.pa_reshape_and_cache_fp8(g["k_new"], g["v_new"], slots, kd, vd, ks, vs)
+    out = pa.pa_decode_attention_fp8(g["q"], kd, vd, g["block_tables"], g["seq_lens"], inp.scale,
+                                     8, ks, vs, max_seq_len=inp.max_seq_len)
+    torch.cuda.synchronize()
+    assert np.array_equal(kd.cpu().numpy(), ko) and np.array_equal(vd.cpu().numpy(), vo)
+    assert max_abs_err(out, want) <= TOL["bf16"]
