@@ -41,21 +41,29 @@ constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 #define kNegInfM (-__int_as_float(0x7f800000))
 
 
-template <typename T, int D, int G>
+// KV8 = the pools hold fp8 (E4M3) codes: TMA brings the codes (unswizzled,
+// D bytes per row); each consumer warp widens its own 16 rows into a private
+// 16-bit tile in the swizzled layout below, releases the stage, and runs the
+// same tensor-core code on the private tile. k_scale / v_scale are the
+// pools' scales (1 for 16-bit pools).
+template <typename T, int D, int G, bool KV8>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV) {
-  constexpr int HALVES = D / 64;                 // 128-byte lines per token row
-  constexpr int ROW_BYTES = HALVES * 128;        // one token row (D * 2 bytes)
-  constexpr int KV_BYTES = kTile * ROW_BYTES;    // K (or V) part of a stage
+                  const __grid_constant__ CUtensorMap tmV, float k_scale, float v_scale) {
+  constexpr int HALVES = D / 64;                 // 128-byte lines per 16-bit token row
+  constexpr int ROW_BYTES = HALVES * 128;        // one 16-bit token row (D * 2 bytes)
+  constexpr int IN_ROW = KV8 ? D : ROW_BYTES;    // one token row as loaded
+  constexpr int KV_BYTES = kTile * IN_ROW;       // K (or V) part of a stage
   constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  constexpr int PRIV_BYTES = KV8 ? 2 * 16 * ROW_BYTES : 0;   // per consumer warp
   constexpr int KSTEPS = D / 16;
   static_assert(G == 2 || G == 4 || G == 8, "group");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * STAGE_BYTES +
+                                                kMmaConsumers * PRIV_BYTES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
   // bit p set = piece p of the stage's tile was loaded (written by the
   // producer before it arms the stage's full barrier)
@@ -135,18 +143,23 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           ok = mbar_wait_bounded(empty_bar(st), ((i / kStages) - 1) & 1, abort_flag, kWaitCycles);
         if (ok) {
           tile_mask[st] = pm;
-          mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * ROW_BYTES);
+          mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * IN_ROW);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if (mine) {
-        const uint32_t kdst = smem0 + st * STAGE_BYTES + lane * R * ROW_BYTES;
+        const uint32_t kdst = smem0 + st * STAGE_BYTES + lane * R * IN_ROW;
         const uint32_t vdst = kdst + KV_BYTES;
         const int z = (int)(blk * Hkv + kvh);
         const int y = tok & (B - 1);
-        tma_load_4d(kdst, &tmK, 0, 0, y, z, full_bar(st));
-        tma_load_4d(vdst, &tmV, 0, 0, y, z, full_bar(st));
+        if (KV8) {
+          tma_load_3d(kdst, &tmK, 0, y, z, full_bar(st));
+          tma_load_3d(vdst, &tmV, 0, y, z, full_bar(st));
+        } else {
+          tma_load_4d(kdst, &tmK, 0, 0, y, z, full_bar(st));
+          tma_load_4d(vdst, &tmV, 0, 0, y, z, full_bar(st));
+        }
       }
       issued = i + 1;
     }
@@ -170,7 +183,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         }
       }
     }
-    const float sl2 = a.scale * kLog2e;
+    const float sl2 = a.scale * kLog2e * k_scale;
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % kStages;
       if (!mbar_wait_bounded(full_bar(st), (i / kStages) & 1, abort_flag, kWaitCycles)) break;
@@ -186,7 +199,39 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           row_ok = (ts + r < te) && ((tile_mask[st] >> (r / R)) & 1u);
         }
         const unsigned okm = __ballot_sync(0xffffffffu, row_ok) & 0xffffu;
-        if (okm != 0xffffu) {
+        uint32_t kb = kst, vb = vst;
+        int rbase = warp * 16;
+        if (KV8) {
+          // widen this warp's 16 rows of codes into its private 16-bit tile
+          // (rows without a token become zeros), then free the stage
+          const uint32_t pk = smem0 + kStages * STAGE_BYTES + warp * PRIV_BYTES;
+          const uint32_t pv = pk + 16 * ROW_BYTES;
+          constexpr int CH = D / 16;                 // 16-code chunks per row
+          const int rr = lane >> 1;
+          const bool rok = (okm >> rr) & 1u;
+          const uint8_t* krow = smem + (kst - smem0) + (warp * 16 + rr) * IN_ROW;
+          const uint8_t* vrow = smem + (vst - smem0) + (warp * 16 + rr) * IN_ROW;
+#pragma unroll
+          for (int cc = 0; cc < CH / 2; ++cc) {
+            const int ci = (lane & 1) * (CH / 2) + cc;
+            const uint4 z4 = make_uint4(0, 0, 0, 0);
+            const uint4 ck = rok ? *reinterpret_cast<const uint4*>(krow + ci * 16) : z4;
+            const uint4 cv = rok ? *reinterpret_cast<const uint4*>(vrow + ci * 16) : z4;
+            uint4 w0, w1;
+            widen_e4m3x16<T>(ck, w0, w1);
+            *reinterpret_cast<uint4*>(smem + (swz<HALVES>(pk, rr, 2 * ci) - smem0)) = w0;
+            *reinterpret_cast<uint4*>(smem + (swz<HALVES>(pk, rr, 2 * ci + 1) - smem0)) = w1;
+            widen_e4m3x16<T>(cv, w0, w1);
+            *reinterpret_cast<uint4*>(smem + (swz<HALVES>(pv, rr, 2 * ci) - smem0)) = w0;
+            *reinterpret_cast<uint4*>(smem + (swz<HALVES>(pv, rr, 2 * ci + 1) - smem0)) = w1;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty_bar(st));
+          kb = pk;
+          vb = pv;
+          rbase = 0;
+        }
+        if (!KV8 && okm != 0xffffu) {
           const int r = lane & 15, h = lane >> 4;
           if (h < HALVES && !((okm >> r) & 1u)) {
             uint4* p = reinterpret_cast<uint4*>(smem + (vst - smem0) +
@@ -200,12 +245,12 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         float sacc[4] = {0.f, 0.f, 0.f, 0.f};
         {
           const int j = lane >> 3;
-          const int row = warp * 16 + (j & 1) * 8 + (lane & 7);
+          const int row = rbase + (j & 1) * 8 + (lane & 7);
 #pragma unroll
           for (int ks = 0; ks < KSTEPS; ++ks) {
             const int dch = ks * 2 + (j >> 1);
             uint32_t af[4];
-            ldsm_x4(af, swz<HALVES>(kst, row, dch));
+            ldsm_x4(af, swz<HALVES>(kb, row, dch));
             MmaOps<T>::mma(sacc, af, qf[ks][0], qf[ks][1]);
           }
         }
@@ -245,19 +290,22 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         // O^T += V^T * P^T
         {
           const int j = lane >> 3;
-          const int row = warp * 16 + (j >> 1) * 8 + (lane & 7);
+          const int row = rbase + (j >> 1) * 8 + (lane & 7);
 #pragma unroll
           for (int mt = 0; mt < KSTEPS; ++mt) {
             const int dch = mt * 2 + (j & 1);
             uint32_t af[4];
-            ldsm_x4_trans(af, swz<HALVES>(vst, row, dch));
+            ldsm_x4_trans(af, swz<HALVES>(vb, row, dch));
             MmaOps<T>::mma(o[mt], af, pb0, pb1);
           }
         }
-        if (okm != 0xffffu) fence_proxy_async_smem();
+        if (!KV8 && okm != 0xffffu) fence_proxy_async_smem();
+        __syncwarp();
+        if (!KV8 && lane == 0) mbar_arrive(empty_bar(st));
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(st));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(st));
     }
     // sum the per-lane denominators over the 8 lanes that share a head pair
 #pragma unroll
@@ -309,6 +357,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       Ls += sm_l[w * 8 + g] * wt;
       O += sm_o[(w * 8 + g) * D + d] * wt;
     }
+    O *= v_scale;
     const int h = kvh * G + g;
     if (nsplit == 1) {
       out[((int64_t)s * Hq + h) * D + d] = Vec<T>::cvt_out(Ls > 0.f ? O / Ls : 0.f);
@@ -356,49 +405,68 @@ bool encode_pool_map(CUtensorMap* map, const void* base, CUtensorMapDataType typ
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
-constexpr int mma_smem_bytes() {
-  return 1024 + kStages * 2 * (D / 64) * kTile * 128 + 2 * kStages * 8 + 4 + 4 * kStages + 16;
+// fp8 pool [NB][Hkv][B][D] of 1-byte codes as a 3-D tensor {D, B, NB*Hkv},
+// unswizzled; one box is min(B, 64) whole rows of one slice.
+bool encode_pool_map_fp8(CUtensorMap* map, const void* base, const DecodeArgs& a) {
+  const uint64_t D = a.head_size, B = a.block_size;
+  const uint64_t planes = (uint64_t)a.num_blocks * a.num_kv_heads;
+  if (planes == 0 || planes > 0x7fffffffull) return false;
+  cuuint64_t dims[3] = {D, B, planes};
+  cuuint64_t strides[2] = {D, B * D};
+  cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)(B < 64 ? B : 64), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int D, int G>
-cudaError_t launch_mma_tdg(const DecodeArgs& a, cudaStream_t st) {
+template <int D, bool KV8>
+constexpr int mma_smem_bytes() {
+  return 1024 + kStages * 2 * kTile * (KV8 ? D : 2 * D) +
+         (KV8 ? kMmaConsumers * 2 * 16 * 2 * D : 0) + 2 * kStages * 8 + 4 + 4 * kStages + 16;
+}
+
+template <typename T, int D, int G, bool KV8>
+cudaError_t launch_mma_tdg(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
   if (!get_encode()) return cudaErrorNotSupported;
   CUtensorMap tk, tv;
-  if (!encode_pool_map(&tk, a.kc, MmaOps<T>::kTmaType, a) ||
-      !encode_pool_map(&tv, a.vc, MmaOps<T>::kTmaType, a))
-    return cudaErrorInvalidValue;
-  constexpr int smem = mma_smem_bytes<D>();
-  static_assert(smem >= kMmaConsumers * 8 * D * 4 + 2 * kMmaConsumers * 8 * 4 + 1024,
+  const bool ok = KV8 ? (encode_pool_map_fp8(&tk, a.kc, a) && encode_pool_map_fp8(&tv, a.vc, a))
+                      : (encode_pool_map(&tk, a.kc, MmaOps<T>::kTmaType, a) &&
+                         encode_pool_map(&tv, a.vc, MmaOps<T>::kTmaType, a));
+  if (!ok) return cudaErrorInvalidValue;
+  constexpr int smem = mma_smem_bytes<D, KV8>();
+  static_assert(kStages * 2 * kTile * (KV8 ? D : 2 * D) >=
+                    kMmaConsumers * 8 * D * 4 + 2 * kMmaConsumers * 8 * 4,
                 "merge area must fit in the stage ring");
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, []() {
-    attr_err = cudaFuncSetAttribute(decode_mma_kernel<T, D, G>,
+    attr_err = cudaFuncSetAttribute(decode_mma_kernel<T, D, G, KV8>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(a.num_splits, a.num_kv_heads, a.num_seqs);
-  decode_mma_kernel<T, D, G><<<grid, kMmaThreads, smem, st>>>(a, tk, tv);
+  decode_mma_kernel<T, D, G, KV8><<<grid, kMmaThreads, smem, st>>>(a, tk, tv, ks, vs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_combine(a, st);
 }
 
-template <typename T, int D>
-cudaError_t launch_mma_td(const DecodeArgs& a, cudaStream_t st) {
+template <typename T, int D, bool KV8>
+cudaError_t launch_mma_td(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
   switch (a.num_q_heads / a.num_kv_heads) {
-    case 2: return launch_mma_tdg<T, D, 2>(a, st);
-    case 4: return launch_mma_tdg<T, D, 4>(a, st);
-    case 8: return launch_mma_tdg<T, D, 8>(a, st);
+    case 2: return launch_mma_tdg<T, D, 2, KV8>(a, ks, vs, st);
+    case 4: return launch_mma_tdg<T, D, 4, KV8>(a, ks, vs, st);
+    case 8: return launch_mma_tdg<T, D, 8, KV8>(a, ks, vs, st);
   }
   return cudaErrorInvalidValue;
 }
 
-template <typename T>
-cudaError_t launch_mma_t(const DecodeArgs& a, cudaStream_t st) {
-  if (a.head_size == 64) return launch_mma_td<T, 64>(a, st);
-  if (a.head_size == 128) return launch_mma_td<T, 128>(a, st);
+template <typename T, bool KV8>
+cudaError_t launch_mma_t(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
+  if (a.head_size == 64) return launch_mma_td<T, 64, KV8>(a, ks, vs, st);
+  if (a.head_size == 128) return launch_mma_td<T, 128, KV8>(a, ks, vs, st);
   return cudaErrorInvalidValue;
 }
 
@@ -424,8 +492,15 @@ bool mma_path_applies(const DecodeArgs& a) {
 }
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st) {
-  if (a.dtype == PA_BF16) return launch_mma_t<__nv_bfloat16>(a, st);
-  if (a.dtype == PA_F16) return launch_mma_t<__half>(a, st);
+  if (a.dtype == PA_BF16) return launch_mma_t<__nv_bfloat16, false>(a, 1.f, 1.f, st);
+  if (a.dtype == PA_F16) return launch_mma_t<__half, false>(a, 1.f, 1.f, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_mma_fp8(const DecodeArgs& a, float k_scale, float v_scale,
+                                  cudaStream_t st) {
+  if (a.dtype == PA_BF16) return launch_mma_t<__nv_bfloat16, true>(a, k_scale, v_scale, st);
+  if (a.dtype == PA_F16) return launch_mma_t<__half, true>(a, k_scale, v_scale, st);
   return cudaErrorInvalidValue;
 }
 

@@ -65,6 +65,8 @@ cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, int64_t n
                                          float v_scale, cudaStream_t st, int* err);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, float k_scale, float v_scale,
                               cudaStream_t st);
+cudaError_t launch_decode_mma_fp8(const DecodeArgs& a, float k_scale, float v_scale,
+                                  cudaStream_t st);
 bool mma_path_applies(const DecodeArgs& a);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);

@@ -9,6 +9,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace pa {
 
 template <typename T> struct MmaOps;
@@ -75,6 +77,37 @@ template <int HALVES>
 __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int dch) {
   const int line = row * HALVES + (dch >> 3);
   return base + line * 128 + (((dch & 7) ^ (line & 7)) << 4);
+}
+
+}  // namespace pa
+
+#include <cuda_fp8.h>
+
+namespace pa {
+
+// 16 E4M3 codes -> 16 values of T (f16 or bf16), exactly (every E4M3 value
+// is representable in both), as two 16-byte words of 8 values.
+template <typename T>
+__device__ __forceinline__ void widen_e4m3x16(const uint4 codes, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[i] >> (16 * j)) & 0xffffu);
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+      uint32_t bits = (uint32_t)hr.x | ((uint32_t)hr.y << 16);
+      if constexpr (!std::is_same<T, __half>::value) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&bits));
+        const __nv_bfloat162 b = __float22bfloat162_rn(f);
+        bits = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      o[2 * i + j] = bits;
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 }  // namespace pa
