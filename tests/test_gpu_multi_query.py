@@ -145,3 +145,36 @@ def test_short_query_runs_split_automatically():
     assert need > 0                      # few CTAs without splits: the library splits
     out, want, _ = run_both(b)
     assert max_abs_err(out, want) <= TOL["bf16"]
+
+
+SHORT = [(dt, D, G, B) for dt in ("bf16", "f16") for D in (64, 128) for G in (1, 2, 4, 8)
+         for B in (16,)] + [("bf16", 128, 8, 8), ("bf16", 128, 4, 128), ("f16", 128, 1, 64)]
+
+
+@pytest.mark.parametrize("dtype,D,G,B", SHORT)
+def test_short_runs_column_kernel(dtype, D, G, B):
+    """At most 32 (token, head) columns per sequence and KV head: the
+    column kernel (KV tokens as M), with and without KV partitions."""
+    n_max = max(1, 32 // G)
+    n_new = [1, n_max, max(1, n_max // 2), n_max]
+    ctx = [0, 17, 700, 1500]
+    b = make_batch(dtype, D, 2 * G, 2, B, ctx, n_new, 900 + 13 * G + D + B)
+    for partition in (0, 128):
+        out, want, _ = run_both(b, partition)
+        assert torch.isfinite(out.float()).all()
+        err = max_abs_err(out, want)
+        assert err <= TOL[dtype], (partition, err)
+    assert pa.pa_get_device_error() == 0
+
+
+def test_short_runs_with_garbage_rows():
+    b = make_batch("bf16", 128, 16, 2, 16, [3, 40, 0], [2, 4, 1], 43)
+    used = torch.zeros(b["kc"].shape[0], 16, dtype=torch.bool)
+    for s, L in enumerate(b["lens"].tolist()):
+        for j in range(L):
+            used[int(b["tables"][s, j // 16]), j % 16] = True
+    for cache in (b["kc"], b["vc"]):
+        cache.permute(0, 2, 1, 3)[~used] = float("nan")
+    out, want, _ = run_both(b)
+    assert torch.isfinite(out.float()).all()
+    assert max_abs_err(out, want) <= TOL["bf16"]
