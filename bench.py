@@ -56,6 +56,10 @@ def parse():
                     help="launch the step's kernels eagerly instead of replaying a CUDA graph")
     ap.add_argument("--partition", type=int, default=0,
                     help="tokens per context partition (0 = the library's choice)")
+    ap.add_argument("--kv-dtype", default="model", choices=["model", "fp8"],
+                    help="fp8: E4M3 pools (one new token per sequence)")
+    ap.add_argument("--new-tokens", type=int, default=1,
+                    help="new tokens per sequence per step (>1: causal multi-query attention)")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="use only the first N sequences (smaller profiling case)")
     return ap.parse_args()
@@ -67,9 +71,15 @@ def kv_read_bytes(seq_lens, num_kv_heads, head_size, elt):
     return int(sum(int(L) for L in seq_lens)) * 2 * num_kv_heads * head_size * elt
 
 
+# the sources a decode-attention launch is built from (kernels, shared device
+# helpers, host dispatch and partitioning)
+DECODE_SOURCES = ("api.cu", "common.cuh", "decode_mma.cu", "decode_simt.cu", "launchers.h",
+                  "mma_util.cuh", "tma.cuh")
+
+
 def kernel_sources_digest():
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
+    for name in DECODE_SOURCES:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -362,37 +372,79 @@ def ours_arm(args):
                                   else cfg.ctx_fixed[:args.num_seqs])
     inp = workloads.make_decode_inputs(cfg, device=str(dev), seed=cfg.seed + rank)
     B, Hkv, D = cfg.block_size, cfg.num_kv_heads, cfg.head_size
-    elt = inp.q.element_size()
     S = cfg.num_seqs
+    N = max(1, args.new_tokens)
+    fp8 = args.kv_dtype == "fp8"
+    if fp8 and N > 1:
+        raise SystemExit("--kv-dtype fp8 runs one new token per sequence")
+    # orc_arrays: host copies for the CPU baseline, taken before any kernel
+    # touches the pools (the 16-bit, one-new-token step only)
+    orc_arrays = oracle_arrays(inp) if (rank == 0 and world == 1 and N == 1 and not fp8
+                                        and not args.no_cpu_baseline) else None
+    kc, vc = inp.key_cache, inp.value_cache
+    kscale = vscale = 1.0 / 48
+    if fp8:   # E4M3 pools holding the same N(0,1) draws at scale 1/48
+        kc = (kc.float() / kscale).clamp_(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        vc = (vc.float() / vscale).clamp_(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        del inp.key_cache, inp.value_cache
+        torch.cuda.empty_cache()
+    elt = 1 if fp8 else inp.q.element_size()
     lens = inp.seq_lens.cpu()
     kv_bytes = kv_read_bytes(lens.tolist(), Hkv, D, elt)
     tokens = int(lens.sum())
     max_len = inp.max_seq_len
     P = args.partition
-    splits, ptoks = pa.pa_decode_partitioning(S, cfg.num_q_heads, Hkv, B, max_len, P)
-    ws_bytes = pa.pa_decode_workspace_bytes(S, cfg.num_q_heads, Hkv, D, B, max_len, P)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    out = torch.empty_like(inp.q)
-    slots = torch.empty(S, dtype=torch.int64, device=dev)
     g = dict(q=inp.q, k_new=inp.k_new, v_new=inp.v_new, tables=inp.block_tables,
              lens=inp.seq_lens, pos=inp.positions, qsl=inp.query_start_loc)
+    if N > 1:   # the last N tokens of every sequence are new this step
+        gen = torch.Generator(device=dev).manual_seed(cfg.seed + 77)
+        for k, h in (("q", cfg.num_q_heads), ("k_new", Hkv), ("v_new", Hkv)):
+            g[k] = torch.empty((S * N, h, D), dtype=inp.q.dtype, device=dev)
+            workloads.randn_into(g[k], gen)
+        g["qsl"] = torch.arange(S + 1, dtype=torch.int32, device=dev) * N
+        g["pos"] = (inp.seq_lens.to(torch.int64)[:, None] - N +
+                    torch.arange(N, device=dev)[None, :]).reshape(-1).contiguous()
+        ws_bytes = pa.pa_multi_query_workspace_bytes(S * N, S, cfg.num_q_heads, Hkv, D, B, N,
+                                                     max_len, P)
+        splits = 1 if ws_bytes == 0 else 2
+        ptoks = None
+    else:
+        splits, ptoks = pa.pa_decode_partitioning(S, cfg.num_q_heads, Hkv, B, max_len, P)
+        ws_bytes = pa.pa_decode_workspace_bytes(S, cfg.num_q_heads, Hkv, D, B, max_len, P)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(g["q"])
+    slots = torch.empty(S * N, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream()
+
+    def attention(t):
+        if N > 1:
+            pa.pa_multi_query_attention(t["q"], t["qsl"], kc, vc, t["tables"], t["lens"],
+                                        inp.scale, Hkv, out, max_query_len=N, max_seq_len=max_len,
+                                        partition_size=P, workspace=ws)
+        elif fp8:
+            pa.pa_decode_attention_fp8(t["q"], kc, vc, t["tables"], t["lens"], inp.scale, Hkv,
+                                       kscale, vscale, out, max_seq_len=max_len,
+                                       partition_size=P, workspace=ws)
+        else:
+            pa.pa_decode_attention(t["q"], kc, vc, t["tables"], t["lens"], inp.scale, Hkv, out,
+                                   max_seq_len=max_len, partition_size=P, workspace=ws)
 
     def step(t, ev=None):
         pa.pa_compute_slot_mapping(t["qsl"], t["pos"], t["tables"], B, slot_mapping=slots)
-        pa.pa_reshape_and_cache(t["k_new"], t["v_new"], slots, inp.key_cache, inp.value_cache)
+        if fp8:
+            pa.pa_reshape_and_cache_fp8(t["k_new"], t["v_new"], slots, kc, vc, kscale, vscale)
+        else:
+            pa.pa_reshape_and_cache(t["k_new"], t["v_new"], slots, kc, vc)
         if ev is not None:
             ev[0].record(stream)
-        pa.pa_decode_attention(t["q"], inp.key_cache, inp.value_cache, t["tables"], t["lens"],
-                               inp.scale, Hkv, out, max_seq_len=max_len, partition_size=P,
-                               workspace=ws)
+        attention(t)
         if ev is not None:
             ev[1].record(stream)
 
     launches_per_step = 3 + (1 if splits > 1 else 0)
-    # host copies for the CPU baseline, taken before any kernel touches the pools
-    orc_arrays = oracle_arrays(inp) if (rank == 0 and world == 1
-                                        and not args.no_cpu_baseline) else None
+    label = cfg.name + ("_fp8" if fp8 else "") + (f"_q{N}" if N > 1 else "")
+    kernel_name = ("pa_multi_query_attention" if N > 1 else
+                   "pa_decode_attention_fp8" if fp8 else "pa_decode_attention")
     for _ in range(max(3, args.warmup)):
         step(g)
     torch.cuda.synchronize()
@@ -519,10 +571,12 @@ def ours_arm(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * step_s, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": cfg.dtype, "accum_dtype": "f32", "data": "synthetic",
+        "dtype": cfg.dtype, "kv_dtype": "e4m3" if fp8 else cfg.dtype, "accum_dtype": "f32",
+        "data": "synthetic",
         "seq_tokens_per_s": round(world * tokens / step_s, 1),
         "config": {
-            "workload": cfg.name,
+            "workload": label,
+            "new_tokens_per_seq": N,
             "shape": f"{S} seqs, ctx U[{cfg.ctx_lo},{cfg.ctx_hi}]+1 new token, "
                      f"{cfg.num_q_heads}q/{Hkv}kv heads, D={D}, B={B}, {cfg.dtype}"
             if cfg.ctx_fixed is None else f"{S} seqs x {cfg.ctx_fixed[0]}+1, "
@@ -530,13 +584,13 @@ def ours_arm(args):
             "context_tokens": tokens, "kv_read_bytes_per_step": kv_bytes,
             "pool_blocks": inp.num_blocks, "partitions": splits, "partition_tokens": ptoks,
             "l2": "inputs larger than L2 (KV pool %.2f GB >> 129 MB L2), no flush" %
-                  (2 * inp.key_cache.numel() * elt / 1e9),
+                  (2 * kc.numel() * elt / 1e9),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
-        "roofline": {"bound": "hbm", "kernel": "pa_decode_attention",
+        "roofline": {"bound": "hbm", "kernel": kernel_name,
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(cfg.name),
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(label),
                      "avg_launch_us": round(attn_ms * 1e3, 2),
                      "algorithmic_bytes_per_launch": kv_bytes},
         "gpu_launches": launches_per_step * args.steps,

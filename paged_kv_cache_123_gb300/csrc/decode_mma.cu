@@ -207,14 +207,17 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           const uint32_t pk = smem0 + kStages * STAGE_BYTES + warp * PRIV_BYTES;
           const uint32_t pv = pk + 16 * ROW_BYTES;
           constexpr int CH = D / 16;                 // 16-code chunks per row
-          const int rr = lane >> 1;
-          const bool rok = (okm >> rr) & 1u;
-          const uint8_t* krow = smem + (kst - smem0) + (warp * 16 + rr) * IN_ROW;
-          const uint8_t* vrow = smem + (vst - smem0) + (warp * 16 + rr) * IN_ROW;
+          constexpr int RPI = 32 / CH;               // rows per pass of the warp
+          // lane -> (row, chunk) so that every group of CH lanes reads one
+          // whole unswizzled row: conflict-free 16-byte loads
 #pragma unroll
-          for (int cc = 0; cc < CH / 2; ++cc) {
-            const int ci = (lane & 1) * (CH / 2) + cc;
+          for (int pass = 0; pass < 16 / RPI; ++pass) {
+            const int rr = pass * RPI + lane / CH;
+            const int ci = lane % CH;
+            const bool rok = (okm >> rr) & 1u;
             const uint4 z4 = make_uint4(0, 0, 0, 0);
+            const uint8_t* krow = smem + (kst - smem0) + (warp * 16 + rr) * IN_ROW;
+            const uint8_t* vrow = smem + (vst - smem0) + (warp * 16 + rr) * IN_ROW;
             const uint4 ck = rok ? *reinterpret_cast<const uint4*>(krow + ci * 16) : z4;
             const uint4 cv = rok ? *reinterpret_cast<const uint4*>(vrow + ci * 16) : z4;
             uint4 w0, w1;
