@@ -41,11 +41,13 @@ constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 #define kNegInfM (-__int_as_float(0x7f800000))
 
 
-// KV8 = the pools hold fp8 (E4M3) codes: TMA brings the codes (unswizzled,
-// D bytes per row); each consumer warp widens its own 16 rows into a private
-// 16-bit tile in the swizzled layout below, releases the stage, and runs the
-// same tensor-core code on the private tile. k_scale / v_scale are the
-// pools' scales (1 for 16-bit pools).
+// KV8 = the pools hold fp8 (E4M3) codes (head size 128): TMA brings the
+// codes (128-byte rows, 128-byte swizzle) and each lane widens the codes it
+// needs straight into fp16 mma fragments — K with the head dims of a k-step
+// permuted so a lane's codes are contiguous (q uses the same permutation),
+// V with two token rows byte-interleaved per head dim — so the products run
+// in fp16 without a widened copy in shared memory. k_scale / v_scale are
+// the pools' scales (1 for 16-bit pools).
 template <typename T, int D, int G, bool KV8>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
@@ -55,7 +57,12 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   constexpr int IN_ROW = KV8 ? D : ROW_BYTES;    // one token row as loaded
   constexpr int KV_BYTES = kTile * IN_ROW;       // K (or V) part of a stage
   constexpr int STAGE_BYTES = 2 * KV_BYTES;
-  constexpr int PRIV_BYTES = KV8 ? 2 * 16 * ROW_BYTES : 0;   // per consumer warp
+  constexpr int PRIV_BYTES = 0;
+  static_assert(!KV8 || D == 128, "fp8 pools: head size 128 (one 128-byte line per row)");
+  // fp8 pools run the products in fp16 whatever the query type: codes widen
+  // to fp16 in one conversion, and bf16 queries of ordinary magnitude
+  // ([6.1e-5, 65504]) are exact in fp16
+  using MT = typename std::conditional<KV8, __half, T>::type;
   constexpr int KSTEPS = D / 16;
   static_assert(G == 2 || G == 4 || G == 8, "group");
 
@@ -176,8 +183,13 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
         if (n < G) {
-          qf[ks][0] = *reinterpret_cast<const uint32_t*>(qb + n * D + ks * 16 + 2 * c);
-          qf[ks][1] = *reinterpret_cast<const uint32_t*>(qb + n * D + ks * 16 + 8 + 2 * c);
+          // fp8 pools: k-step ks, lane quad c covers head dims
+          // c*D/4 + 4ks .. +3 (a fixed permutation of the contraction order,
+          // applied to K the same way) so a lane's codes are contiguous
+          const int d0 = KV8 ? c * (D / 4) + ks * 4 : ks * 16 + 2 * c;
+          const int d1 = KV8 ? d0 + 2 : d0 + 8;
+          qf[ks][0] = to_mma_pair<T, MT>(*reinterpret_cast<const uint32_t*>(qb + n * D + d0));
+          qf[ks][1] = to_mma_pair<T, MT>(*reinterpret_cast<const uint32_t*>(qb + n * D + d1));
         } else {
           qf[ks][0] = qf[ks][1] = 0u;
         }
@@ -199,41 +211,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           row_ok = (ts + r < te) && ((tile_mask[st] >> (r / R)) & 1u);
         }
         const unsigned okm = __ballot_sync(0xffffffffu, row_ok) & 0xffffu;
-        uint32_t kb = kst, vb = vst;
-        int rbase = warp * 16;
-        if (KV8) {
-          // widen this warp's 16 rows of codes into its private 16-bit tile
-          // (rows without a token become zeros), then free the stage
-          const uint32_t pk = smem0 + kStages * STAGE_BYTES + warp * PRIV_BYTES;
-          const uint32_t pv = pk + 16 * ROW_BYTES;
-          constexpr int CH = D / 16;                 // 16-code chunks per row
-          constexpr int RPI = 32 / CH;               // rows per pass of the warp
-          // lane -> (row, chunk) so that every group of CH lanes reads one
-          // whole unswizzled row: conflict-free 16-byte loads
-#pragma unroll
-          for (int pass = 0; pass < 16 / RPI; ++pass) {
-            const int rr = pass * RPI + lane / CH;
-            const int ci = lane % CH;
-            const bool rok = (okm >> rr) & 1u;
-            const uint4 z4 = make_uint4(0, 0, 0, 0);
-            const uint8_t* krow = smem + (kst - smem0) + (warp * 16 + rr) * IN_ROW;
-            const uint8_t* vrow = smem + (vst - smem0) + (warp * 16 + rr) * IN_ROW;
-            const uint4 ck = rok ? *reinterpret_cast<const uint4*>(krow + ci * 16) : z4;
-            const uint4 cv = rok ? *reinterpret_cast<const uint4*>(vrow + ci * 16) : z4;
-            uint4 w0, w1;
-            widen_e4m3x16<T>(ck, w0, w1);
-            *reinterpret_cast<uint4*>(smem + (swz<HALVES>(pk, rr, 2 * ci) - smem0)) = w0;
-            *reinterpret_cast<uint4*>(smem + (swz<HALVES>(pk, rr, 2 * ci + 1) - smem0)) = w1;
-            widen_e4m3x16<T>(cv, w0, w1);
-            *reinterpret_cast<uint4*>(smem + (swz<HALVES>(pv, rr, 2 * ci) - smem0)) = w0;
-            *reinterpret_cast<uint4*>(smem + (swz<HALVES>(pv, rr, 2 * ci + 1) - smem0)) = w1;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty_bar(st));
-          kb = pk;
-          vb = pv;
-          rbase = 0;
-        }
+        const uint32_t kb = kst, vb = vst;
+        const int rbase = warp * 16;
         if (!KV8 && okm != 0xffffu) {
           const int r = lane & 15, h = lane >> 4;
           if (h < HALVES && !((okm >> r) & 1u)) {
@@ -246,7 +225,29 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         }
         // S^T = K * Q^T for this warp's 16 tokens
         float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-        {
+        if constexpr (KV8) {
+          // codes of rows n and n+8, head dims c*D/4 .. +D/4-1 (two 16-byte
+          // chunks, 128-byte swizzle), widened straight into A fragments
+          const uint8_t* kbase = smem + (kst - smem0);
+          const int ra = warp * 16 + n, rb = ra + 8;
+          uint4 ka[2], kq[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            ka[h] = *reinterpret_cast<const uint4*>(kbase + ra * 128 + (((2 * c + h) ^ (ra & 7)) << 4));
+            kq[h] = *reinterpret_cast<const uint4*>(kbase + rb * 128 + (((2 * c + h) ^ (rb & 7)) << 4));
+          }
+          const uint32_t wa[8] = {ka[0].x, ka[0].y, ka[0].z, ka[0].w, ka[1].x, ka[1].y, ka[1].z, ka[1].w};
+          const uint32_t wb[8] = {kq[0].x, kq[0].y, kq[0].z, kq[0].w, kq[1].x, kq[1].y, kq[1].z, kq[1].w};
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            uint32_t af[4];
+            af[0] = e4m3x2_to_f16x2(wa[ks] & 0xffffu);
+            af[1] = e4m3x2_to_f16x2(wb[ks] & 0xffffu);
+            af[2] = e4m3x2_to_f16x2(wa[ks] >> 16);
+            af[3] = e4m3x2_to_f16x2(wb[ks] >> 16);
+            MmaOps<MT>::mma(sacc, af, qf[ks][0], qf[ks][1]);
+          }
+        } else {
           const int j = lane >> 3;
           const int row = rbase + (j & 1) * 8 + (lane & 7);
 #pragma unroll
@@ -254,7 +255,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
             const int dch = ks * 2 + (j >> 1);
             uint32_t af[4];
             ldsm_x4(af, swz<HALVES>(kb, row, dch));
-            MmaOps<T>::mma(sacc, af, qf[ks][0], qf[ks][1]);
+            MmaOps<MT>::mma(sacc, af, qf[ks][0], qf[ks][1]);
           }
         }
         const bool okA = (okm >> n) & 1u, okB = (okm >> (n + 8)) & 1u;
@@ -276,10 +277,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         const float p2 = live0 ? exp2f(x2 - mn0) : 0.f;
         const float p1 = live1 ? exp2f(x1 - mn1) : 0.f;
         const float p3 = live1 ? exp2f(x3 - mn1) : 0.f;
-        const uint32_t cA = MmaOps<T>::pack(p0, p1);
-        const uint32_t cB = MmaOps<T>::pack(p2, p3);
+        const uint32_t cA = MmaOps<MT>::pack(p0, p1);
+        const uint32_t cB = MmaOps<MT>::pack(p2, p3);
         // the denominator sums the same rounded weights the MMA multiplies
-        const float2 fA = MmaOps<T>::unpack(cA), fB = MmaOps<T>::unpack(cB);
+        const float2 fA = MmaOps<MT>::unpack(cA), fB = MmaOps<MT>::unpack(cB);
         l0 = l0 * al0 + fA.x + fB.x;
         l1 = l1 * al1 + fA.y + fB.y;
         m0 = mn0;
@@ -291,7 +292,42 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         const uint32_t pb0 = movmatrix_trans(cA);
         const uint32_t pb1 = movmatrix_trans(cB);
         // O^T += V^T * P^T
-        {
+        if constexpr (KV8) {
+          // token rows 2c, 2c+1, 2c+8, 2c+9, head dims n*16 .. +15 (one
+          // 16-byte chunk each); bytes of rows paired per head dim; the M
+          // order of this product is head dim n*16 + 8*(row >= 8) + mt
+          const uint8_t* vbase = smem + (vst - smem0);
+          uint32_t w[4][4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int row = warp * 16 + 2 * c + (r & 1) + (r >> 1) * 8;
+            const bool rok = (okm >> (row - warp * 16)) & 1u;
+            const uint4 v = *reinterpret_cast<const uint4*>(vbase + row * 128 + ((n ^ (row & 7)) << 4));
+            w[r][0] = rok ? v.x : 0u; w[r][1] = rok ? v.y : 0u;
+            w[r][2] = rok ? v.z : 0u; w[r][3] = rok ? v.w : 0u;
+          }
+          uint32_t p01[16], p23[16];      // (token pair, head dim j) as f16x2
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint32_t lo01 = __byte_perm(w[0][q4], w[1][q4], 0x5140);
+            const uint32_t hi01 = __byte_perm(w[0][q4], w[1][q4], 0x7362);
+            const uint32_t lo23 = __byte_perm(w[2][q4], w[3][q4], 0x5140);
+            const uint32_t hi23 = __byte_perm(w[2][q4], w[3][q4], 0x7362);
+            p01[4 * q4 + 0] = e4m3x2_to_f16x2(lo01 & 0xffffu);
+            p01[4 * q4 + 1] = e4m3x2_to_f16x2(lo01 >> 16);
+            p01[4 * q4 + 2] = e4m3x2_to_f16x2(hi01 & 0xffffu);
+            p01[4 * q4 + 3] = e4m3x2_to_f16x2(hi01 >> 16);
+            p23[4 * q4 + 0] = e4m3x2_to_f16x2(lo23 & 0xffffu);
+            p23[4 * q4 + 1] = e4m3x2_to_f16x2(lo23 >> 16);
+            p23[4 * q4 + 2] = e4m3x2_to_f16x2(hi23 & 0xffffu);
+            p23[4 * q4 + 3] = e4m3x2_to_f16x2(hi23 >> 16);
+          }
+#pragma unroll
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            const uint32_t af[4] = {p01[mt], p01[8 + mt], p23[mt], p23[8 + mt]};
+            MmaOps<MT>::mma(o[mt], af, pb0, pb1);
+          }
+        } else {
           const int j = lane >> 3;
           const int row = rbase + (j >> 1) * 8 + (lane & 7);
 #pragma unroll
@@ -299,12 +335,12 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
             const int dch = mt * 2 + (j & 1);
             uint32_t af[4];
             ldsm_x4_trans(af, swz<HALVES>(vb, row, dch));
-            MmaOps<T>::mma(o[mt], af, pb0, pb1);
+            MmaOps<MT>::mma(o[mt], af, pb0, pb1);
           }
         }
         if (!KV8 && okm != 0xffffu) fence_proxy_async_smem();
         __syncwarp();
-        if (!KV8 && lane == 0) mbar_arrive(empty_bar(st));
+        if (lane == 0) mbar_arrive(empty_bar(st));
       } else {
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(st));
@@ -333,10 +369,13 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
     for (int mt = 0; mt < KSTEPS; ++mt) {
       float* base = sm_o + warp * 8 * D;
-      base[(2 * c) * D + mt * 16 + n] = o[mt][0];
-      base[(2 * c + 1) * D + mt * 16 + n] = o[mt][1];
-      base[(2 * c) * D + mt * 16 + n + 8] = o[mt][2];
-      base[(2 * c + 1) * D + mt * 16 + n + 8] = o[mt][3];
+      // head dim of M rows n and n+8 of m-tile mt
+      const int da = KV8 ? n * 16 + mt : mt * 16 + n;
+      const int db = KV8 ? n * 16 + 8 + mt : mt * 16 + n + 8;
+      base[(2 * c) * D + da] = o[mt][0];
+      base[(2 * c + 1) * D + da] = o[mt][1];
+      base[(2 * c) * D + db] = o[mt][2];
+      base[(2 * c + 1) * D + db] = o[mt][3];
     }
     if (n == 0) {
       sm_m[warp * 8 + 2 * c] = m0;
@@ -408,8 +447,9 @@ bool encode_pool_map(CUtensorMap* map, const void* base, CUtensorMapDataType typ
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp8 pool [NB][Hkv][B][D] of 1-byte codes as a 3-D tensor {D, B, NB*Hkv},
-// unswizzled; one box is min(B, 64) whole rows of one slice.
+// fp8 pool [NB][Hkv][B][128] of 1-byte codes as a 3-D tensor {128, B, NB*Hkv}
+// with the 128-byte swizzle (one row = one line); one box is min(B, 64) whole
+// rows of one slice.
 bool encode_pool_map_fp8(CUtensorMap* map, const void* base, const DecodeArgs& a) {
   const uint64_t D = a.head_size, B = a.block_size;
   const uint64_t planes = (uint64_t)a.num_blocks * a.num_kv_heads;
@@ -419,15 +459,15 @@ bool encode_pool_map_fp8(CUtensorMap* map, const void* base, const DecodeArgs& a
   cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)(B < 64 ? B : 64), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D, bool KV8>
 constexpr int mma_smem_bytes() {
-  return 1024 + kStages * 2 * kTile * (KV8 ? D : 2 * D) +
-         (KV8 ? kMmaConsumers * 2 * 16 * 2 * D : 0) + 2 * kStages * 8 + 4 + 4 * kStages + 16;
+  return 1024 + kStages * 2 * kTile * (KV8 ? D : 2 * D) + 2 * kStages * 8 + 4 + 4 * kStages +
+         16;
 }
 
 template <typename T, int D, int G, bool KV8>
@@ -468,7 +508,9 @@ cudaError_t launch_mma_td(const DecodeArgs& a, float ks, float vs, cudaStream_t 
 
 template <typename T, bool KV8>
 cudaError_t launch_mma_t(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
-  if (a.head_size == 64) return launch_mma_td<T, 64, KV8>(a, ks, vs, st);
+  if constexpr (!KV8) {
+    if (a.head_size == 64) return launch_mma_td<T, 64, false>(a, ks, vs, st);
+  }
   if (a.head_size == 128) return launch_mma_td<T, 128, KV8>(a, ks, vs, st);
   return cudaErrorInvalidValue;
 }

@@ -111,3 +111,29 @@ __device__ __forceinline__ void widen_e4m3x16(const uint4 codes, uint4& lo, uint
 }
 
 }  // namespace pa
+
+namespace pa {
+
+// A pair of query values of type T as the operand type MT of the products.
+template <typename T, typename MT>
+__device__ __forceinline__ uint32_t to_mma_pair(uint32_t v) {
+  if constexpr (std::is_same<T, MT>::value) {
+    return v;
+  } else {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+    const __half2 h = __floats2half2_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+}  // namespace pa
+
+namespace pa {
+
+// Two E4M3 codes (low byte first) -> an fp16 pair, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  return (uint32_t)hr.x | ((uint32_t)hr.y << 16);
+}
+
+}  // namespace pa

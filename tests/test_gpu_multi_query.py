@@ -178,3 +178,29 @@ def test_short_runs_with_garbage_rows():
     out, want, _ = run_both(b)
     assert torch.isfinite(out.float()).all()
     assert max_abs_err(out, want) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("n_new", [[2, 2, 2], [40, 40, 40]])
+def test_bad_block_id_is_latched_and_other_sequences_are_exact(n_new):
+    """A block id outside the pool in one sequence's table: the error is
+    latched; sequences with valid tables still match the oracle (both the
+    column kernel and the row kernel)."""
+    b = make_batch("bf16", 128, 16, 2, 16, [100, 300, 50], n_new, 97)
+    kco, vco = np_(b["kc"]), np_(b["vc"])
+    slots_o = oracle.slot_mapping(b["qsl"].numpy(), b["pos"].numpy(), b["tables"].numpy(), 16)
+    oracle.reshape_and_cache(np_(b["kn"]), np_(b["vn"]), slots_o, kco, vco, 16)
+    want = oracle.multi_query_attention(np_(b["q"]), kco, vco, b["tables"].numpy(),
+                                        b["qsl"].numpy(), b["lens"].numpy(), b["scale"], 2, 16,
+                                        "bf16")
+    g = {k: v.to(DEV) for k, v in b.items() if isinstance(v, torch.Tensor)}
+    slots = pa.pa_compute_slot_mapping(g["qsl"], g["pos"], g["tables"], 16)
+    pa.pa_reshape_and_cache(g["kn"], g["vn"], slots, g["kc"], g["vc"])
+    pa.pa_get_device_error()
+    g["tables"][1, 2] = b["kc"].shape[0] + 7           # sequence 1 now points outside
+    out = pa.pa_multi_query_attention(g["q"], g["qsl"], g["kc"], g["vc"], g["tables"], g["lens"],
+                                      b["scale"], 2, max_query_len=max(n_new),
+                                      max_seq_len=b["max_len"])
+    assert pa.pa_get_device_error() == -5
+    q0, q1 = int(b["qsl"][1]), int(b["qsl"][2])
+    keep = [t for t in range(out.shape[0]) if not (q0 <= t < q1)]
+    assert max_abs_err(out[keep], want[keep]) <= TOL["bf16"]
