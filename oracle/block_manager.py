@@ -16,6 +16,10 @@ Follows, in order:
     on the original, then writes; a writer that is the last holder writes in
     place.
 
+  * [P1] §3.2 allocate_slots phase 1 and §3.3.1: with a sliding window, the
+    blocks before the skipped-token count // B hold no attended token and
+    are released (remove_skipped).
+
 Readings: no block id is reserved as a null block (the pages' figures use P0
 as an ordinary block); the free order is FIFO as in [P1]'s free_blocks.
 """
@@ -64,7 +68,8 @@ class OracleBlockManager:
         self.tables[child] = list(self.tables[parent])
         self.lens[child] = self.lens[parent]
         for b in self.tables[child]:
-            self.ref[b] += 1
+            if b is not None:
+                self.ref[b] += 1
 
     def append_slot(self, seq):
         """Reserve the slot for seq's next token. Returns (slot, cow) where
@@ -85,7 +90,22 @@ class OracleBlockManager:
         self.lens[seq] = L + 1
         return table[lb] * B + (L - lb * B), cow
 
+    def remove_skipped(self, seq, window: int):
+        """Release the leading blocks of seq that hold only tokens before its
+        window (the last `window` tokens); their entries become None.
+        Returns the released ids in table order."""
+        from .paged_attention import skipped_blocks
+        table = self.tables[seq]
+        gone = []
+        for i in range(skipped_blocks(self.lens[seq], window, self.block_size)):
+            if table[i] is not None:
+                gone.append(table[i])
+                self._release(table[i])
+                table[i] = None
+        return gone
+
     def free_seq(self, seq):
         for b in self.tables.pop(seq):
-            self._release(b)
+            if b is not None:
+                self._release(b)
         self.lens.pop(seq)

@@ -164,14 +164,35 @@ def copy_blocks(key_caches, value_caches, src_dst_pairs):
 # --------------------------------------------------------------------------
 # paged decode attention
 # --------------------------------------------------------------------------
+def window_start(seq_len: int, window: int) -> int:
+    """First token a decode query attends under a sliding window of `window`
+    tokens (0 = no window). A reading: the window is the last `window`
+    tokens of the sequence, the new token included, so token j is attended
+    iff seq_len - window <= j < seq_len. The pages name the sliding window
+    only through the blocks it lets the allocator release ([P1] §3.2
+    allocate_slots, phase 1, "release blocks outside the sliding window")."""
+    if window <= 0 or seq_len <= window:
+        return 0
+    return seq_len - window
+
+
+def skipped_blocks(seq_len: int, window: int, block_size: int) -> int:
+    """Leading logical blocks that hold no attended token: the skipped
+    tokens // B ([P1] §3.3.1 get_num_blocks_to_allocate: skipped blocks are
+    the skipped tokens floor-divided by the block size). Their table entries
+    are never read, so the allocator may free them."""
+    return window_start(seq_len, window) // block_size
+
+
 def gather_kv(cache, table_row, seq_len: int, kv_head: int, block_size: int,
-              dtype: str) -> np.ndarray:
-    """Contiguous fp64 copy of one sequence's K (or V) rows for one KV head,
-    token j read from physical block table_row[j // B], row j % B ([P4]
-    "按 Block 分配": token 8 -> logical block 2 -> P4, row 0)."""
-    j = np.arange(seq_len, dtype=np.int64)
+              dtype: str, start: int = 0) -> np.ndarray:
+    """Contiguous fp64 copy of one sequence's K (or V) rows start..seq_len-1
+    for one KV head, token j read from physical block table_row[j // B], row
+    j % B ([P4] "按 Block 分配": token 8 -> logical block 2 -> P4, row 0).
+    Table entries of blocks before start // B are not read."""
+    j = np.arange(start, seq_len, dtype=np.int64)
     blk = np.asarray(table_row, dtype=np.int64)[j // block_size]
-    if seq_len and (blk.min() < 0 or blk.max() >= cache.shape[0]):
+    if len(j) and (blk.min() < 0 or blk.max() >= cache.shape[0]):
         raise ValueError("block id outside the pool")
     rows = cache[blk, kv_head, j % block_size, :]
     return upcast(np.ascontiguousarray(rows), dtype)
@@ -193,7 +214,7 @@ def decode_attention_one(q_vec64, K64, V64, scale: float) -> np.ndarray:
 
 def decode_attention(q, key_cache, value_cache, block_tables, seq_lens,
                      scale: float, num_kv_heads: int, block_size: int,
-                     dtype: str, seqs=None, heads=None) -> np.ndarray:
+                     dtype: str, seqs=None, heads=None, window: int = 0) -> np.ndarray:
     """Paged decode attention for every (sequence, query head), or for the
     listed subsets. Query head h reads KV head h // (Hq / Hkv) (contiguous
     groups; [P3] §2.1: 64 query heads share 8 KV heads).
@@ -202,6 +223,8 @@ def decode_attention(q, key_cache, value_cache, block_tables, seq_lens,
     section; [P2]: the kernel reads block by block, so blocks need not be
     contiguous). The oracle therefore gathers each sequence's K and V through
     its block table into contiguous arrays and runs dense attention on them.
+
+    window > 0: sliding-window attention over tokens window_start .. L-1.
 
     Returns float64 [S, Hq, D] (rows outside `seqs`/`heads` stay zero)."""
     S, Hq, D = q.shape
@@ -213,13 +236,14 @@ def decode_attention(q, key_cache, value_cache, block_tables, seq_lens,
     heads = range(Hq) if heads is None else heads
     for s in seqs:
         L = int(seq_lens[s])
+        lo = window_start(L, window)
         by_kv = {}
         for h in heads:
             kvh = h // g
             if kvh not in by_kv:
                 by_kv[kvh] = (
-                    gather_kv(key_cache, block_tables[s], L, kvh, block_size, dtype),
-                    gather_kv(value_cache, block_tables[s], L, kvh, block_size, dtype))
+                    gather_kv(key_cache, block_tables[s], L, kvh, block_size, dtype, lo),
+                    gather_kv(value_cache, block_tables[s], L, kvh, block_size, dtype, lo))
             K, V = by_kv[kvh]
             out[s, h] = decode_attention_one(q64[s, h], K, V, scale)
     return out
@@ -363,16 +387,17 @@ def reshape_and_cache_fp8(k, v, slots, key_cache8, value_cache8, block_size: int
 
 def decode_attention_fp8(q, key_cache8, value_cache8, block_tables, seq_lens, scale: float,
                          num_kv_heads: int, block_size: int, dtype: str, k_scale: float,
-                         v_scale: float, seqs=None, heads=None) -> np.ndarray:
+                         v_scale: float, seqs=None, heads=None, window: int = 0) -> np.ndarray:
     """Decode attention over e4m3 pools: K = decode(code) * k_scale and
-    V = decode(code) * v_scale exactly in fp64, then decode_attention."""
+    V = decode(code) * v_scale exactly in fp64, then decode_attention
+    (window as there)."""
     S, Hq, D = q.shape
     g = Hq // num_kv_heads
     q64 = upcast(q, dtype)
     out = np.zeros((S, Hq, D), dtype=np.float64)
     for s in (range(S) if seqs is None else seqs):
         L = int(seq_lens[s])
-        j = np.arange(L)
+        j = np.arange(window_start(L, window), L)
         blk = np.asarray(block_tables[s], dtype=np.int64)[j // block_size]
         for h in (range(Hq) if heads is None else heads):
             kvh = h // g

@@ -12,6 +12,11 @@ PagedAttention", copy-on-write figure):
     to a fresh copy (the caller runs pa_copy_blocks on the returned pairs
     before the KV write), releasing one reference on the original.
 
+With a sliding window of W tokens, `release_skipped` frees the leading
+blocks that hold no token of the window (same page, §3.2 allocate_slots,
+phase 1, and §3.3.1: skipped blocks = skipped tokens // B); their table
+entries become -1, which the windowed attention call never reads.
+
 The per-step work (`prepare_decode_step`) is batched: it returns, for a list
 of sequences each appending one token, the positions, the copy pairs and the
 updated dense block-table rows, ready to upload in one copy each.
@@ -72,12 +77,31 @@ class BlockPool:
         row = self.blocks[parent]
         self.blocks[child] = list(row)
         self.num_tokens[child] = self.num_tokens[parent]
-        np.add.at(self.refcount, np.asarray(row, dtype=np.int64), 1)
+        held = np.asarray([b for b in row if b >= 0], dtype=np.int64)
+        np.add.at(self.refcount, held, 1)
 
     def release(self, seq) -> None:
         for blk in self.blocks.pop(seq):
-            self._drop(blk)
+            if blk >= 0:
+                self._drop(blk)
         del self.num_tokens[seq]
+
+    def release_skipped(self, seq, window: int) -> List[int]:
+        """Drop one reference on each leading block of seq that holds no
+        token of its last `window` tokens (window <= 0: none) and mark the
+        entry -1. Returns the blocks released, in table order."""
+        n = self.num_tokens[seq]
+        if window <= 0 or n <= window:
+            return []
+        skip = (n - window) // self.block_size
+        row = self.blocks[seq]
+        out = []
+        for i in range(min(skip, len(row))):
+            if row[i] >= 0:
+                out.append(row[i])
+                self._drop(row[i])
+                row[i] = -1
+        return out
 
     # ---- one decode step ----------------------------------------------------
     def prepare_decode_step(self, seqs: Sequence) -> Tuple[np.ndarray, List[Tuple[int, int]]]:
@@ -121,7 +145,7 @@ class BlockPool:
         """Share of logical block mappings served by an already-counted
         physical block."""
         seqs = list(self.blocks) if seqs is None else seqs
-        rows = [self.blocks[s] for s in seqs]
+        rows = [[b for b in self.blocks[s] if b >= 0] for s in seqs]
         logical = sum(map(len, rows))
         unique = len(set().union(*map(set, rows))) if rows else 0
         return 0.0 if logical == 0 else (logical - unique) / logical

@@ -73,6 +73,10 @@ def test_matches_oracle_on_random_operation_sequences(seed):
             s = live.pop(rng.integers(len(live)))
             pool.release(s)
             orc.free_seq(s)
+        elif op == 3:
+            s = live[rng.integers(len(live))]
+            W = int(rng.integers(1, 14))
+            assert pool.release_skipped(s, W) == orc.remove_skipped(s, W)
         elif op == 2 and len(live) < 8 and pool.num_free() > 4:
             n = int(rng.integers(1, 12))
             pool.add_sequence(nxt, n)
@@ -94,5 +98,21 @@ def test_matches_oracle_on_random_operation_sequences(seed):
                     want_pairs.append(cow)
             assert pairs == want_pairs
         assert pool.refcount.tolist() == orc.ref
-        assert {s: pool.blocks[s] for s in live} == {s: orc.tables[s] for s in live}
+        assert {s: pool.blocks[s] for s in live} == {
+            s: [-1 if b is None else b for b in orc.tables[s]] for s in live}
         assert list(pool._free) == list(orc.free)
+
+
+def test_release_skipped_frees_only_whole_blocks_before_the_window():
+    pool = BlockPool(16, 4)
+    pool.add_sequence("a", 10)                  # blocks 0, 1, 2 hold tokens 0..9
+    pool.fork("a", "b")
+    assert pool.release_skipped("a", 7) == []   # window 3..9 touches block 0
+    assert pool.release_skipped("a", 6) == [0]  # window 4..9
+    assert pool.blocks["a"] == [-1, 1, 2]
+    assert pool.refcount[0] == 1 and 0 not in pool._free   # still held by "b"
+    assert pool.release_skipped("b", 1) == [0, 1]          # window 9..9
+    assert list(pool._free)[-1] == 0 and pool.refcount[1] == 1   # 1 still held by "a"
+    pool.release("a")
+    pool.release("b")
+    assert pool.num_free() == 16 and not pool.refcount.any()

@@ -11,6 +11,7 @@ import oracle.paged_attention as opa
 import oracle.block_manager as obm
 import tests.test_oracle_attention as ta
 import tests.test_oracle_pins as tp
+import tests.test_oracle_window as tw
 
 
 def _slot_no_subtract(qsl, pos, tab, B, num_tokens=None):
@@ -67,9 +68,9 @@ def _attn_keys_as_values(q, K, V, scale):
     return (p @ K) / p.sum()
 
 
-def _gather_head_modulo(cache, table_row, L, kv_head, B, dtype):
+def _gather_head_modulo(cache, table_row, L, kv_head, B, dtype, start=0):
     # wrong row inside the block: j // B instead of j % B
-    j = np.arange(L)
+    j = np.arange(start, L)
     blk = np.asarray(table_row)[j // B]
     return opa.upcast(np.ascontiguousarray(cache[blk, kv_head, (j // B) % B, :]), dtype)
 
@@ -81,15 +82,17 @@ def _upcast_bf16_wrong_shift(a, dtype):
     return a.astype(np.float64)
 
 
-def _decode_gqa_modulo(q, kc, vc, tables, lens, scale, Hkv, B, dtype, seqs=None, heads=None):
+def _decode_gqa_modulo(q, kc, vc, tables, lens, scale, Hkv, B, dtype, seqs=None, heads=None,
+                       window=0):
     S, Hq, D = q.shape
     out = np.zeros((S, Hq, D))
     q64 = opa.upcast(q, dtype)
     for s in range(S):
         for h in range(Hq):
             kvh = h % Hkv                                  # wrong group map
-            K = opa.gather_kv(kc, tables[s], int(lens[s]), kvh, B, dtype)
-            V = opa.gather_kv(vc, tables[s], int(lens[s]), kvh, B, dtype)
+            lo = opa.window_start(int(lens[s]), window)
+            K = opa.gather_kv(kc, tables[s], int(lens[s]), kvh, B, dtype, lo)
+            V = opa.gather_kv(vc, tables[s], int(lens[s]), kvh, B, dtype, lo)
             out[s, h] = opa.decode_attention_one(q64[s, h], K, V, scale)
     return out
 
@@ -111,6 +114,18 @@ def _mq_sees_one_future_token(q, kc, vc, tables, qsl, lens, scale, Hkv, B, dtype
                                                                   K[:last + 1], V[:last + 1],
                                                                   scale)
     return out
+
+
+def _window_one_late(L, W):
+    return L - W + 1 if 0 < W < L else 0               # window one token short
+
+
+def _window_one_early(L, W):
+    return max(L - W - 1, 0) if 0 < W < L else 0       # one token too many
+
+
+def _skipped_ceil(L, W, B):
+    return -(-opa.window_start(L, W) // B)             # frees a partly used block
 
 
 class _NoDecrementOnCow(obm.OracleBlockManager):
@@ -155,6 +170,11 @@ PIN_TESTS = [
     ta.test_gqa_query_head_reads_its_group_kv_head,
     ta.test_multi_query_with_one_new_token_is_decode,
     ta.test_multi_query_matches_sdpa_with_causal_offset_mask,
+    tw.test_window_start_reading,
+    lambda: tw.test_skipped_blocks_brute_force(4),
+    tw.test_window_of_one_is_the_new_value,
+    tw.test_equal_keys_give_mean_of_last_w_values,
+    lambda: tw.test_window_matches_masked_sdpa("f16", 8, 9),
 ]
 
 MUTANTS = {
@@ -171,13 +191,16 @@ MUTANTS = {
     "cow_no_decrement": [("OracleBlockManager", _NoDecrementOnCow)],
     "cow_always": [("OracleBlockManager", _CowAlways)],
     "mq_future_token": [("multi_query_attention", _mq_sees_one_future_token)],
+    "window_one_late": [("window_start", _window_one_late)],
+    "window_one_early": [("window_start", _window_one_early)],
+    "skipped_ceil": [("skipped_blocks", _skipped_ceil)],
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_planted_mistake(name, monkeypatch):
     for attr, fn in MUTANTS[name]:
-        for mod in (oracle, opa, obm, tp):
+        for mod in (oracle, opa, obm, tp, tw):
             if hasattr(mod, attr):
                 monkeypatch.setattr(mod, attr, fn)
     caught = []
