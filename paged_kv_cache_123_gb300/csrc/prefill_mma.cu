@@ -37,9 +37,19 @@ constexpr int kMqStages = 3;
 constexpr long long kMqWaitCycles = 4000000000LL;
 #define kNegInfQ (-__int_as_float(0x7f800000))
 
+// Address of 16-byte chunk `dch` of token row `row` when each 64-column half
+// of the head dim is its own [64 rows][128 B] region with the 128-byte
+// swizzle: 8 consecutive rows at one chunk hit 8 different bank groups.
+__device__ __forceinline__ uint32_t swz_split(uint32_t base, int row, int dch) {
+  return base + (dch >> 3) * (kMqTile * 128) + row * 128 + (((dch & 7) ^ (row & 7)) << 4);
+}
+
 // Producer warp: fill the ring with the KV tiles [0, ntiles) of (sequence,
 // kv head): lane p issues the TMA loads of the tile's block-piece p.
-template <int ROW_BYTES, int KV_BYTES, int STAGE_BYTES>
+// SPLIT: the stage holds each 64-column half of the head dim as its own
+// [64 rows][128 B] region (one 3-D box per half); otherwise whole rows (one
+// 4-D box).
+template <int ROW_BYTES, int KV_BYTES, int STAGE_BYTES, bool SPLIT>
 __device__ void mq_produce(const MultiQueryArgs& a, const CUtensorMap* tmK,
                            const CUtensorMap* tmV, const int32_t* trow, int kvh, int kv_lo,
                            int kv_end, int ntiles, uint32_t smem0, uint32_t bar0, unsigned* tile_mask,
@@ -82,8 +92,17 @@ __device__ void mq_produce(const MultiQueryArgs& a, const CUtensorMap* tmK,
       const uint32_t kdst = smem0 + st * STAGE_BYTES + lane * R * ROW_BYTES;
       const int z = (int)(blk * a.num_kv_heads + kvh);
       const int y = tok & (B - 1);
-      tma_load_4d(kdst, tmK, 0, 0, y, z, bar0 + 8u * st);
-      tma_load_4d(kdst + KV_BYTES, tmV, 0, 0, y, z, bar0 + 8u * st);
+      if (SPLIT) {
+        const uint32_t base = smem0 + st * STAGE_BYTES + lane * R * 128;
+#pragma unroll
+        for (int h = 0; h < ROW_BYTES / 128; ++h) {
+          tma_load_3d(base + h * kMqTile * 128, tmK, h * 64, y, z, bar0 + 8u * st);
+          tma_load_3d(base + KV_BYTES + h * kMqTile * 128, tmV, h * 64, y, z, bar0 + 8u * st);
+        }
+      } else {
+        tma_load_4d(kdst, tmK, 0, 0, y, z, bar0 + 8u * st);
+        tma_load_4d(kdst + KV_BYTES, tmV, 0, 0, y, z, bar0 + 8u * st);
+      }
     }
     issued = i + 1;
   }
@@ -147,7 +166,8 @@ multi_query_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMap t
   __syncthreads();
 
   if (warp == kMqConsumers) {
-    mq_produce<ROW_BYTES, KV_BYTES, STAGE_BYTES>(a, &tmK, &tmV, trow, kvh, kv_lo, kv_end, ntiles,
+    mq_produce<ROW_BYTES, KV_BYTES, STAGE_BYTES, true>(a, &tmK, &tmV, trow, kvh, kv_lo, kv_end,
+                                                       ntiles,
                                                  smem0, bar0, tile_mask, abort_flag, lane);
     __syncthreads();
     if (*abort_flag && lane == 0) latch(a.err, PA_ERR_TIMEOUT);
@@ -220,7 +240,7 @@ multi_query_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMap t
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
           uint32_t kb[4];
-          ldsm_x4(kb, swz<HALVES>(kst, nt * 8 + (lane & 7), 4 * kp + (lane >> 3)));
+          ldsm_x4(kb, swz_split(kst, nt * 8 + (lane & 7), 4 * kp + (lane >> 3)));
           MmaOps<T>::mma(sacc[nt], qa[2 * kp], kb[0], kb[1]);
           MmaOps<T>::mma(sacc[nt], qa[2 * kp + 1], kb[2], kb[3]);
         }
@@ -289,8 +309,8 @@ multi_query_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMap t
 #pragma unroll
         for (int dp = 0; dp < DN / 2; ++dp) {
           uint32_t vb[4];
-          ldsm_x4_trans(vb, swz<HALVES>(vst, kt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7),
-                                        2 * dp + (lane >> 4)));
+          ldsm_x4_trans(vb, swz_split(vst, kt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7),
+                                      2 * dp + (lane >> 4)));
           vb[0] &= vm[kt][0]; vb[1] &= vm[kt][1]; vb[2] &= vm[kt][0]; vb[3] &= vm[kt][1];
           MmaOps<T>::mma(o[2 * dp], pa[kt], vb[0], vb[1]);
           MmaOps<T>::mma(o[2 * dp + 1], pa[kt], vb[2], vb[3]);
@@ -453,8 +473,8 @@ multi_query_cols_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensor
   }
 
   if (warp == kMqConsumers) {
-    mq_produce<ROW_BYTES, KV_BYTES, STAGE_BYTES>(a, &tmK, &tmV, trow, kvh, kv_lo, kv_end,
-                                                 ntiles, smem0, bar0, tile_mask, abort_flag,
+    mq_produce<ROW_BYTES, KV_BYTES, STAGE_BYTES, false>(a, &tmK, &tmV, trow, kvh, kv_lo, kv_end,
+                                                        ntiles, smem0, bar0, tile_mask, abort_flag,
                                                  lane);
   } else {
     uint32_t qf[NT][KSTEPS][2];
@@ -632,6 +652,38 @@ multi_query_cols_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensor
 
 namespace {
 
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_halves = nullptr;
+std::once_flag g_encode_halves_once;
+
+// Pool [NB][Hkv][B][D] (16-bit dtype) as a 3-D tensor {D, B, NB*Hkv} with
+// boxes of one 64-column half of min(B, 64) rows, 128-byte swizzle.
+bool encode_pool_halves_map(CUtensorMap* map, const void* base, int dtype, int64_t num_blocks,
+                            int num_kv_heads, int block_size, int head_size) {
+  std::call_once(g_encode_halves_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode_halves = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode_halves) return false;
+  const uint64_t D = head_size, B = block_size;
+  const uint64_t planes = (uint64_t)num_blocks * num_kv_heads;
+  if (planes == 0 || planes > 0x7fffffffull || D % 64 != 0) return false;
+  cuuint64_t dims[3] = {D, B, planes};
+  cuuint64_t strides[2] = {D * 2, B * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)(B < 64 ? B : 64), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode_halves(map,
+                         dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                         3, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 constexpr int mq_smem_bytes() {
   return 1024 + kMqStages * 2 * kMqTile * (D / 64) * 128 + 2 * kMqStages * 8 + 4 +
@@ -640,12 +692,22 @@ constexpr int mq_smem_bytes() {
 
 template <typename T, int D, int G>
 cudaError_t launch_mq_tdg(const MultiQueryArgs& a, cudaStream_t st) {
+  const int64_t rows_ = (int64_t)a.max_query_len * G;
+  const bool cols_kernel = (rows_ + kMqsCols - 1) / kMqsCols <= 2;
+  // the row kernel reads every K/V row many times: conflict-free halves; the
+  // column kernel streams: whole-row boxes
   CUtensorMap tk, tv;
-  if (!encode_kv_pool_map(&tk, a.kc, a.dtype, a.num_blocks, a.num_kv_heads, a.block_size,
-                          a.head_size) ||
-      !encode_kv_pool_map(&tv, a.vc, a.dtype, a.num_blocks, a.num_kv_heads, a.block_size,
-                          a.head_size))
-    return cudaErrorInvalidValue;
+  const bool ok =
+      cols_kernel
+          ? encode_kv_pool_map(&tk, a.kc, a.dtype, a.num_blocks, a.num_kv_heads, a.block_size,
+                               a.head_size) &&
+                encode_kv_pool_map(&tv, a.vc, a.dtype, a.num_blocks, a.num_kv_heads,
+                                   a.block_size, a.head_size)
+          : encode_pool_halves_map(&tk, a.kc, a.dtype, a.num_blocks, a.num_kv_heads,
+                                   a.block_size, a.head_size) &&
+                encode_pool_halves_map(&tv, a.vc, a.dtype, a.num_blocks, a.num_kv_heads,
+                                       a.block_size, a.head_size);
+  if (!ok) return cudaErrorInvalidValue;
   constexpr int smem = mq_smem_bytes<D>();
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
