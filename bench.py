@@ -60,6 +60,9 @@ def parse():
                     help="fp8: E4M3 pools (one new token per sequence)")
     ap.add_argument("--new-tokens", type=int, default=1,
                     help="new tokens per sequence per step (>1: causal multi-query attention)")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window in tokens for one-new-token decode (0 = none); "
+                         "blocks wholly before the window are released from the tables")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="use only the first N sequences (smaller profiling case)")
     return ap.parse_args()
@@ -377,10 +380,13 @@ def ours_arm(args):
     fp8 = args.kv_dtype == "fp8"
     if fp8 and N > 1:
         raise SystemExit("--kv-dtype fp8 runs one new token per sequence")
+    W = max(0, args.window)
+    if W and N > 1:
+        raise SystemExit("--window runs one new token per sequence")
     # orc_arrays: host copies for the CPU baseline, taken before any kernel
     # touches the pools (the 16-bit, one-new-token step only)
     orc_arrays = oracle_arrays(inp) if (rank == 0 and world == 1 and N == 1 and not fp8
-                                        and not args.no_cpu_baseline) else None
+                                        and not W and not args.no_cpu_baseline) else None
     kc, vc = inp.key_cache, inp.value_cache
     kscale = vscale = 1.0 / 48
     if fp8:   # E4M3 pools holding the same N(0,1) draws at scale 1/48
@@ -390,8 +396,16 @@ def ours_arm(args):
         torch.cuda.empty_cache()
     elt = 1 if fp8 else inp.q.element_size()
     lens = inp.seq_lens.cpu()
-    kv_bytes = kv_read_bytes(lens.tolist(), Hkv, D, elt)
-    tokens = int(lens.sum())
+    if W:   # attended tokens per sequence; skipped blocks' table entries -> -1
+        attended = [min(int(L), W) for L in lens.tolist()]
+        tab = inp.block_tables.cpu()
+        for s_, L in enumerate(lens.tolist()):
+            tab[s_, :max(0, L - W) // B] = -1
+        inp.block_tables.copy_(tab)
+    else:
+        attended = lens.tolist()
+    kv_bytes = kv_read_bytes(attended, Hkv, D, elt)
+    tokens = int(sum(attended))
     max_len = inp.max_seq_len
     P = args.partition
     g = dict(q=inp.q, k_new=inp.k_new, v_new=inp.v_new, tables=inp.block_tables,
@@ -409,8 +423,10 @@ def ours_arm(args):
         splits = 1 if ws_bytes == 0 else 2
         ptoks = None
     else:
-        splits, ptoks = pa.pa_decode_partitioning(S, cfg.num_q_heads, Hkv, B, max_len, P)
-        ws_bytes = pa.pa_decode_workspace_bytes(S, cfg.num_q_heads, Hkv, D, B, max_len, P)
+        covered = max_len if not W or W >= max_len else min(max_len, W + 63)
+        splits, ptoks = pa.pa_decode_partitioning(S, cfg.num_q_heads, Hkv, B, covered, P)
+        ws_bytes = pa.pa_decode_window_workspace_bytes(S, cfg.num_q_heads, Hkv, D, B, max_len,
+                                                       W, P)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     out = torch.empty_like(g["q"])
     slots = torch.empty(S * N, dtype=torch.int64, device=dev)
@@ -421,6 +437,14 @@ def ours_arm(args):
             pa.pa_multi_query_attention(t["q"], t["qsl"], kc, vc, t["tables"], t["lens"],
                                         inp.scale, Hkv, out, max_query_len=N, max_seq_len=max_len,
                                         partition_size=P, workspace=ws)
+        elif fp8 and W:
+            pa.pa_decode_attention_fp8_window(t["q"], kc, vc, t["tables"], t["lens"], inp.scale,
+                                              Hkv, kscale, vscale, W, out, max_seq_len=max_len,
+                                              partition_size=P, workspace=ws)
+        elif W:
+            pa.pa_decode_attention_window(t["q"], kc, vc, t["tables"], t["lens"], inp.scale, Hkv,
+                                          W, out, max_seq_len=max_len, partition_size=P,
+                                          workspace=ws)
         elif fp8:
             pa.pa_decode_attention_fp8(t["q"], kc, vc, t["tables"], t["lens"], inp.scale, Hkv,
                                        kscale, vscale, out, max_seq_len=max_len,
@@ -442,9 +466,11 @@ def ours_arm(args):
             ev[1].record(stream)
 
     launches_per_step = 3 + (1 if splits > 1 else 0)
-    label = cfg.name + ("_fp8" if fp8 else "") + (f"_q{N}" if N > 1 else "")
+    label = (cfg.name + ("_fp8" if fp8 else "") + (f"_q{N}" if N > 1 else "") +
+             (f"_w{W}" if W else ""))
     kernel_name = ("pa_multi_query_attention" if N > 1 else
-                   "pa_decode_attention_fp8" if fp8 else "pa_decode_attention")
+                   "pa_decode_attention_fp8" if fp8 else "pa_decode_attention") + (
+                       "_window" if W else "")
     for _ in range(max(3, args.warmup)):
         step(g)
     torch.cuda.synchronize()
@@ -583,8 +609,10 @@ def ours_arm(args):
                                           f"{cfg.num_q_heads}q/{Hkv}kv heads, D={D}, B={B}",
             "context_tokens": tokens, "kv_read_bytes_per_step": kv_bytes,
             "pool_blocks": inp.num_blocks, "partitions": splits, "partition_tokens": ptoks,
-            "l2": "inputs larger than L2 (KV pool %.2f GB >> 129 MB L2), no flush" %
-                  (2 * kc.numel() * elt / 1e9),
+            "l2": ("inputs larger than L2 (KV read per step %.2f GB, pool %.2f GB; "
+                   "129 MB L2), no flush" % (kv_bytes / 1e9, 2 * kc.numel() * elt / 1e9))
+                  if kv_bytes > 2 * 129e6 else
+                  "KV read per step %.3f GB fits in twice L2: L2-warm" % (kv_bytes / 1e9),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "roofline": {"bound": "hbm", "kernel": kernel_name,

@@ -294,7 +294,7 @@ PA_API int pa_reshape_and_cache_fp8(const void* k, const void* v, int64_t num_to
  * pa_decode_attention_fp8 — pa_decode_attention over fp8 pools: q and out of
  * `dtype`, K = code * k_scale, V = code * v_scale. Same partitioning and
  * workspace as pa_decode_attention (pa_decode_workspace_bytes applies).
- * Runs on the CUDA cores for every group size.
+ * k_scale and v_scale must be positive (else PA_ERR_SHAPE).
  */
 PA_API int pa_decode_attention_fp8(const void* q, const void* key_cache,
                                    const void* value_cache, const int32_t* block_tables,
@@ -304,6 +304,49 @@ PA_API int pa_decode_attention_fp8(const void* q, const void* key_cache,
                                    int dtype, float scale, float k_scale, float v_scale,
                                    int max_seq_len, int partition_size, void* out,
                                    void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
+ * Sliding-window decode. The pages name the window through the blocks the
+ * allocator may release ("PagedAttention 核心创新深度分析" §3.2
+ * allocate_slots, phase 1, and §3.3.1 get_num_blocks_to_allocate: skipped
+ * blocks = skipped tokens / block_size). Reading: the query of sequence s
+ * attends its last `window` tokens, the new token included:
+ *     lo = L - window  if 0 < window < L,  else 0
+ *     out[s,h] = sum_{lo <= j < L} softmax(x)_j * V_s[j]
+ * window = 0 is plain pa_decode_attention. The table entries of the leading
+ * lo / block_size blocks are never read: the caller may have released those
+ * blocks and left any value there (e.g. -1).
+ *
+ * pa_decode_window_workspace_bytes — scratch for the windowed calls with the
+ * same arguments (window >= 0; returns a negative status on invalid sizes).
+ * pa_decode_attention_window — pa_decode_attention with a window.
+ * pa_decode_attention_fp8_window — pa_decode_attention_fp8 with a window.
+ * Other arguments, layouts and errors as in the unwindowed calls; window < 0
+ * is PA_ERR_SHAPE.
+ */
+PA_API int64_t pa_decode_window_workspace_bytes(int num_seqs, int num_q_heads,
+                                                int num_kv_heads, int head_size,
+                                                int block_size, int max_seq_len, int window,
+                                                int partition_size);
+PA_API int pa_decode_attention_window(const void* q, const void* key_cache,
+                                      const void* value_cache, const int32_t* block_tables,
+                                      int64_t block_tables_stride, const int32_t* seq_lens,
+                                      int num_seqs, int num_q_heads, int num_kv_heads,
+                                      int head_size, int block_size, int64_t num_blocks,
+                                      int dtype, float scale, int window, int max_seq_len,
+                                      int partition_size, void* out, void* workspace,
+                                      int64_t workspace_bytes, void* stream);
+PA_API int pa_decode_attention_fp8_window(const void* q, const void* key_cache,
+                                          const void* value_cache,
+                                          const int32_t* block_tables,
+                                          int64_t block_tables_stride,
+                                          const int32_t* seq_lens, int num_seqs,
+                                          int num_q_heads, int num_kv_heads, int head_size,
+                                          int block_size, int64_t num_blocks, int dtype,
+                                          float scale, float k_scale, float v_scale,
+                                          int window, int max_seq_len, int partition_size,
+                                          void* out, void* workspace,
+                                          int64_t workspace_bytes, void* stream);
 
 /*
  * pa_copy_blocks — block-level copy-on-write data movement ([P2] Figure 8:

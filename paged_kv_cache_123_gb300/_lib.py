@@ -47,6 +47,14 @@ SIGNATURES = {
     "pa_decode_attention_fp8": ([_c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32, _c_i32,
                                  _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_f, _c_f, _c_i32,
                                  _c_i32, _c_p, _c_p, _c_i64, _c_p], _c_i32),
+    "pa_decode_window_workspace_bytes": ([_c_i32] * 8, _c_i64),
+    "pa_decode_attention_window": ([_c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32,
+                                    _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32,
+                                    _c_i32, _c_i32, _c_p, _c_p, _c_i64, _c_p], _c_i32),
+    "pa_decode_attention_fp8_window": ([_c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32,
+                                        _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_f,
+                                        _c_f, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i64,
+                                        _c_p], _c_i32),
     "pa_copy_blocks": ([_c_p, _c_p, _c_i32, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p], _c_i32),
     "pa_get_device_error": ([_c_p, _c_p], _c_i32),
     "pa_map_to_kernel_blocks": ([_c_p, _c_i64, _c_i64, _c_i64, _c_i32, _c_p, _c_i64, _c_p],

@@ -107,6 +107,25 @@ int64_t workspace_for(int num_seqs, int num_q_heads, int head_size, int splits) 
   return ((acc + 255) / 256) * 256 + ml;
 }
 
+// Longest token range one sequence's partitions cover: with a sliding
+// window the range starts at the window's first token rounded down to a
+// 64-token tile (the kernels' window_base), so it spans at most
+// window + 63 tokens.
+int covered_len(int max_seq_len, int window) {
+  if (window <= 0 || window >= max_seq_len) return max_seq_len;
+  return std::min<int64_t>(max_seq_len, (int64_t)window + 63);
+}
+
+// Validation, partitioning and launch shared by the decode entry points
+// (16-bit/fp32 pools or E4M3 pools, with or without a window).
+int run_decode(const void* q, const void* key_cache, const void* value_cache,
+               const int32_t* block_tables, int64_t block_tables_stride,
+               const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+               int head_size, int block_size, int64_t num_blocks, int dtype, float scale,
+               bool fp8, float k_scale, float v_scale, int window, int max_seq_len,
+               int partition_size, void* out, void* workspace, int64_t workspace_bytes,
+               void* stream);
+
 int check_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
                        int block_size, int max_seq_len) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0)
@@ -222,41 +241,35 @@ int pa_decode_attention(const void* q, const void* key_cache, const void* value_
                         int64_t num_blocks, int dtype, float scale, int max_seq_len,
                         int partition_size, void* out, void* workspace,
                         int64_t workspace_bytes, void* stream) {
-  if (elt_bytes(dtype) == 0) return PA_ERR_DTYPE;
+  return run_decode(q, key_cache, value_cache, block_tables, block_tables_stride, seq_lens,
+                    num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
+                    dtype, scale, false, 1.f, 1.f, 0, max_seq_len, partition_size, out,
+                    workspace, workspace_bytes, stream);
+}
+
+int64_t pa_decode_window_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                         int head_size, int block_size, int max_seq_len,
+                                         int window, int partition_size) {
+  if (window < 0) return PA_ERR_SHAPE;
   int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size,
                               block_size, max_seq_len);
   if (st != PA_OK) return st;
-  if (partition_size < 0 || num_blocks < 0 || block_tables_stride < 0) return PA_ERR_SHAPE;
-  if ((int64_t)max_seq_len > block_tables_stride * block_size) return PA_ERR_OUT_OF_RANGE;
-  if (num_seqs == 0) return PA_OK;
-  if (!q || !key_cache || !value_cache || !block_tables || !seq_lens || !out)
-    return PA_ERR_NULL;
-  if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) || !aligned16(out))
-    return PA_ERR_ALIGN;
-  int dev;
-  st = device_setup(&dev);
-  if (st != PA_OK) return st;
-  pa::DecodeArgs a;
-  a.q = q; a.kc = key_cache; a.vc = value_cache;
-  a.tables = block_tables; a.table_stride = block_tables_stride; a.seq_lens = seq_lens;
-  a.num_seqs = num_seqs; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
-  a.head_size = head_size; a.block_size = block_size; a.num_blocks = num_blocks;
-  a.dtype = dtype; a.scale = scale; a.max_seq_len = max_seq_len;
-  partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size,
-               g_sm_count[dev], &a.num_splits, &a.partition);
-  const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);
-  a.ws_acc = nullptr; a.ws_ml = nullptr;
-  if (need > 0) {
-    if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return PA_ERR_ALIGN;
-    const int64_t n = (int64_t)num_seqs * num_q_heads * a.num_splits;
-    a.ws_acc = static_cast<float*>(workspace);
-    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                       ((n * head_size * 4 + 255) / 256) * 256);
-  }
-  a.out = out;
-  a.err = g_err_ptr[dev];
-  return check_launch(pa::launch_decode(a, (cudaStream_t)stream));
+  return pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                                   covered_len(max_seq_len, window), partition_size);
+}
+
+int pa_decode_attention_window(const void* q, const void* key_cache, const void* value_cache,
+                               const int32_t* block_tables, int64_t block_tables_stride,
+                               const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_size, int block_size,
+                               int64_t num_blocks, int dtype, float scale, int window,
+                               int max_seq_len, int partition_size, void* out,
+                               void* workspace, int64_t workspace_bytes, void* stream) {
+  if (window < 0) return PA_ERR_SHAPE;
+  return run_decode(q, key_cache, value_cache, block_tables, block_tables_stride, seq_lens,
+                    num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
+                    dtype, scale, false, 1.f, 1.f, window, max_seq_len, partition_size, out,
+                    workspace, workspace_bytes, stream);
 }
 
 // Context partitions of the multi-query kernel. Only short query runs
@@ -388,41 +401,25 @@ int pa_decode_attention_fp8(const void* q, const void* key_cache, const void* va
                             int dtype, float scale, float k_scale, float v_scale,
                             int max_seq_len, int partition_size, void* out, void* workspace,
                             int64_t workspace_bytes, void* stream) {
-  if (elt_bytes(dtype) == 0) return PA_ERR_DTYPE;
-  int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
-                              max_seq_len);
-  if (st != PA_OK) return st;
-  if (partition_size < 0 || num_blocks < 0 || block_tables_stride < 0) return PA_ERR_SHAPE;
-  if (!(k_scale > 0.f) || !(v_scale > 0.f)) return PA_ERR_SHAPE;
-  if ((int64_t)max_seq_len > block_tables_stride * block_size) return PA_ERR_OUT_OF_RANGE;
-  if (num_seqs == 0) return PA_OK;
-  if (!q || !key_cache || !value_cache || !block_tables || !seq_lens || !out) return PA_ERR_NULL;
-  if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) || !aligned16(out))
-    return PA_ERR_ALIGN;
-  int dev;
-  st = device_setup(&dev);
-  if (st != PA_OK) return st;
-  pa::DecodeArgs a;
-  a.q = q; a.kc = key_cache; a.vc = value_cache;
-  a.tables = block_tables; a.table_stride = block_tables_stride; a.seq_lens = seq_lens;
-  a.num_seqs = num_seqs; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
-  a.head_size = head_size; a.block_size = block_size; a.num_blocks = num_blocks;
-  a.dtype = dtype; a.scale = scale; a.max_seq_len = max_seq_len;
-  partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size,
-               g_sm_count[dev], &a.num_splits, &a.partition);
-  const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);
-  a.ws_acc = nullptr; a.ws_ml = nullptr;
-  if (need > 0) {
-    if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return PA_ERR_ALIGN;
-    const int64_t n = (int64_t)num_seqs * num_q_heads * a.num_splits;
-    a.ws_acc = static_cast<float*>(workspace);
-    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                       ((n * head_size * 4 + 255) / 256) * 256);
-  }
-  a.out = out;
-  a.err = g_err_ptr[dev];
-  return check_launch(pa::launch_decode_fp8(a, k_scale, v_scale, (cudaStream_t)stream));
+  return run_decode(q, key_cache, value_cache, block_tables, block_tables_stride, seq_lens,
+                    num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
+                    dtype, scale, true, k_scale, v_scale, 0, max_seq_len, partition_size, out,
+                    workspace, workspace_bytes, stream);
+}
+
+int pa_decode_attention_fp8_window(const void* q, const void* key_cache,
+                                   const void* value_cache, const int32_t* block_tables,
+                                   int64_t block_tables_stride, const int32_t* seq_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_size, int block_size, int64_t num_blocks, int dtype,
+                                   float scale, float k_scale, float v_scale, int window,
+                                   int max_seq_len, int partition_size, void* out,
+                                   void* workspace, int64_t workspace_bytes, void* stream) {
+  if (window < 0) return PA_ERR_SHAPE;
+  return run_decode(q, key_cache, value_cache, block_tables, block_tables_stride, seq_lens,
+                    num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
+                    dtype, scale, true, k_scale, v_scale, window, max_seq_len, partition_size,
+                    out, workspace, workspace_bytes, stream);
 }
 
 int pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
@@ -495,3 +492,55 @@ int pa_get_device_error(int* code_out, void* stream) {
 }
 
 }  // extern "C"
+
+namespace {
+
+int run_decode(const void* q, const void* key_cache, const void* value_cache,
+               const int32_t* block_tables, int64_t block_tables_stride,
+               const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+               int head_size, int block_size, int64_t num_blocks, int dtype, float scale,
+               bool fp8, float k_scale, float v_scale, int window, int max_seq_len,
+               int partition_size, void* out, void* workspace, int64_t workspace_bytes,
+               void* stream) {
+  if (elt_bytes(dtype) == 0) return PA_ERR_DTYPE;
+  int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size,
+                              block_size, max_seq_len);
+  if (st != PA_OK) return st;
+  if (partition_size < 0 || num_blocks < 0 || block_tables_stride < 0) return PA_ERR_SHAPE;
+  if (fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f))) return PA_ERR_SHAPE;
+  if ((int64_t)max_seq_len > block_tables_stride * block_size) return PA_ERR_OUT_OF_RANGE;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !key_cache || !value_cache || !block_tables || !seq_lens || !out)
+    return PA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) || !aligned16(out))
+    return PA_ERR_ALIGN;
+  int dev;
+  st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  pa::DecodeArgs a;
+  a.q = q; a.kc = key_cache; a.vc = value_cache;
+  a.tables = block_tables; a.table_stride = block_tables_stride; a.seq_lens = seq_lens;
+  a.num_seqs = num_seqs; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size; a.block_size = block_size; a.num_blocks = num_blocks;
+  a.dtype = dtype; a.scale = scale; a.max_seq_len = max_seq_len; a.window = window;
+  partitioning(num_seqs, num_q_heads, num_kv_heads, block_size,
+               covered_len(max_seq_len, window), partition_size, g_sm_count[dev],
+               &a.num_splits, &a.partition);
+  const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);
+  a.ws_acc = nullptr; a.ws_ml = nullptr;
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PA_ERR_ALIGN;
+    const int64_t n = (int64_t)num_seqs * num_q_heads * a.num_splits;
+    a.ws_acc = static_cast<float*>(workspace);
+    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       ((n * head_size * 4 + 255) / 256) * 256);
+  }
+  a.out = out;
+  a.err = g_err_ptr[dev];
+  cudaStream_t cs = (cudaStream_t)stream;
+  return check_launch(fp8 ? pa::launch_decode_fp8(a, k_scale, v_scale, cs)
+                          : pa::launch_decode(a, cs));
+}
+
+}  // namespace

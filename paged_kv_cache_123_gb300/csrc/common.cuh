@@ -15,6 +15,17 @@ __device__ __forceinline__ void latch(int* err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
 }
 
+// Sliding-window decode: a query attends tokens lo .. L-1 with
+// lo = L - window when 0 < window < L, else 0 (window 0 = whole sequence).
+// Partition 0 starts at lo rounded down to a 64-token tile, so every tile
+// and TMA piece keeps the alignment of the unwindowed kernels; rows before
+// lo are masked, and pieces entirely before lo are neither looked up in the
+// block table nor loaded.
+__device__ __forceinline__ int window_lo(int L, int window) {
+  return (window > 0 && L > window) ? L - window : 0;
+}
+__device__ __forceinline__ int window_base(int lo) { return lo & ~63; }
+
 // ---- 16-byte vector <-> fp32 conversion per storage type ------------------
 template <typename T> struct Vec;
 

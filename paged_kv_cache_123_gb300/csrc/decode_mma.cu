@@ -95,10 +95,11 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     }
     return;
   }
-  const int t0 = split * a.partition;
+  const int lo = window_lo(L, a.window);
+  const int t0 = window_base(lo) + split * a.partition;
   if (t0 >= L) return;
   const int t1 = min(L, t0 + a.partition);
-  const int nsplit = (L + a.partition - 1) / a.partition;
+  const int nsplit = (L - window_base(lo) + a.partition - 1) / a.partition;
   const int ntiles = (t1 - t0 + kTile - 1) / kTile;
   const int B = a.block_size;
   const int bshift = __ffs(B) - 1;
@@ -138,7 +139,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       const int tok = ts + lane * R;
       int64_t blk = -1;
       bool mine = false;
-      if (lane < npieces && tok < te) {
+      if (lane < npieces && tok < te && tok + R > lo) {
         blk = trow[tok >> bshift];
         mine = blk >= 0 && blk < a.num_blocks;
         if (!mine) latch(a.err, PA_ERR_OUT_OF_RANGE);
@@ -208,7 +209,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         bool row_ok = false;
         {
           const int r = warp * 16 + (lane & 15);   // row inside the tile
-          row_ok = (ts + r < te) && ((tile_mask[st] >> (r / R)) & 1u);
+          row_ok = (ts + r < te) && (ts + r >= lo) && ((tile_mask[st] >> (r / R)) & 1u);
         }
         const unsigned okm = __ballot_sync(0xffffffffu, row_ok) & 0xffffu;
         const uint32_t kb = kst, vb = vst;

@@ -57,10 +57,12 @@ decode_simt_kernel(const DecodeArgs a) {
     }
     return;
   }
-  const int t0 = split * a.partition;
+  const int lo = window_lo(L, a.window);
+  const int tb = window_base(lo);
+  const int t0 = tb + split * a.partition;
   if (t0 >= L) return;
   const int t1 = min(L, t0 + a.partition);
-  const int nsplit = (L + a.partition - 1) / a.partition;
+  const int nsplit = (L - tb + a.partition - 1) / a.partition;
 
   // q for the G heads of this group, pre-multiplied by scale * log2(e) so
   // the softmax runs on exp2.
@@ -101,7 +103,7 @@ decode_simt_kernel(const DecodeArgs a) {
       ok[u] = false;
       ku[u] = make_uint4(0, 0, 0, 0);
       vu[u] = ku[u];
-      if (t < t1) {
+      if (t >= lo && t < t1) {
         const int64_t blk = trow[t >> bshift];
         if (blk >= 0 && blk < a.num_blocks) {
           const int64_t off = ((blk * Hkv + kvh) * B + (t & (B - 1))) * D + sub * VEC;
@@ -216,7 +218,8 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a) {
   const int s = blockIdx.y, h = blockIdx.x, d = threadIdx.x;
   const int L = a.seq_lens[s];
   if (bad_length(a, L) || L == 0) return;
-  const int n = (L + a.partition - 1) / a.partition;
+  const int tb = window_base(window_lo(L, a.window));
+  const int n = (L - tb + a.partition - 1) / a.partition;
   if (n <= 1) return;
   const int64_t base = ((int64_t)s * a.num_q_heads + h) * a.num_splits;
   float M = kNegInf;

@@ -161,10 +161,11 @@ decode_fp8_kernel(const DecodeArgs a, float k_scale, float v_scale) {
     }
     return;
   }
-  const int t0 = split * a.partition;
+  const int lo = window_lo(L, a.window);
+  const int t0 = window_base(lo) + split * a.partition;
   if (t0 >= L) return;
   const int t1 = min(L, t0 + a.partition);
-  const int nsplit = (L + a.partition - 1) / a.partition;
+  const int nsplit = (L - window_base(lo) + a.partition - 1) / a.partition;
 
   float qf[G][8];
   {
@@ -199,7 +200,7 @@ decode_fp8_kernel(const DecodeArgs a, float k_scale, float v_scale) {
       ok[u] = false;
       ku[u] = make_uint2(0, 0);
       vu[u] = ku[u];
-      if (t < t1) {
+      if (t >= lo && t < t1) {
         const int64_t blk = trow[t >> bshift];
         if (blk >= 0 && blk < a.num_blocks) {
           const int64_t off = ((blk * Hkv + kvh) * B + (t & (B - 1))) * D + sub * 8;

@@ -44,6 +44,7 @@ struct DecodeArgs {
   int dtype;
   float scale;
   int max_seq_len;
+  int window;        // sliding window in tokens; 0 = the whole sequence
   int partition;     // tokens per split (multiple of max(64, block_size))
   int num_splits;    // ceil(max_seq_len / partition), >= 1
   void* out;

@@ -263,3 +263,71 @@ def pa_decode_attention_fp8(q: torch.Tensor, key_cache: torch.Tensor, value_cach
         float(v_scale), int(max_seq_len), int(partition_size), ptr(out), ptr(workspace),
         ws_bytes, stream_handle(stream)))
     return out
+
+
+def pa_decode_window_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                     head_size: int, block_size: int, max_seq_len: int,
+                                     window: int, partition_size: int = 0) -> int:
+    n = lib().pa_decode_window_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                               block_size, max_seq_len, window, partition_size)
+    if n < 0:
+        check("pa_decode_window_workspace_bytes", int(n))
+    return int(n)
+
+
+def _window_call(name, q, key_cache, value_cache, block_tables, seq_lens, scale, num_kv_heads,
+                 scales, window, out, max_seq_len, partition_size, workspace, stream):
+    for n, t in (("q", q), ("key_cache", key_cache), ("value_cache", value_cache)):
+        _dev(t, n)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = key_cache.shape
+    pool_dtype = torch.uint8 if scales else q.dtype
+    if Hkv != num_kv_heads or Dk != D or value_cache.shape != key_cache.shape:
+        raise ValueError("pool shape does not match q / num_kv_heads")
+    if key_cache.dtype != pool_dtype or value_cache.dtype != pool_dtype:
+        raise ValueError(f"pools must be {pool_dtype}")
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out")
+    need = pa_decode_window_workspace_bytes(S, Hq, Hkv, D, B, max_seq_len, window,
+                                            partition_size)
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(name, getattr(lib(), name)(
+        ptr(q), ptr(key_cache), ptr(value_cache), ptr(block_tables), block_tables.shape[1],
+        ptr(seq_lens), S, Hq, Hkv, D, B, NB, DTYPE_CODE[q.dtype], float(scale),
+        *[float(x) for x in scales], int(window), int(max_seq_len), int(partition_size),
+        ptr(out), ptr(workspace), ws_bytes, stream_handle(stream)))
+    return out
+
+
+def pa_decode_attention_window(q: torch.Tensor, key_cache: torch.Tensor,
+                               value_cache: torch.Tensor, block_tables: torch.Tensor,
+                               seq_lens: torch.Tensor, scale: float, num_kv_heads: int,
+                               window: int, out: Optional[torch.Tensor] = None, *,
+                               max_seq_len: int, partition_size: int = 0,
+                               workspace: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """Sliding-window decode: each query attends its sequence's last
+    `window` tokens (0 = all); table entries of blocks wholly before the
+    window are never read."""
+    return _window_call("pa_decode_attention_window", q, key_cache, value_cache, block_tables,
+                        seq_lens, scale, num_kv_heads, (), window, out, max_seq_len,
+                        partition_size, workspace, stream)
+
+
+def pa_decode_attention_fp8_window(q: torch.Tensor, key_cache: torch.Tensor,
+                                   value_cache: torch.Tensor, block_tables: torch.Tensor,
+                                   seq_lens: torch.Tensor, scale: float, num_kv_heads: int,
+                                   k_scale: float, v_scale: float, window: int,
+                                   out: Optional[torch.Tensor] = None, *, max_seq_len: int,
+                                   partition_size: int = 0,
+                                   workspace: Optional[torch.Tensor] = None,
+                                   stream=None) -> torch.Tensor:
+    """pa_decode_attention_window over E4M3 pools."""
+    return _window_call("pa_decode_attention_fp8_window", q, key_cache, value_cache,
+                        block_tables, seq_lens, scale, num_kv_heads, (k_scale, v_scale),
+                        window, out, max_seq_len, partition_size, workspace, stream)
