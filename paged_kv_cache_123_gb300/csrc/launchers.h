@@ -104,5 +104,8 @@ struct MultiQueryArgs {
   int* err;
 };
 cudaError_t launch_multi_query(const MultiQueryArgs& a, cudaStream_t st);
+// The attention launch alone (no partition combine) of the tcgen05 kernel
+// for runs of more than 64 (token, head) rows per KV head (prefill_tc.cu).
+cudaError_t launch_multi_query_tc(const MultiQueryArgs& a, cudaStream_t st);
 
 }  // namespace pa

@@ -731,6 +731,10 @@ cudaError_t launch_mq_tdg(const MultiQueryArgs& a, cudaStream_t st) {
     if (attr_cols != cudaSuccess) return attr_cols;
     dim3 grid((unsigned)(col_tiles * a.num_splits), a.num_kv_heads, a.num_seqs);
     multi_query_cols_kernel<T, D, G><<<grid, kMqThreads, smem, st>>>(a, tk, tv);
+  } else if (rows > kMqTile) {
+    // long runs (prefill chunks): the tcgen05 kernel, 128 rows per CTA
+    cudaError_t e = launch_multi_query_tc(a, st);
+    if (e != cudaSuccess) return e;
   } else {
     dim3 grid((unsigned)(tiles * a.num_splits), a.num_kv_heads, a.num_seqs);
     multi_query_kernel<T, D, G><<<grid, kMqThreads, smem, st>>>(a, tk, tv);

@@ -1,0 +1,588 @@
+// Causal paged attention for long runs of new tokens (prefill chunks) on the
+// fifth-generation tensor cores: tcgen05.mma with operands in shared memory
+// and fp32 accumulators in tensor memory (TMEM).
+//
+// What is computed is the multi-query attention of prefill_mma.cu: new token
+// i of sequence s (n_s new tokens, L_s tokens in the pool including them)
+// sits at position L_s - n_s + i and attends to positions 0 .. L_s - n_s + i
+// through the block table ("vLLM 的 PagedAttention：显存管理如何撑起大模型推理"
+// §2.5: one token budget covers prefill chunks; "PagedAttention 核心创新深度
+// 分析" §2.3: the slot mapping places any number of tokens per request).
+//
+// One CTA owns 128 rows — (new token, query head) pairs of one KV head,
+// query-major — and walks its causal KV range in tiles of 128 tokens:
+//   * a producer warp loads the CTA's Q tile once (3-D TMA straight from the
+//     [tokens][heads][D] query tensor) and each K/V tile by 3-D TMA boxes of
+//     one 64-column half of one block's rows (128-byte swizzle), two stages;
+//   * one thread of an MMA warp issues S = Q K^T (M = 128 rows, N = 128
+//     tokens, K = D) into one of two TMEM score buffers, and O += P V (M =
+//     128, N = D, K = 128 tokens; V read N-major straight from its token
+//     rows) into the TMEM output, each completing on an mbarrier
+//     (tcgen05.commit);
+//   * four softmax warps own one row each per thread (TMEM lane = row): they
+//     read the scores with tcgen05.ld, apply the causal limit and the scale in
+//     the log2 domain, write P (16-bit, K-major, 128-byte swizzle) to shared
+//     memory for the next MMA, and rescale the TMEM output only when a row's
+//     running maximum grew by more than 2^8 (the exponentials stay below 256,
+//     and the final division uses the same reference), so most tiles skip
+//     the rescale.
+// S of tile j+1 is computed while the softmax warps work on tile j.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <type_traits>
+
+#include "common.cuh"
+#include "launchers.h"
+#include "tcgen05.cuh"
+#include "tma.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kTcRows = 128;              // query rows per CTA (MMA M)
+constexpr int kTcKv = 128;                // KV tokens per tile
+constexpr int kTcSoftmaxWarps = 4;
+constexpr int kTcProducerWarp = 4;
+constexpr int kTcMmaWarp = 5;
+constexpr int kTcThreads = 6 * 32;
+constexpr uint32_t kTcTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256, 256+D)
+constexpr uint32_t kTcOCol = 256;
+constexpr long long kTcWaitCycles = 4000000000LL;
+constexpr float kTcRescaleLog2 = 8.f;
+#define kNegInfT (-__int_as_float(0x7f800000))
+
+template <int D>
+struct TcLayout {
+  static constexpr int HALVES = D / 64;
+  static constexpr int HALF_BYTES = kTcRows * 128;          // 128 rows x 64 columns
+  static constexpr int Q_BYTES = HALVES * HALF_BYTES;
+  static constexpr int KV_HALF = kTcKv * 128;
+  static constexpr int KV_BYTES = HALVES * KV_HALF;         // one K (or V) tile
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  static constexpr int P_BYTES = 2 * HALF_BYTES;            // 128 rows x 128 tokens
+  // two P buffers: P_j is written while P V of tile j-1 may still run
+  static constexpr int Q_OFF = 0;
+  static constexpr int STAGE_OFF = Q_OFF + Q_BYTES;
+  static constexpr int P_OFF = STAGE_OFF + 2 * STAGE_BYTES;
+  static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
+  // q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done, done
+  static constexpr int NBARS = 12;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;     // tmem base, abort, tile masks
+  static constexpr int SMEM = MISC_OFF + 32 + 1024;        // + alignment slack
+};
+
+enum : int { kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = 3, kBarSFull = 5, kBarSFree = 7,
+             kBarPFull = 9, kBarODone = 10, kBarDone = 11 };
+
+template <typename T>
+struct Pack2;
+template <>
+struct Pack2<__nv_bfloat16> {
+  __device__ __forceinline__ static uint32_t pack(float a, float b, float& ra, float& rb) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 f = __bfloat1622float2(h);
+    ra = f.x;
+    rb = f.y;
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ __forceinline__ static uint32_t pack_out(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+};
+template <>
+struct Pack2<__half> {
+  __device__ __forceinline__ static uint32_t pack(float a, float b, float& ra, float& rb) {
+    __half2 h = __floats2half2_rn(a, b);
+    const float2 f = __half22float2(h);
+    ra = f.x;
+    rb = f.y;
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ __forceinline__ static uint32_t pack_out(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+};
+
+// Producer warp: the Q tile once, then the K/V tiles of [kv_lo, kv_end) into
+// the two-stage ring. Lane p loads piece p (R = min(B, 128) rows of one
+// block) of a tile, both 64-column halves of K and of V.
+template <int D>
+__device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
+                           const CUtensorMap* tmK, const CUtensorMap* tmV, const int32_t* trow,
+                           int kvh, int q_tok, int kv_lo, int kv_end, int ntiles, uint32_t s0,
+                           uint32_t bar, volatile uint32_t* tile_mask, volatile int* abort_flag,
+                           int lane, int G) {
+  using Ly = TcLayout<D>;
+  if (lane == 0) {
+    prefetch_tensormap(tmQ);
+    prefetch_tensormap(tmK);
+    prefetch_tensormap(tmV);
+    mbar_arrive_expect_tx(bar + 8u * kBarQ, (uint32_t)Ly::Q_BYTES);
+#pragma unroll
+    for (int h = 0; h < Ly::HALVES; ++h)
+      tma_load_3d(s0 + Ly::Q_OFF + h * Ly::HALF_BYTES, tmQ, h * 64, kvh * G, q_tok,
+                  bar + 8u * kBarQ);
+  }
+  const int B = a.block_size;
+  const int bshift = __ffs(B) - 1;
+  const int R = B < kTcKv ? B : kTcKv;
+  const int npieces = kTcKv / R;                 // <= 16 (B >= 8)
+  int issued = 0;
+  for (int i = 0; i < ntiles; ++i) {
+    const int st = i & 1;
+    const int ts = kv_lo + i * kTcKv;
+    const int te = min(kv_end, ts + kTcKv);
+    const int tok = ts + lane * R;
+    int64_t blk = -1;
+    bool mine = false;
+    if (lane < npieces && tok < te) {
+      blk = trow[tok >> bshift];
+      mine = blk >= 0 && blk < a.num_blocks;
+      if (!mine) latch(a.err, PA_ERR_OUT_OF_RANGE);
+    }
+    const unsigned pm = __ballot_sync(0xffffffffu, mine);
+    int ok = 1;
+    if (lane == 0) {
+      if (i >= 2)
+        ok = mbar_wait_bounded(bar + 8u * (kBarKvEmpty + st), ((i >> 1) - 1) & 1, abort_flag,
+                               kTcWaitCycles);
+      if (ok) {
+        tile_mask[st] = pm;
+        mbar_arrive_expect_tx(bar + 8u * (kBarKvFull + st),
+                              (uint32_t)__popc(pm) * 2u * (uint32_t)R * (uint32_t)(D * 2));
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+    if (mine) {
+      const int z = (int)(blk * a.num_kv_heads + kvh);
+      const int y = tok & (B - 1);
+      const uint32_t kd = s0 + Ly::STAGE_OFF + st * Ly::STAGE_BYTES + lane * R * 128;
+#pragma unroll
+      for (int h = 0; h < Ly::HALVES; ++h) {
+        tma_load_3d(kd + h * Ly::KV_HALF, tmK, h * 64, y, z, bar + 8u * (kBarKvFull + st));
+        tma_load_3d(kd + Ly::KV_BYTES + h * Ly::KV_HALF, tmV, h * 64, y, z,
+                    bar + 8u * (kBarKvFull + st));
+      }
+    }
+    issued = i + 1;
+  }
+  // let this warp's copies land before the CTA can leave
+  if (lane == 0) {
+    mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
+    for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+      mbar_wait_bounded(bar + 8u * (kBarKvFull + (j & 1)), (j >> 1) & 1, abort_flag,
+                        kTcWaitCycles);
+  }
+}
+
+// MMA issue (one thread): S_j = Q K_j^T into TMEM buffer j&1, then
+// O += P_{j-1} V_{j-1} once the softmax warps have written P_{j-1}.
+template <typename T, int D>
+__device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
+                         volatile int* abort_flag) {
+  using Ly = TcLayout<D>;
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  constexpr uint32_t idS = idesc_f16(kBf16, kTcRows, kTcKv, false, false);
+  constexpr uint32_t idO = idesc_f16(kBf16, kTcRows, D, false, true);
+  const uint32_t qa = s0 + Ly::Q_OFF, pa = s0 + Ly::P_OFF;
+  auto issue_pv = [&](int t) -> bool {
+    if (!mbar_wait_bounded(bar + 8u * kBarPFull, t & 1, abort_flag, kTcWaitCycles)) return false;
+    tc_fence_after();
+    const uint32_t vb = s0 + Ly::STAGE_OFF + (t & 1) * Ly::STAGE_BYTES + Ly::KV_BYTES;
+    const uint32_t pb = pa + (t & 1) * Ly::P_BYTES;
+#pragma unroll
+    for (int ks = 0; ks < kTcKv / 16; ++ks) {
+      const uint64_t ad = smem_desc_sw128(pb + (ks >> 2) * Ly::HALF_BYTES + (ks & 3) * 32, 16, 1024);
+      // V tile: token rows of 64 head dims per 128-byte line (N-major);
+      // 16 tokens per k-step, the second half of D at KV_HALF
+      const uint64_t bd = smem_desc_sw128(vb + ks * 2048, Ly::KV_HALF, 1024);
+      mma_f16_ss(tmem + kTcOCol, ad, bd, idO, (t > 0 || ks > 0) ? 1u : 0u);
+    }
+    mma_commit(bar + 8u * kBarODone);
+    mma_commit(bar + 8u * (kBarKvEmpty + (t & 1)));
+    return true;
+  };
+  bool ok = mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
+  for (int j = 0; ok && j < ntiles; ++j) {
+    const int st = j & 1;
+    ok = mbar_wait_bounded(bar + 8u * (kBarKvFull + st), (j >> 1) & 1, abort_flag,
+                           kTcWaitCycles);
+    if (ok && j >= 2)
+      ok = mbar_wait_bounded(bar + 8u * (kBarSFree + st), ((j >> 1) - 1) & 1, abort_flag,
+                             kTcWaitCycles);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t kb = s0 + Ly::STAGE_OFF + st * Ly::STAGE_BYTES;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint64_t ad = smem_desc_sw128(qa + (ks >> 2) * Ly::HALF_BYTES + (ks & 3) * 32, 16, 1024);
+      const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * Ly::KV_HALF + (ks & 3) * 32, 16, 1024);
+      mma_f16_ss(tmem + st * kTcKv, ad, bd, idS, ks > 0 ? 1u : 0u);
+    }
+    mma_commit(bar + 8u * (kBarSFull + st));
+    if (j >= 1) ok = issue_pv(j - 1);
+  }
+  if (ok && ntiles > 0) issue_pv(ntiles - 1);
+  // every MMA issued above has completed once this barrier fires
+  mma_commit(bar + 8u * kBarDone);
+  mbar_wait_bounded(bar + 8u * kBarDone, 0, abort_flag, kTcWaitCycles);
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kTcThreads, 1)
+multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV) {
+  using Ly = TcLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t bar = s0 + Ly::BAR_OFF;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile uint32_t* tile_mask = misc + 2;
+
+  const int s = blockIdx.z, kvh = blockIdx.y;
+  const int row_tiles = (a.max_query_len * G + kTcRows - 1) / kTcRows;
+  const int qt = row_tiles - 1 - (int)(blockIdx.x % row_tiles);   // longest rows first
+  const int split = (int)(blockIdx.x / row_tiles);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hq = a.num_q_heads;
+  const int q0 = a.qsl[s];
+  const int n = a.qsl[s + 1] - q0;
+  const int L = a.seq_lens[s];
+  if (n < 0 || n > a.max_query_len || L < n || L > a.max_seq_len ||
+      (int64_t)L > a.table_stride * a.block_size || q0 < 0) {
+    if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) latch(a.err, PA_ERR_OUT_OF_RANGE);
+    return;
+  }
+  const int r0 = qt * kTcRows;                      // first row of this CTA
+  if (r0 >= n * G) return;
+  const int i_last = min(n - 1, (r0 + kTcRows - 1) / G);
+  const int kv_all = L - n + i_last + 1;            // keys any row here may see
+  const int kv_lo = split * a.partition;
+  if (kv_lo >= kv_all) return;
+  const int kv_end = min(kv_all, kv_lo + a.partition);
+  const int ntiles = (kv_end - kv_lo + kTcKv - 1) / kTcKv;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar + 8u * kBarQ, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar + 8u * (kBarKvFull + i), 1);
+      mbar_init(bar + 8u * (kBarKvEmpty + i), 1);
+      mbar_init(bar + 8u * (kBarSFull + i), 1);
+      mbar_init(bar + 8u * (kBarSFree + i), kTcSoftmaxWarps);
+    }
+    mbar_init(bar + 8u * kBarPFull, kTcSoftmaxWarps);
+    mbar_init(bar + 8u * kBarODone, 1);
+    mbar_init(bar + 8u * kBarDone, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == kTcMmaWarp) {
+    tmem_alloc(s0 + Ly::MISC_OFF, kTcTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  if (warp == kTcProducerWarp) {
+    tc_produce<D>(a, &tmQ, &tmK, &tmV, a.tables + (int64_t)s * a.table_stride, kvh,
+                  q0 + r0 / G, kv_lo, kv_end, ntiles, s0, bar, tile_mask, abort_flag, lane, G);
+  } else if (warp == kTcMmaWarp) {
+    if (lane == 0) tc_issue<T, D>(ntiles, s0, bar, tmem, abort_flag);
+    __syncwarp();
+  } else {
+    // ---- softmax warps: thread = row (TMEM lane) r
+    const int r = warp * 32 + lane;
+    const int rr = r0 + r;
+    const int i = rr / G;
+    const bool rv = i < n;
+    const int pos = rv ? L - n + i : -1;            // causal limit of this row
+    const float sl2 = a.scale * kLog2e;
+    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    const int B = a.block_size;
+    const int R = B < kTcKv ? B : kTcKv;
+    const int rshift = __ffs(R) - 1;
+    const unsigned full_mask = (kTcKv / R) >= 32 ? 0xffffffffu : ((1u << (kTcKv / R)) - 1u);
+    float m_use = kNegInfT, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      const int ts = kv_lo + j * kTcKv;
+      const int te = min(kv_end, ts + kTcKv);
+      ok = mbar_wait_bounded(bar + 8u * (kBarSFull + st), (j >> 1) & 1, abort_flag,
+                             kTcWaitCycles) &&
+           mbar_wait_bounded(bar + 8u * (kBarKvFull + st), (j >> 1) & 1, abort_flag,
+                             kTcWaitCycles);
+      // tcgen05.ld / st are warp-collective: the whole warp goes on or stops
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const unsigned pm = tile_mask[st];
+      const bool whole = (pm == full_mask) && (te - ts == kTcKv);
+      const int lim = min(pos, te - 1) - ts;        // last column this row may use
+      // valid columns of each 32-column chunk: causal / length limit and
+      // loaded pieces
+      uint32_t vmask[kTcKv / 32];
+#pragma unroll
+      for (int ch = 0; ch < kTcKv / 32; ++ch) {
+        const int c0 = ch * 32;
+        uint32_t m = lim < c0 ? 0u : (lim >= c0 + 31 ? 0xffffffffu : ((2u << (lim - c0)) - 1u));
+        if (!whole) {
+          uint32_t pmask = 0;
+          if (R >= 32) {
+            pmask = ((pm >> (c0 >> rshift)) & 1u) ? 0xffffffffu : 0u;
+          } else {
+            for (int k = 0; k < 32 / R; ++k)
+              if ((pm >> ((c0 >> rshift) + k)) & 1u) pmask |= ((1u << R) - 1u) << (k * R);
+          }
+          m &= pmask;
+        }
+        vmask[ch] = m;
+      }
+      const uint32_t sadr = tmem + lanes + st * kTcKv;
+      // pass 1: row maximum of the valid scaled scores
+      float mx = kNegInfT;
+#pragma unroll
+      for (int ch = 0; ch < kTcKv / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(sadr + ch * 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          mx = fmaxf(mx, ((vmask[ch] >> e) & 1u) ? __uint_as_float(v[e]) * sl2 : kNegInfT);
+      }
+      const float m_new = fmaxf(m_use, mx);
+      float alpha = 1.f;
+      bool resc = false;
+      if (m_use == kNegInfT) {
+        m_use = m_new;                  // nothing accumulated for this row yet
+      } else if (m_new > m_use + kTcRescaleLog2) {
+        alpha = exp2f(m_use - m_new);
+        resc = true;
+        m_use = m_new;
+        l *= alpha;
+      }
+      // pass 2: P = 2^(x - m_use) rounded to the input type, written chunk by
+      // chunk to P buffer j&1 (row r; 16-byte chunk k holds tokens 8k..8k+7,
+      // 64 tokens per half); l sums the rounded weights the MMA multiplies
+      const bool live = m_use != kNegInfT;
+      const uint32_t p_row = s0 + Ly::P_OFF + st * Ly::P_BYTES + r * 128;
+#pragma unroll
+      for (int ch = 0; ch < kTcKv / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(sadr + ch * 32, v);
+        const uint32_t vm = live ? vmask[ch] : 0u;
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = ((vm >> e) & 1u) ? exp2f(__uint_as_float(v[e]) * sl2 - m_use) : 0.f;
+          const float p1 =
+              ((vm >> (e + 1)) & 1u) ? exp2f(__uint_as_float(v[e + 1]) * sl2 - m_use) : 0.f;
+          float q0r, q1r;
+          pk[e >> 1] = Pack2<T>::pack(p0, p1, q0r, q1r);
+          l += q0r + q1r;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int k = ch * 4 + kk;
+          const uint32_t adr = p_row + (k >> 3) * Ly::HALF_BYTES + (((k & 7) ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                       ::"r"(adr), "r"(pk[4 * kk]), "r"(pk[4 * kk + 1]), "r"(pk[4 * kk + 2]),
+                         "r"(pk[4 * kk + 3]) : "memory");
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + 8u * (kBarSFree + st));
+      // the output is rescaled only when some row of the warp needs it; P V
+      // of tile j-1 must have completed first (P V of tile j-2 completed
+      // before S of tile j, which this thread has seen)
+      if (__any_sync(0xffffffffu, resc)) {
+        if (j >= 1) {
+          ok = mbar_wait_bounded(bar + 8u * kBarODone, (j - 1) & 1, abort_flag, kTcWaitCycles);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lanes + kTcOCol + ch * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tmem_st32(tmem + lanes + kTcOCol + ch * 32, v);
+        }
+        tmem_wait_st();
+      }
+      // V rows that hold no token of this tile may contain anything (NaN
+      // included) and 0 * NaN is NaN inside the MMA: clear them (row r)
+      if (!whole) {
+        const bool row_ok = r < te - ts && ((pm >> (r >> rshift)) & 1u);
+        if (!row_ok) {
+          const uint32_t vrow = s0 + Ly::STAGE_OFF + st * Ly::STAGE_BYTES + Ly::KV_BYTES + r * 128;
+#pragma unroll
+          for (int h = 0; h < Ly::HALVES; ++h)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
+                           ::"r"(vrow + h * Ly::KV_HALF + k * 16), "r"(0u) : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + 8u * kBarPFull);
+    }
+    if (ok && ntiles > 0) {
+      // the MMA thread commits kBarDone after its last P V
+      ok = mbar_wait_bounded(bar + 8u * kBarDone, 0, abort_flag, kTcWaitCycles);
+      tc_fence_after();
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      const int64_t t = q0 + i;
+      const int head = kvh * G + rr % G;
+      const int count = rv ? (pos + a.partition) / a.partition : 0;
+      const bool direct = rv && count == 1 && split == 0;
+      const bool partial = rv && count > 1 && split < count;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      T* out = reinterpret_cast<T*>(a.out);
+      const int64_t slot = (t * Hq + head) * a.num_splits + split;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lanes + kTcOCol + ch * 32, v);
+        if (direct) {
+          uint32_t* op = reinterpret_cast<uint32_t*>(out + (t * Hq + head) * D + ch * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
+            w.y = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
+            w.z = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
+            w.w = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
+            reinterpret_cast<uint4*>(op)[q] = w;
+          }
+        } else if (partial) {
+          float4* acc = reinterpret_cast<float4*>(a.ws_acc + slot * D + ch * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            acc[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+      }
+      if (partial) {
+        a.ws_ml[2 * slot] = m_use;
+        a.ws_ml[2 * slot + 1] = l;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTcMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTcTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) latch(a.err, PA_ERR_TIMEOUT);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_tc_encode = nullptr;
+std::once_flag g_tc_encode_once;
+
+bool tc_encoder() {
+  std::call_once(g_tc_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_tc_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_tc_encode != nullptr;
+}
+
+bool tc_encode3(CUtensorMap* map, const void* base, int dtype, const uint64_t (&dims)[3],
+                const uint64_t (&strides)[2], const uint32_t (&box)[3]) {
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {strides[0], strides[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_tc_encode(map,
+                     dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     3, const_cast<void*>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_tc(const MultiQueryArgs& a, cudaStream_t st) {
+  using Ly = TcLayout<D>;
+  if (!tc_encoder()) return cudaErrorNotSupported;
+  const uint64_t planes = (uint64_t)a.num_blocks * a.num_kv_heads;
+  if (planes == 0 || planes > 0x7fffffffull || a.num_tokens <= 0 ||
+      a.num_tokens > 0x7fffffffll)
+    return cudaErrorInvalidValue;
+  const uint32_t R = a.block_size < kTcKv ? (uint32_t)a.block_size : (uint32_t)kTcKv;
+  CUtensorMap tq, tk, tv;
+  // q [tokens][Hq][D]: a box is one 64-column half of G heads x 128/G tokens
+  const bool ok =
+      tc_encode3(&tq, a.q, a.dtype, {(uint64_t)D, (uint64_t)a.num_q_heads, (uint64_t)a.num_tokens},
+                 {(uint64_t)D * 2, (uint64_t)a.num_q_heads * D * 2},
+                 {64u, (uint32_t)G, (uint32_t)(kTcRows / G)}) &&
+      // pools [NB][Hkv][B][D] as {D, B, NB*Hkv}: one half of R rows of one slice
+      tc_encode3(&tk, a.kc, a.dtype, {(uint64_t)D, (uint64_t)a.block_size, planes},
+                 {(uint64_t)D * 2, (uint64_t)a.block_size * D * 2}, {64u, R, 1u}) &&
+      tc_encode3(&tv, a.vc, a.dtype, {(uint64_t)D, (uint64_t)a.block_size, planes},
+                 {(uint64_t)D * 2, (uint64_t)a.block_size * D * 2}, {64u, R, 1u});
+  if (!ok) return cudaErrorInvalidValue;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, []() {
+    attr = cudaFuncSetAttribute(multi_query_tc_kernel<T, D, G>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
+  });
+  if (attr != cudaSuccess) return attr;
+  const int64_t tiles = ((int64_t)a.max_query_len * G + kTcRows - 1) / kTcRows;
+  if (tiles == 0 || a.num_seqs == 0) return cudaSuccess;
+  if (tiles * a.num_splits > 0x7fffffffll) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)(tiles * a.num_splits), a.num_kv_heads, a.num_seqs);
+  multi_query_tc_kernel<T, D, G><<<grid, kTcThreads, Ly::SMEM, st>>>(a, tq, tk, tv);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_tc_d(const MultiQueryArgs& a, cudaStream_t st) {
+  switch (a.num_q_heads / a.num_kv_heads) {
+    case 1: return launch_tc<T, D, 1>(a, st);
+    case 2: return launch_tc<T, D, 2>(a, st);
+    case 4: return launch_tc<T, D, 4>(a, st);
+    case 8: return launch_tc<T, D, 8>(a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t launch_tc_t(const MultiQueryArgs& a, cudaStream_t st) {
+  if (a.head_size == 64) return launch_tc_d<T, 64>(a, st);
+  if (a.head_size == 128) return launch_tc_d<T, 128>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_multi_query_tc(const MultiQueryArgs& a, cudaStream_t st) {
+  if (a.dtype == PA_BF16) return launch_tc_t<__nv_bfloat16>(a, st);
+  if (a.dtype == PA_F16) return launch_tc_t<__half>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

@@ -204,3 +204,53 @@ def test_bad_block_id_is_latched_and_other_sequences_are_exact(n_new):
     q0, q1 = int(b["qsl"][1]), int(b["qsl"][2])
     keep = [t for t in range(out.shape[0]) if not (q0 <= t < q1)]
     assert max_abs_err(out[keep], want[keep]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype,G,D", [("bf16", 8, 128), ("f16", 1, 128), ("bf16", 4, 64)])
+def test_long_prefill_with_growing_logits(dtype, G, D):
+    """Keys scaled up along the sequence make each row's running maximum jump
+    by far more than 2^8 across KV tiles, so the tensor-core kernel's output
+    rescale runs many times; several 128-row tiles and KV tiles, ragged."""
+    ctx, n_new = [700, 0, 37], [300, 257, 129]
+    b = make_batch(dtype, D, 2 * G, 2, 16, ctx, n_new, 321 + G + D)
+    f = lambda j: 1.0 + j / 40.0
+    kc = b["kc"].float()
+    for s, c in enumerate(ctx):
+        for j in range(c):
+            kc[int(b["tables"][s, j // 16]), :, j % 16, :] *= f(j)
+    b["kc"] = kc.to(b["kc"].dtype)
+    kn = b["kn"].float()
+    for t, p in enumerate(b["pos"].tolist()):
+        kn[t] *= f(p)
+    b["kn"] = kn.to(b["kn"].dtype)
+    out, want, _ = run_both(b)
+    assert torch.isfinite(out.float()).all()
+    assert max_abs_err(out, want) <= TOL[dtype]
+    assert pa.pa_get_device_error() == 0
+
+
+def test_long_prefill_many_tiles_against_oracle_sampled():
+    """A 1024-token prefill chunk after 3000 cached tokens (GQA group 8):
+    8 x 128-row tiles per KV head, 32 KV tiles; sampled rows vs the oracle."""
+    b = make_batch("bf16", 128, 16, 2, 16, [3000], [1024], 404)
+    kco, vco = np_(b["kc"]), np_(b["vc"])
+    slots_o = oracle.slot_mapping(b["qsl"].numpy(), b["pos"].numpy(), b["tables"].numpy(), 16)
+    oracle.reshape_and_cache(np_(b["kn"]), np_(b["vn"]), slots_o, kco, vco, 16)
+    g = {k: v.to(DEV) for k, v in b.items() if isinstance(v, torch.Tensor)}
+    slots = pa.pa_compute_slot_mapping(g["qsl"], g["pos"], g["tables"], 16)
+    pa.pa_reshape_and_cache(g["kn"], g["vn"], slots, g["kc"], g["vc"])
+    out = pa.pa_multi_query_attention(g["q"], g["qsl"], g["kc"], g["vc"], g["tables"], g["lens"],
+                                      b["scale"], 2, max_query_len=1024, max_seq_len=4024)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    rows = [0, 1, 127, 128, 129, 500, 895, 1023]
+    q = np_(b["q"])
+    for i in rows:
+        L_i = 3000 + i + 1
+        for h in (0, 7, 8, 15):
+            kvh = h // 8
+            K = oracle.gather_kv(kco, b["tables"][0].numpy(), L_i, kvh, 16, "bf16")
+            V = oracle.gather_kv(vco, b["tables"][0].numpy(), L_i, kvh, 16, "bf16")
+            want = oracle.decode_attention_one(oracle.upcast(q[i, h], "bf16"), K, V, b["scale"])
+            got = out[i, h].double().cpu().numpy()
+            assert np.abs(got - want).max() <= TOL["bf16"], (i, h)
