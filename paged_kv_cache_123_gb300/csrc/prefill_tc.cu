@@ -75,6 +75,13 @@ struct TcLayout {
 enum : int { kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = 3, kBarSFull = 5, kBarSFree = 7,
              kBarPFull = 9, kBarODone = 10, kBarDone = 11 };
 
+// 2^x by the SFU's ex2.approx (inputs here are <= 8; -inf gives +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <typename T>
 struct Pack2;
 template <>
@@ -329,11 +336,9 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       const unsigned pm = tile_mask[st];
       const bool whole = (pm == full_mask) && (te - ts == kTcKv);
       const int lim = min(pos, te - 1) - ts;        // last column this row may use
-      // valid columns of each 32-column chunk: causal / length limit and
-      // loaded pieces
-      uint32_t vmask[kTcKv / 32];
-#pragma unroll
-      for (int ch = 0; ch < kTcKv / 32; ++ch) {
+      // valid columns of 32-column chunk ch: causal / length limit and loaded
+      // pieces
+      auto chunk_mask = [&](int ch) -> uint32_t {
         const int c0 = ch * 32;
         uint32_t m = lim < c0 ? 0u : (lim >= c0 + 31 ? 0xffffffffu : ((2u << (lim - c0)) - 1u));
         if (!whole) {
@@ -346,18 +351,37 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
           }
           m &= pmask;
         }
-        vmask[ch] = m;
-      }
+        return m;
+      };
+      // interior tiles (every column valid for every row of the warp) skip
+      // the per-column masks
+      const bool fast = __all_sync(0xffffffffu, whole && lim >= kTcKv - 1) && sl2 > 0.f;
       const uint32_t sadr = tmem + lanes + st * kTcKv;
       // pass 1: row maximum of the valid scaled scores
       float mx = kNegInfT;
+      if (fast) {
+        float mx0 = kNegInfT, mx1 = kNegInfT;
+#pragma unroll 1
+        for (int ch = 0; ch < kTcKv / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(sadr + ch * 32, v);
 #pragma unroll
-      for (int ch = 0; ch < kTcKv / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(sadr + ch * 32, v);
+          for (int e = 0; e < 32; e += 2) {
+            mx0 = fmaxf(mx0, __uint_as_float(v[e]));
+            mx1 = fmaxf(mx1, __uint_as_float(v[e + 1]));
+          }
+        }
+        mx = fmaxf(mx0, mx1) * sl2;       // the scale is positive: max commutes
+      } else {
+#pragma unroll 1
+        for (int ch = 0; ch < kTcKv / 32; ++ch) {
+          const uint32_t m = chunk_mask(ch);
+          uint32_t v[32];
+          tmem_ld32(sadr + ch * 32, v);
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          mx = fmaxf(mx, ((vmask[ch] >> e) & 1u) ? __uint_as_float(v[e]) * sl2 : kNegInfT);
+          for (int e = 0; e < 32; ++e)
+            mx = fmaxf(mx, ((m >> e) & 1u) ? __uint_as_float(v[e]) * sl2 : kNegInfT);
+        }
       }
       const float m_new = fmaxf(m_use, mx);
       float alpha = 1.f;
@@ -372,33 +396,42 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       }
       // pass 2: P = 2^(x - m_use) rounded to the input type, written chunk by
       // chunk to P buffer j&1 (row r; 16-byte chunk k holds tokens 8k..8k+7,
-      // 64 tokens per half); l sums the rounded weights the MMA multiplies
+      // 64 tokens per half); l sums the rounded weights the MMA multiplies,
+      // so the normalised weights sum to one
       const bool live = m_use != kNegInfT;
+      const float nm = -m_use;
       const uint32_t p_row = s0 + Ly::P_OFF + st * Ly::P_BYTES + r * 128;
-#pragma unroll
+      float l0 = 0.f, l1 = 0.f;
+#pragma unroll 1
       for (int ch = 0; ch < kTcKv / 32; ++ch) {
+        const uint32_t vm = fast ? 0xffffffffu : (live ? chunk_mask(ch) : 0u);
         uint32_t v[32];
         tmem_ld32(sadr + ch * 32, v);
-        const uint32_t vm = live ? vmask[ch] : 0u;
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ((vm >> e) & 1u) ? exp2f(__uint_as_float(v[e]) * sl2 - m_use) : 0.f;
-          const float p1 =
-              ((vm >> (e + 1)) & 1u) ? exp2f(__uint_as_float(v[e + 1]) * sl2 - m_use) : 0.f;
+          float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), sl2, nm));
+          float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), sl2, nm));
+          if (!fast) {
+            p0 = ((vm >> e) & 1u) ? p0 : 0.f;
+            p1 = ((vm >> (e + 1)) & 1u) ? p1 : 0.f;
+          }
           float q0r, q1r;
           pk[e >> 1] = Pack2<T>::pack(p0, p1, q0r, q1r);
-          l += q0r + q1r;
+          l0 += q0r;
+          l1 += q1r;
         }
+        const uint32_t prow = p_row + (ch >> 1) * Ly::HALF_BYTES;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const int k = ch * 4 + kk;
-          const uint32_t adr = p_row + (k >> 3) * Ly::HALF_BYTES + (((k & 7) ^ (r & 7)) << 4);
+          const int k = (ch & 1) * 4 + kk;           // chunk inside the 64-token half
+          const uint32_t adr = prow + ((k ^ (r & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                        ::"r"(adr), "r"(pk[4 * kk]), "r"(pk[4 * kk + 1]), "r"(pk[4 * kk + 2]),
                          "r"(pk[4 * kk + 3]) : "memory");
         }
       }
+      l += l0 + l1;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar + 8u * (kBarSFree + st));
