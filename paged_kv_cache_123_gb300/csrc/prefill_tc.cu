@@ -43,9 +43,10 @@ namespace {
 constexpr int kTcRows = 128;              // query rows per CTA (MMA M)
 constexpr int kTcKv = 128;                // KV tokens per tile
 constexpr int kTcSoftmaxWarps = 4;
-constexpr int kTcProducerWarp = 4;
+constexpr int kTcKProducerWarp = 4;     // Q and K tiles
 constexpr int kTcMmaWarp = 5;
-constexpr int kTcThreads = 6 * 32;
+constexpr int kTcVProducerWarp = 6;     // V tiles
+constexpr int kTcThreads = 7 * 32;
 constexpr uint32_t kTcTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256, 256+D)
 constexpr uint32_t kTcOCol = 256;
 constexpr long long kTcWaitCycles = 4000000000LL;
@@ -59,21 +60,22 @@ struct TcLayout {
   static constexpr int Q_BYTES = HALVES * HALF_BYTES;
   static constexpr int KV_HALF = kTcKv * 128;
   static constexpr int KV_BYTES = HALVES * KV_HALF;         // one K (or V) tile
-  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
   static constexpr int P_BYTES = 2 * HALF_BYTES;            // 128 rows x 128 tokens
   // two P buffers: P_j is written while P V of tile j-1 may still run
   static constexpr int Q_OFF = 0;
-  static constexpr int STAGE_OFF = Q_OFF + Q_BYTES;
-  static constexpr int P_OFF = STAGE_OFF + 2 * STAGE_BYTES;
+  static constexpr int K_OFF = Q_OFF + Q_BYTES;            // two K stages
+  static constexpr int V_OFF = K_OFF + 2 * KV_BYTES;         // two V stages
+  static constexpr int P_OFF = V_OFF + 2 * KV_BYTES;
   static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
-  // q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done, done
-  static constexpr int NBARS = 12;
-  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;     // tmem base, abort, tile masks
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2],
+  // p_full, o_done, done
+  static constexpr int NBARS = 16;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;     // tmem base, abort flag
   static constexpr int SMEM = MISC_OFF + 32 + 1024;        // + alignment slack
 };
 
-enum : int { kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = 3, kBarSFull = 5, kBarSFree = 7,
-             kBarPFull = 9, kBarODone = 10, kBarDone = 11 };
+enum : int { kBarQ = 0, kBarKFull = 1, kBarKEmpty = 3, kBarVFull = 5, kBarVEmpty = 7,
+             kBarSFull = 9, kBarSFree = 11, kBarPFull = 13, kBarODone = 14, kBarDone = 15 };
 
 // 2^x by the SFU's ex2.approx (inputs here are <= 8; -inf gives +0)
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -113,76 +115,86 @@ struct Pack2<__half> {
   }
 };
 
-// Producer warp: the Q tile once, then the K/V tiles of [kv_lo, kv_end) into
-// the two-stage ring. Lane p loads piece p (R = min(B, 128) rows of one
-// block) of a tile, both 64-column halves of K and of V.
-template <int D>
+// Lanes of the producer warp that hold a block piece of tile [ts, te):
+// piece p = R = min(B, 128) rows of one block; bit p set when its table
+// entry names a block of the pool.
+__device__ __forceinline__ unsigned tc_piece_mask(const MultiQueryArgs& a, const int32_t* trow,
+                                                  int ts, int te, int lane, int64_t* blk_out) {
+  const int B = a.block_size;
+  const int R = B < kTcKv ? B : kTcKv;
+  const int tok = ts + lane * R;
+  int64_t blk = -1;
+  bool mine = false;
+  if (lane < kTcKv / R && tok < te) {
+    blk = trow[tok >> (__ffs(B) - 1)];
+    mine = blk >= 0 && blk < a.num_blocks;
+  }
+  *blk_out = blk;
+  return __ballot_sync(0xffffffffu, mine);
+}
+
+// Producer warp for one operand (K, with the Q tile first, or V): the tiles
+// of [kv_lo, kv_end) into that operand's two-stage ring. Lane p loads piece
+// p of a tile, both 64-column halves. K stages are released when S of the
+// tile has been computed, V stages when P V has: K runs ahead of V.
+template <int D, bool IS_V>
 __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
-                           const CUtensorMap* tmK, const CUtensorMap* tmV, const int32_t* trow,
-                           int kvh, int q_tok, int kv_lo, int kv_end, int ntiles, uint32_t s0,
-                           uint32_t bar, volatile uint32_t* tile_mask, volatile int* abort_flag,
-                           int lane, int G) {
+                           const CUtensorMap* tm, const int32_t* trow, int kvh, int q_tok,
+                           int kv_lo, int kv_end, int ntiles, uint32_t s0, uint32_t bar,
+                           volatile int* abort_flag, int lane, int G) {
   using Ly = TcLayout<D>;
+  const int full = IS_V ? kBarVFull : kBarKFull;
+  const int empty = IS_V ? kBarVEmpty : kBarKEmpty;
+  const uint32_t base = s0 + (IS_V ? Ly::V_OFF : Ly::K_OFF);
   if (lane == 0) {
-    prefetch_tensormap(tmQ);
-    prefetch_tensormap(tmK);
-    prefetch_tensormap(tmV);
-    mbar_arrive_expect_tx(bar + 8u * kBarQ, (uint32_t)Ly::Q_BYTES);
+    prefetch_tensormap(tm);
+    if (!IS_V) {
+      prefetch_tensormap(tmQ);
+      mbar_arrive_expect_tx(bar + 8u * kBarQ, (uint32_t)Ly::Q_BYTES);
 #pragma unroll
-    for (int h = 0; h < Ly::HALVES; ++h)
-      tma_load_3d(s0 + Ly::Q_OFF + h * Ly::HALF_BYTES, tmQ, h * 64, kvh * G, q_tok,
-                  bar + 8u * kBarQ);
+      for (int h = 0; h < Ly::HALVES; ++h)
+        tma_load_3d(s0 + Ly::Q_OFF + h * Ly::HALF_BYTES, tmQ, h * 64, kvh * G, q_tok,
+                    bar + 8u * kBarQ);
+    }
   }
   const int B = a.block_size;
-  const int bshift = __ffs(B) - 1;
   const int R = B < kTcKv ? B : kTcKv;
-  const int npieces = kTcKv / R;                 // <= 16 (B >= 8)
   int issued = 0;
   for (int i = 0; i < ntiles; ++i) {
     const int st = i & 1;
     const int ts = kv_lo + i * kTcKv;
     const int te = min(kv_end, ts + kTcKv);
-    const int tok = ts + lane * R;
-    int64_t blk = -1;
-    bool mine = false;
-    if (lane < npieces && tok < te) {
-      blk = trow[tok >> bshift];
-      mine = blk >= 0 && blk < a.num_blocks;
-      if (!mine) latch(a.err, PA_ERR_OUT_OF_RANGE);
-    }
-    const unsigned pm = __ballot_sync(0xffffffffu, mine);
+    int64_t blk;
+    const unsigned pm = tc_piece_mask(a, trow, ts, te, lane, &blk);
+    const bool mine = (pm >> lane) & 1u;
+    if (!IS_V && lane < kTcKv / R && ts + lane * R < te && !mine)
+      latch(a.err, PA_ERR_OUT_OF_RANGE);
     int ok = 1;
     if (lane == 0) {
       if (i >= 2)
-        ok = mbar_wait_bounded(bar + 8u * (kBarKvEmpty + st), ((i >> 1) - 1) & 1, abort_flag,
+        ok = mbar_wait_bounded(bar + 8u * (empty + st), ((i >> 1) - 1) & 1, abort_flag,
                                kTcWaitCycles);
-      if (ok) {
-        tile_mask[st] = pm;
-        mbar_arrive_expect_tx(bar + 8u * (kBarKvFull + st),
-                              (uint32_t)__popc(pm) * 2u * (uint32_t)R * (uint32_t)(D * 2));
-      }
+      if (ok)
+        mbar_arrive_expect_tx(bar + 8u * (full + st),
+                              (uint32_t)__popc(pm) * (uint32_t)R * (uint32_t)(D * 2));
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
     if (mine) {
       const int z = (int)(blk * a.num_kv_heads + kvh);
-      const int y = tok & (B - 1);
-      const uint32_t kd = s0 + Ly::STAGE_OFF + st * Ly::STAGE_BYTES + lane * R * 128;
+      const int y = (ts + lane * R) & (B - 1);
+      const uint32_t d = base + st * Ly::KV_BYTES + lane * R * 128;
 #pragma unroll
-      for (int h = 0; h < Ly::HALVES; ++h) {
-        tma_load_3d(kd + h * Ly::KV_HALF, tmK, h * 64, y, z, bar + 8u * (kBarKvFull + st));
-        tma_load_3d(kd + Ly::KV_BYTES + h * Ly::KV_HALF, tmV, h * 64, y, z,
-                    bar + 8u * (kBarKvFull + st));
-      }
+      for (int h = 0; h < Ly::HALVES; ++h)
+        tma_load_3d(d + h * Ly::KV_HALF, tm, h * 64, y, z, bar + 8u * (full + st));
     }
     issued = i + 1;
   }
   // let this warp's copies land before the CTA can leave
   if (lane == 0) {
-    mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
+    if (!IS_V) mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
     for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-      mbar_wait_bounded(bar + 8u * (kBarKvFull + (j & 1)), (j >> 1) & 1, abort_flag,
-                        kTcWaitCycles);
+      mbar_wait_bounded(bar + 8u * (full + (j & 1)), (j >> 1) & 1, abort_flag, kTcWaitCycles);
   }
 }
 
@@ -198,8 +210,11 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
   const uint32_t qa = s0 + Ly::Q_OFF, pa = s0 + Ly::P_OFF;
   auto issue_pv = [&](int t) -> bool {
     if (!mbar_wait_bounded(bar + 8u * kBarPFull, t & 1, abort_flag, kTcWaitCycles)) return false;
+    if (!mbar_wait_bounded(bar + 8u * (kBarVFull + (t & 1)), (t >> 1) & 1, abort_flag,
+                           kTcWaitCycles))
+      return false;
     tc_fence_after();
-    const uint32_t vb = s0 + Ly::STAGE_OFF + (t & 1) * Ly::STAGE_BYTES + Ly::KV_BYTES;
+    const uint32_t vb = s0 + Ly::V_OFF + (t & 1) * Ly::KV_BYTES;
     const uint32_t pb = pa + (t & 1) * Ly::P_BYTES;
 #pragma unroll
     for (int ks = 0; ks < kTcKv / 16; ++ks) {
@@ -210,20 +225,20 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
       mma_f16_ss(tmem + kTcOCol, ad, bd, idO, (t > 0 || ks > 0) ? 1u : 0u);
     }
     mma_commit(bar + 8u * kBarODone);
-    mma_commit(bar + 8u * (kBarKvEmpty + (t & 1)));
+    mma_commit(bar + 8u * (kBarVEmpty + (t & 1)));
     return true;
   };
   bool ok = mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
   for (int j = 0; ok && j < ntiles; ++j) {
     const int st = j & 1;
-    ok = mbar_wait_bounded(bar + 8u * (kBarKvFull + st), (j >> 1) & 1, abort_flag,
+    ok = mbar_wait_bounded(bar + 8u * (kBarKFull + st), (j >> 1) & 1, abort_flag,
                            kTcWaitCycles);
     if (ok && j >= 2)
       ok = mbar_wait_bounded(bar + 8u * (kBarSFree + st), ((j >> 1) - 1) & 1, abort_flag,
                              kTcWaitCycles);
     if (!ok) break;
     tc_fence_after();
-    const uint32_t kb = s0 + Ly::STAGE_OFF + st * Ly::STAGE_BYTES;
+    const uint32_t kb = s0 + Ly::K_OFF + st * Ly::KV_BYTES;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       const uint64_t ad = smem_desc_sw128(qa + (ks >> 2) * Ly::HALF_BYTES + (ks & 3) * 32, 16, 1024);
@@ -231,6 +246,7 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
       mma_f16_ss(tmem + st * kTcKv, ad, bd, idS, ks > 0 ? 1u : 0u);
     }
     mma_commit(bar + 8u * (kBarSFull + st));
+    mma_commit(bar + 8u * (kBarKEmpty + st));
     if (j >= 1) ok = issue_pv(j - 1);
   }
   if (ok && ntiles > 0) issue_pv(ntiles - 1);
@@ -252,7 +268,6 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
   const uint32_t bar = s0 + Ly::BAR_OFF;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-  volatile uint32_t* tile_mask = misc + 2;
 
   const int s = blockIdx.z, kvh = blockIdx.y;
   const int row_tiles = (a.max_query_len * G + kTcRows - 1) / kTcRows;
@@ -280,8 +295,10 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
   if (threadIdx.x == 0) {
     mbar_init(bar + 8u * kBarQ, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar + 8u * (kBarKvFull + i), 1);
-      mbar_init(bar + 8u * (kBarKvEmpty + i), 1);
+      mbar_init(bar + 8u * (kBarKFull + i), 1);
+      mbar_init(bar + 8u * (kBarKEmpty + i), 1);
+      mbar_init(bar + 8u * (kBarVFull + i), 1);
+      mbar_init(bar + 8u * (kBarVEmpty + i), 1);
       mbar_init(bar + 8u * (kBarSFull + i), 1);
       mbar_init(bar + 8u * (kBarSFree + i), kTcSoftmaxWarps);
     }
@@ -300,9 +317,13 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
-  if (warp == kTcProducerWarp) {
-    tc_produce<D>(a, &tmQ, &tmK, &tmV, a.tables + (int64_t)s * a.table_stride, kvh,
-                  q0 + r0 / G, kv_lo, kv_end, ntiles, s0, bar, tile_mask, abort_flag, lane, G);
+  const int32_t* trow = a.tables + (int64_t)s * a.table_stride;
+  if (warp == kTcKProducerWarp) {
+    tc_produce<D, false>(a, &tmQ, &tmK, trow, kvh, q0 + r0 / G, kv_lo, kv_end, ntiles, s0, bar,
+                         abort_flag, lane, G);
+  } else if (warp == kTcVProducerWarp) {
+    tc_produce<D, true>(a, &tmQ, &tmV, trow, kvh, q0 + r0 / G, kv_lo, kv_end, ntiles, s0, bar,
+                        abort_flag, lane, G);
   } else if (warp == kTcMmaWarp) {
     if (lane == 0) tc_issue<T, D>(ntiles, s0, bar, tmem, abort_flag);
     __syncwarp();
@@ -325,15 +346,16 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       const int st = j & 1;
       const int ts = kv_lo + j * kTcKv;
       const int te = min(kv_end, ts + kTcKv);
+      // which block pieces of the tile exist (the producers load exactly
+      // these); the table entries are read by this warp itself
+      int64_t blk_unused;
+      const unsigned pm = tc_piece_mask(a, trow, ts, te, lane, &blk_unused);
       ok = mbar_wait_bounded(bar + 8u * (kBarSFull + st), (j >> 1) & 1, abort_flag,
-                             kTcWaitCycles) &&
-           mbar_wait_bounded(bar + 8u * (kBarKvFull + st), (j >> 1) & 1, abort_flag,
                              kTcWaitCycles);
       // tcgen05.ld / st are warp-collective: the whole warp goes on or stops
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const unsigned pm = tile_mask[st];
       const bool whole = (pm == full_mask) && (te - ts == kTcKv);
       const int lim = min(pos, te - 1) - ts;        // last column this row may use
       // valid columns of 32-column chunk ch: causal / length limit and loaded
@@ -458,9 +480,15 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       // V rows that hold no token of this tile may contain anything (NaN
       // included) and 0 * NaN is NaN inside the MMA: clear them (row r)
       if (!whole) {
+        // the V tile must have landed before its rows are cleared (its stage
+        // is not refilled before P V of this tile, so the phase is current)
+        ok = mbar_wait_bounded(bar + 8u * (kBarVFull + st), (j >> 1) & 1, abort_flag,
+                               kTcWaitCycles);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
         const bool row_ok = r < te - ts && ((pm >> (r >> rshift)) & 1u);
         if (!row_ok) {
-          const uint32_t vrow = s0 + Ly::STAGE_OFF + st * Ly::STAGE_BYTES + Ly::KV_BYTES + r * 128;
+          const uint32_t vrow = s0 + Ly::V_OFF + st * Ly::KV_BYTES + r * 128;
 #pragma unroll
           for (int h = 0; h < Ly::HALVES; ++h)
 #pragma unroll
