@@ -49,6 +49,7 @@ constexpr int kTcVProducerWarp = 6;     // V tiles
 constexpr int kTcThreads = 7 * 32;
 constexpr uint32_t kTcTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256, 256+D)
 constexpr uint32_t kTcOCol = 256;
+constexpr uint32_t kTcLCol = 384;          // row sums of P: P x ones, 16 columns
 constexpr long long kTcWaitCycles = 4000000000LL;
 constexpr float kTcRescaleLog2 = 8.f;
 #define kNegInfT (-__int_as_float(0x7f800000))
@@ -66,7 +67,10 @@ struct TcLayout {
   static constexpr int K_OFF = Q_OFF + Q_BYTES;            // two K stages
   static constexpr int V_OFF = K_OFF + 2 * KV_BYTES;         // two V stages
   static constexpr int P_OFF = V_OFF + 2 * KV_BYTES;
-  static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
+  // 8 rows x 128 bytes of 16-bit ones: the B operand of the row-sum MMA
+  // (stride 0 between its 8-row groups, so 16 rows read the same bytes)
+  static constexpr int ONES_OFF = P_OFF + 2 * P_BYTES;
+  static constexpr int BAR_OFF = ONES_OFF + 1024;
   // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2],
   // p_full, o_done, done
   static constexpr int NBARS = 16;
@@ -76,6 +80,23 @@ struct TcLayout {
 
 enum : int { kBarQ = 0, kBarKFull = 1, kBarKEmpty = 3, kBarVFull = 5, kBarVEmpty = 7,
              kBarSFull = 9, kBarSFree = 11, kBarPFull = 13, kBarODone = 14, kBarDone = 15 };
+
+// max of three floats (one instruction)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (a0, a1) * s + t for a pair, one packed f32x2 instruction
+__device__ __forceinline__ void fma2(float a0, float a1, float s, float t, float& d0, float& d1) {
+  uint64_t a, m, c, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(m) : "f"(s));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(c) : "f"(t));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(m), "l"(c));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
 
 // 2^x by the SFU's ex2.approx (inputs here are <= 8; -inf gives +0)
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -207,6 +228,8 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t idS = idesc_f16(kBf16, kTcRows, kTcKv, false, false);
   constexpr uint32_t idO = idesc_f16(kBf16, kTcRows, D, false, true);
+  constexpr uint32_t idL = idesc_f16(kBf16, kTcRows, 16, false, false);
+  const uint64_t ones = smem_desc_sw128(s0 + Ly::ONES_OFF, 16, 0);
   const uint32_t qa = s0 + Ly::Q_OFF, pa = s0 + Ly::P_OFF;
   auto issue_pv = [&](int t) -> bool {
     if (!mbar_wait_bounded(bar + 8u * kBarPFull, t & 1, abort_flag, kTcWaitCycles)) return false;
@@ -223,6 +246,8 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
       // 16 tokens per k-step, the second half of D at KV_HALF
       const uint64_t bd = smem_desc_sw128(vb + ks * 2048, Ly::KV_HALF, 1024);
       mma_f16_ss(tmem + kTcOCol, ad, bd, idO, (t > 0 || ks > 0) ? 1u : 0u);
+      // l += P x ones: the row sums of exactly the rounded weights multiplied
+      mma_f16_ss(tmem + kTcLCol, ad, ones, idL, (t > 0 || ks > 0) ? 1u : 0u);
     }
     mma_commit(bar + 8u * kBarODone);
     mma_commit(bar + 8u * (kBarVEmpty + (t & 1)));
@@ -312,6 +337,12 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
     tmem_alloc(s0 + Ly::MISC_OFF, kTcTmemCols);
     tmem_relinquish();
   }
+  if (threadIdx.x < 64) {          // 1024 bytes of ones (1.0 in either 16-bit type)
+    const uint32_t one2 = std::is_same<T, __nv_bfloat16>::value ? 0x3f803f80u : 0x3c003c00u;
+    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
+                 ::"r"(s0 + Ly::ONES_OFF + threadIdx.x * 16), "r"(one2) : "memory");
+  }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -340,7 +371,7 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
     const int R = B < kTcKv ? B : kTcKv;
     const int rshift = __ffs(R) - 1;
     const unsigned full_mask = (kTcKv / R) >= 32 ? 0xffffffffu : ((1u << (kTcKv / R)) - 1u);
-    float m_use = kNegInfT, l = 0.f;
+    float m_use = kNegInfT;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j & 1;
@@ -388,9 +419,9 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
           uint32_t v[32];
           tmem_ld32(sadr + ch * 32, v);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            mx0 = fmaxf(mx0, __uint_as_float(v[e]));
-            mx1 = fmaxf(mx1, __uint_as_float(v[e + 1]));
+          for (int e = 0; e < 32; e += 4) {
+            mx0 = fmax3(mx0, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
           }
         }
         mx = fmaxf(mx0, mx1) * sl2;       // the scale is positive: max commutes
@@ -414,16 +445,13 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
         alpha = exp2f(m_use - m_new);
         resc = true;
         m_use = m_new;
-        l *= alpha;
       }
       // pass 2: P = 2^(x - m_use) rounded to the input type, written chunk by
       // chunk to P buffer j&1 (row r; 16-byte chunk k holds tokens 8k..8k+7,
-      // 64 tokens per half); l sums the rounded weights the MMA multiplies,
-      // so the normalised weights sum to one
+      // 64 tokens per half). The row sums come from the MMA (P x ones).
       const bool live = m_use != kNegInfT;
       const float nm = -m_use;
       const uint32_t p_row = s0 + Ly::P_OFF + st * Ly::P_BYTES + r * 128;
-      float l0 = 0.f, l1 = 0.f;
 #pragma unroll 1
       for (int ch = 0; ch < kTcKv / 32; ++ch) {
         const uint32_t vm = fast ? 0xffffffffu : (live ? chunk_mask(ch) : 0u);
@@ -432,16 +460,15 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), sl2, nm));
-          float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), sl2, nm));
+          float x0, x1;
+          fma2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), sl2, nm, x0, x1);
+          float p0 = ex2_approx(x0);
+          float p1 = ex2_approx(x1);
           if (!fast) {
             p0 = ((vm >> e) & 1u) ? p0 : 0.f;
             p1 = ((vm >> (e + 1)) & 1u) ? p1 : 0.f;
           }
-          float q0r, q1r;
-          pk[e >> 1] = Pack2<T>::pack(p0, p1, q0r, q1r);
-          l0 += q0r;
-          l1 += q1r;
+          pk[e >> 1] = Pack2<T>::pack_out(p0, p1);
         }
         const uint32_t prow = p_row + (ch >> 1) * Ly::HALF_BYTES;
 #pragma unroll
@@ -453,7 +480,6 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
                          "r"(pk[4 * kk + 3]) : "memory");
         }
       }
-      l += l0 + l1;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar + 8u * (kBarSFree + st));
@@ -475,6 +501,8 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
           for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
           tmem_st32(tmem + lanes + kTcOCol + ch * 32, v);
         }
+        const uint32_t lv = tmem_ld1(tmem + lanes + kTcLCol);
+        tmem_st1(tmem + lanes + kTcLCol, __float_as_uint(__uint_as_float(lv) * alpha));
         tmem_wait_st();
       }
       // V rows that hold no token of this tile may contain anything (NaN
@@ -514,6 +542,7 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       const int count = rv ? (pos + a.partition) / a.partition : 0;
       const bool direct = rv && count == 1 && split == 0;
       const bool partial = rv && count > 1 && split < count;
+      const float l = __uint_as_float(tmem_ld1(tmem + lanes + kTcLCol));
       const float inv = l > 0.f ? 1.f / l : 0.f;
       T* out = reinterpret_cast<T*>(a.out);
       const int64_t slot = (t * Hq + head) * a.num_splits + split;
