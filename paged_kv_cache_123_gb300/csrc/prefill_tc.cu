@@ -1,6 +1,6 @@
 // Causal paged attention for long runs of new tokens (prefill chunks) on the
-// fifth-generation tensor cores: tcgen05.mma with operands in shared memory
-// and fp32 accumulators in tensor memory (TMEM).
+// fifth-generation tensor cores: tcgen05.mma with fp32 accumulators, scores
+// and softmax weights in tensor memory (TMEM).
 //
 // What is computed is the multi-query attention of prefill_mma.cu: new token
 // i of sequence s (n_s new tokens, L_s tokens in the pool including them)
@@ -11,22 +11,25 @@
 //
 // One CTA owns 128 rows — (new token, query head) pairs of one KV head,
 // query-major — and walks its causal KV range in tiles of 128 tokens:
-//   * a producer warp loads the CTA's Q tile once (3-D TMA straight from the
-//     [tokens][heads][D] query tensor) and each K/V tile by 3-D TMA boxes of
-//     one 64-column half of one block's rows (128-byte swizzle), two stages;
-//   * one thread of an MMA warp issues S = Q K^T (M = 128 rows, N = 128
-//     tokens, K = D) into one of two TMEM score buffers, and O += P V (M =
-//     128, N = D, K = 128 tokens; V read N-major straight from its token
-//     rows) into the TMEM output, each completing on an mbarrier
-//     (tcgen05.commit);
+//   * producer warps load the CTA's Q tile once (3-D TMA straight from the
+//     [tokens][heads][D] query tensor) and the K and V tiles into two
+//     separate three-stage rings by 3-D TMA boxes of one 64-column half of
+//     one block's rows (128-byte swizzle); a K stage is released as soon as
+//     S of its tile is computed, a V stage when P V is;
+//   * one thread of the MMA warp issues S = Q K^T (M = 128 rows, N = 128
+//     tokens, K = D; both operands in shared memory) into one of two TMEM
+//     score buffers, and O += P V (M = 128, N = D, K = 128 tokens) with P
+//     read from TMEM and V read N-major straight from its token rows; each
+//     completes on an mbarrier (tcgen05.commit);
 //   * four softmax warps own one row each per thread (TMEM lane = row): they
-//     read the scores with tcgen05.ld, apply the causal limit and the scale in
-//     the log2 domain, write P (16-bit, K-major, 128-byte swizzle) to shared
-//     memory for the next MMA, and rescale the TMEM output only when a row's
-//     running maximum grew by more than 2^8 (the exponentials stay below 256,
-//     and the final division uses the same reference), so most tiles skip
-//     the rescale.
-// S of tile j+1 is computed while the softmax warps work on tile j.
+//     read the scores with tcgen05.ld, apply the causal limit and the scale
+//     in the log2 domain, and write P (16-bit) to one of two TMEM P buffers
+//     with tcgen05.st. The output in TMEM is rescaled only when a row's
+//     running maximum grew by more than 2^8 (the weights stay below 256,
+//     and the final division uses the same reference).
+// Keeping S and P out of shared memory leaves its bandwidth to the K/V
+// operands and their TMA loads. S of tile j+1 is computed while the softmax
+// warps work on tile j.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -42,14 +45,16 @@ namespace {
 
 constexpr int kTcRows = 128;              // query rows per CTA (MMA M)
 constexpr int kTcKv = 128;                // KV tokens per tile
+constexpr int kTcStages = 3;              // K and V ring depth
 constexpr int kTcSoftmaxWarps = 4;
-constexpr int kTcKProducerWarp = 4;     // Q and K tiles
+constexpr int kTcKProducerWarp = 4;       // Q and K tiles
 constexpr int kTcMmaWarp = 5;
-constexpr int kTcVProducerWarp = 6;     // V tiles
+constexpr int kTcVProducerWarp = 6;       // V tiles
 constexpr int kTcThreads = 7 * 32;
-constexpr uint32_t kTcTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256, 256+D)
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), P0 [384,448), P1 [448,512)
+constexpr uint32_t kTcTmemCols = 512;
 constexpr uint32_t kTcOCol = 256;
-constexpr uint32_t kTcLCol = 384;          // row sums of P: P x ones, 16 columns
+constexpr uint32_t kTcPCol = 384;
 constexpr long long kTcWaitCycles = 4000000000LL;
 constexpr float kTcRescaleLog2 = 8.f;
 #define kNegInfT (-__int_as_float(0x7f800000))
@@ -61,25 +66,21 @@ struct TcLayout {
   static constexpr int Q_BYTES = HALVES * HALF_BYTES;
   static constexpr int KV_HALF = kTcKv * 128;
   static constexpr int KV_BYTES = HALVES * KV_HALF;         // one K (or V) tile
-  static constexpr int P_BYTES = 2 * HALF_BYTES;            // 128 rows x 128 tokens
-  // two P buffers: P_j is written while P V of tile j-1 may still run
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + Q_BYTES;            // two K stages
-  static constexpr int V_OFF = K_OFF + 2 * KV_BYTES;         // two V stages
-  static constexpr int P_OFF = V_OFF + 2 * KV_BYTES;
-  // 8 rows x 128 bytes of 16-bit ones: the B operand of the row-sum MMA
-  // (stride 0 between its 8-row groups, so 16 rows read the same bytes)
-  static constexpr int ONES_OFF = P_OFF + 2 * P_BYTES;
-  static constexpr int BAR_OFF = ONES_OFF + 1024;
-  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2],
+  static constexpr int K_OFF = Q_OFF + Q_BYTES;
+  static constexpr int V_OFF = K_OFF + kTcStages * KV_BYTES;
+  static constexpr int BAR_OFF = V_OFF + kTcStages * KV_BYTES;
+  // q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], s_free[2],
   // p_full, o_done, done
-  static constexpr int NBARS = 16;
+  static constexpr int NBARS = 20;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;     // tmem base, abort flag
   static constexpr int SMEM = MISC_OFF + 32 + 1024;        // + alignment slack
 };
 
-enum : int { kBarQ = 0, kBarKFull = 1, kBarKEmpty = 3, kBarVFull = 5, kBarVEmpty = 7,
-             kBarSFull = 9, kBarSFree = 11, kBarPFull = 13, kBarODone = 14, kBarDone = 15 };
+enum : int {
+  kBarQ = 0, kBarKFull = 1, kBarKEmpty = 4, kBarVFull = 7, kBarVEmpty = 10,
+  kBarSFull = 13, kBarSFree = 15, kBarPFull = 17, kBarODone = 18, kBarDone = 19
+};
 
 // max of three floats (one instruction)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -105,16 +106,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// two fp32 weights packed to the 16-bit input type (round to nearest), and
+// the rounded values
 template <typename T>
 struct Pack2;
 template <>
 struct Pack2<__nv_bfloat16> {
   __device__ __forceinline__ static uint32_t pack(float a, float b, float& ra, float& rb) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    const float2 f = __bfloat1622float2(h);
-    ra = f.x;
-    rb = f.y;
-    return *reinterpret_cast<uint32_t*>(&h);
+    const uint32_t u = *reinterpret_cast<uint32_t*>(&h);
+    ra = __uint_as_float(u << 16);
+    rb = __uint_as_float(u & 0xffff0000u);
+    return u;
   }
   __device__ __forceinline__ static uint32_t pack_out(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -136,9 +139,8 @@ struct Pack2<__half> {
   }
 };
 
-// Lanes of the producer warp that hold a block piece of tile [ts, te):
-// piece p = R = min(B, 128) rows of one block; bit p set when its table
-// entry names a block of the pool.
+// Block pieces of tile [ts, te): piece p = R = min(B, 128) rows of one
+// block; bit p set when its table entry names a block of the pool.
 __device__ __forceinline__ unsigned tc_piece_mask(const MultiQueryArgs& a, const int32_t* trow,
                                                   int ts, int te, int lane, int64_t* blk_out) {
   const int B = a.block_size;
@@ -155,9 +157,8 @@ __device__ __forceinline__ unsigned tc_piece_mask(const MultiQueryArgs& a, const
 }
 
 // Producer warp for one operand (K, with the Q tile first, or V): the tiles
-// of [kv_lo, kv_end) into that operand's two-stage ring. Lane p loads piece
-// p of a tile, both 64-column halves. K stages are released when S of the
-// tile has been computed, V stages when P V has: K runs ahead of V.
+// of [kv_lo, kv_end) into that operand's ring. Lane p loads piece p of a
+// tile, both 64-column halves.
 template <int D, bool IS_V>
 __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
                            const CUtensorMap* tm, const int32_t* trow, int kvh, int q_tok,
@@ -182,7 +183,7 @@ __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
   const int R = B < kTcKv ? B : kTcKv;
   int issued = 0;
   for (int i = 0; i < ntiles; ++i) {
-    const int st = i & 1;
+    const int st = i % kTcStages;
     const int ts = kv_lo + i * kTcKv;
     const int te = min(kv_end, ts + kTcKv);
     int64_t blk;
@@ -192,8 +193,8 @@ __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
       latch(a.err, PA_ERR_OUT_OF_RANGE);
     int ok = 1;
     if (lane == 0) {
-      if (i >= 2)
-        ok = mbar_wait_bounded(bar + 8u * (empty + st), ((i >> 1) - 1) & 1, abort_flag,
+      if (i >= kTcStages)
+        ok = mbar_wait_bounded(bar + 8u * (empty + st), ((i / kTcStages) - 1) & 1, abort_flag,
                                kTcWaitCycles);
       if (ok)
         mbar_arrive_expect_tx(bar + 8u * (full + st),
@@ -214,13 +215,15 @@ __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
   // let this warp's copies land before the CTA can leave
   if (lane == 0) {
     if (!IS_V) mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
-    for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-      mbar_wait_bounded(bar + 8u * (full + (j & 1)), (j >> 1) & 1, abort_flag, kTcWaitCycles);
+    for (int j = issued > kTcStages ? issued - kTcStages : 0; j < issued; ++j)
+      mbar_wait_bounded(bar + 8u * (full + j % kTcStages), (j / kTcStages) & 1, abort_flag,
+                        kTcWaitCycles);
   }
 }
 
-// MMA issue (one thread): S_j = Q K_j^T into TMEM buffer j&1, then
-// O += P_{j-1} V_{j-1} once the softmax warps have written P_{j-1}.
+// MMA issue (one thread): S_j = Q K_j^T into TMEM score buffer j&1, then
+// O += P_{j-1} V_{j-1} (P from TMEM buffer (j-1)&1) once the softmax warps
+// have written P_{j-1}.
 template <typename T, int D>
 __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
                          volatile int* abort_flag) {
@@ -228,50 +231,46 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t idS = idesc_f16(kBf16, kTcRows, kTcKv, false, false);
   constexpr uint32_t idO = idesc_f16(kBf16, kTcRows, D, false, true);
-  constexpr uint32_t idL = idesc_f16(kBf16, kTcRows, 16, false, false);
-  const uint64_t ones = smem_desc_sw128(s0 + Ly::ONES_OFF, 16, 0);
-  const uint32_t qa = s0 + Ly::Q_OFF, pa = s0 + Ly::P_OFF;
+  const uint32_t qa = s0 + Ly::Q_OFF;
   auto issue_pv = [&](int t) -> bool {
+    const int vs = t % kTcStages;
     if (!mbar_wait_bounded(bar + 8u * kBarPFull, t & 1, abort_flag, kTcWaitCycles)) return false;
-    if (!mbar_wait_bounded(bar + 8u * (kBarVFull + (t & 1)), (t >> 1) & 1, abort_flag,
+    if (!mbar_wait_bounded(bar + 8u * (kBarVFull + vs), (t / kTcStages) & 1, abort_flag,
                            kTcWaitCycles))
       return false;
     tc_fence_after();
-    const uint32_t vb = s0 + Ly::V_OFF + (t & 1) * Ly::KV_BYTES;
-    const uint32_t pb = pa + (t & 1) * Ly::P_BYTES;
+    const uint32_t vb = s0 + Ly::V_OFF + vs * Ly::KV_BYTES;
+    const uint32_t pt = tmem + kTcPCol + (t & 1) * (kTcKv / 2);
 #pragma unroll
     for (int ks = 0; ks < kTcKv / 16; ++ks) {
-      const uint64_t ad = smem_desc_sw128(pb + (ks >> 2) * Ly::HALF_BYTES + (ks & 3) * 32, 16, 1024);
       // V tile: token rows of 64 head dims per 128-byte line (N-major);
       // 16 tokens per k-step, the second half of D at KV_HALF
       const uint64_t bd = smem_desc_sw128(vb + ks * 2048, Ly::KV_HALF, 1024);
-      mma_f16_ss(tmem + kTcOCol, ad, bd, idO, (t > 0 || ks > 0) ? 1u : 0u);
-      // l += P x ones: the row sums of exactly the rounded weights multiplied
-      mma_f16_ss(tmem + kTcLCol, ad, ones, idL, (t > 0 || ks > 0) ? 1u : 0u);
+      mma_f16_ts(tmem + kTcOCol, pt + ks * 8, bd, idO, (t > 0 || ks > 0) ? 1u : 0u);
     }
     mma_commit(bar + 8u * kBarODone);
-    mma_commit(bar + 8u * (kBarVEmpty + (t & 1)));
+    mma_commit(bar + 8u * (kBarVEmpty + vs));
     return true;
   };
   bool ok = mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
   for (int j = 0; ok && j < ntiles; ++j) {
-    const int st = j & 1;
-    ok = mbar_wait_bounded(bar + 8u * (kBarKFull + st), (j >> 1) & 1, abort_flag,
+    const int sb = j & 1, ks_ = j % kTcStages;
+    ok = mbar_wait_bounded(bar + 8u * (kBarKFull + ks_), (j / kTcStages) & 1, abort_flag,
                            kTcWaitCycles);
     if (ok && j >= 2)
-      ok = mbar_wait_bounded(bar + 8u * (kBarSFree + st), ((j >> 1) - 1) & 1, abort_flag,
+      ok = mbar_wait_bounded(bar + 8u * (kBarSFree + sb), ((j >> 1) - 1) & 1, abort_flag,
                              kTcWaitCycles);
     if (!ok) break;
     tc_fence_after();
-    const uint32_t kb = s0 + Ly::K_OFF + st * Ly::KV_BYTES;
+    const uint32_t kb = s0 + Ly::K_OFF + ks_ * Ly::KV_BYTES;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       const uint64_t ad = smem_desc_sw128(qa + (ks >> 2) * Ly::HALF_BYTES + (ks & 3) * 32, 16, 1024);
       const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * Ly::KV_HALF + (ks & 3) * 32, 16, 1024);
-      mma_f16_ss(tmem + st * kTcKv, ad, bd, idS, ks > 0 ? 1u : 0u);
+      mma_f16_ss(tmem + sb * kTcKv, ad, bd, idS, ks > 0 ? 1u : 0u);
     }
-    mma_commit(bar + 8u * (kBarSFull + st));
-    mma_commit(bar + 8u * (kBarKEmpty + st));
+    mma_commit(bar + 8u * (kBarSFull + sb));
+    mma_commit(bar + 8u * (kBarKEmpty + ks_));
     if (j >= 1) ok = issue_pv(j - 1);
   }
   if (ok && ntiles > 0) issue_pv(ntiles - 1);
@@ -319,11 +318,13 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
 
   if (threadIdx.x == 0) {
     mbar_init(bar + 8u * kBarQ, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kTcStages; ++i) {
       mbar_init(bar + 8u * (kBarKFull + i), 1);
       mbar_init(bar + 8u * (kBarKEmpty + i), 1);
       mbar_init(bar + 8u * (kBarVFull + i), 1);
       mbar_init(bar + 8u * (kBarVEmpty + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar + 8u * (kBarSFull + i), 1);
       mbar_init(bar + 8u * (kBarSFree + i), kTcSoftmaxWarps);
     }
@@ -337,12 +338,6 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
     tmem_alloc(s0 + Ly::MISC_OFF, kTcTmemCols);
     tmem_relinquish();
   }
-  if (threadIdx.x < 64) {          // 1024 bytes of ones (1.0 in either 16-bit type)
-    const uint32_t one2 = std::is_same<T, __nv_bfloat16>::value ? 0x3f803f80u : 0x3c003c00u;
-    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
-                 ::"r"(s0 + Ly::ONES_OFF + threadIdx.x * 16), "r"(one2) : "memory");
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -371,17 +366,17 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
     const int R = B < kTcKv ? B : kTcKv;
     const int rshift = __ffs(R) - 1;
     const unsigned full_mask = (kTcKv / R) >= 32 ? 0xffffffffu : ((1u << (kTcKv / R)) - 1u);
-    float m_use = kNegInfT;
+    float m_use = kNegInfT, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j & 1;
+      const int sb = j & 1;
       const int ts = kv_lo + j * kTcKv;
       const int te = min(kv_end, ts + kTcKv);
       // which block pieces of the tile exist (the producers load exactly
       // these); the table entries are read by this warp itself
       int64_t blk_unused;
       const unsigned pm = tc_piece_mask(a, trow, ts, te, lane, &blk_unused);
-      ok = mbar_wait_bounded(bar + 8u * (kBarSFull + st), (j >> 1) & 1, abort_flag,
+      ok = mbar_wait_bounded(bar + 8u * (kBarSFull + sb), (j >> 1) & 1, abort_flag,
                              kTcWaitCycles);
       // tcgen05.ld / st are warp-collective: the whole warp goes on or stops
       ok = __all_sync(0xffffffffu, ok);
@@ -409,7 +404,7 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       // interior tiles (every column valid for every row of the warp) skip
       // the per-column masks
       const bool fast = __all_sync(0xffffffffu, whole && lim >= kTcKv - 1) && sl2 > 0.f;
-      const uint32_t sadr = tmem + lanes + st * kTcKv;
+      const uint32_t sadr = tmem + lanes + sb * kTcKv;
       // pass 1: row maximum of the valid scaled scores
       float mx = kNegInfT;
       if (fast) {
@@ -445,13 +440,16 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
         alpha = exp2f(m_use - m_new);
         resc = true;
         m_use = m_new;
+        l *= alpha;
       }
-      // pass 2: P = 2^(x - m_use) rounded to the input type, written chunk by
-      // chunk to P buffer j&1 (row r; 16-byte chunk k holds tokens 8k..8k+7,
-      // 64 tokens per half). The row sums come from the MMA (P x ones).
+      // pass 2: P = 2^(x - m_use) rounded to the input type, 16 columns of
+      // packed pairs per 32 scores, into TMEM P buffer j&1 (its previous
+      // reader, P V of tile j-2, completed before S of tile j did); l sums
+      // the rounded weights the MMA multiplies
       const bool live = m_use != kNegInfT;
       const float nm = -m_use;
-      const uint32_t p_row = s0 + Ly::P_OFF + st * Ly::P_BYTES + r * 128;
+      const uint32_t padr = tmem + lanes + kTcPCol + sb * (kTcKv / 2);
+      float l0 = 0.f, l1 = 0.f;
 #pragma unroll 1
       for (int ch = 0; ch < kTcKv / 32; ++ch) {
         const uint32_t vm = fast ? 0xffffffffu : (live ? chunk_mask(ch) : 0u);
@@ -468,21 +466,18 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
             p0 = ((vm >> e) & 1u) ? p0 : 0.f;
             p1 = ((vm >> (e + 1)) & 1u) ? p1 : 0.f;
           }
-          pk[e >> 1] = Pack2<T>::pack_out(p0, p1);
+          float q0r, q1r;
+          pk[e >> 1] = Pack2<T>::pack(p0, p1, q0r, q1r);
+          l0 += q0r;
+          l1 += q1r;
         }
-        const uint32_t prow = p_row + (ch >> 1) * Ly::HALF_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const int k = (ch & 1) * 4 + kk;           // chunk inside the 64-token half
-          const uint32_t adr = prow + ((k ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                       ::"r"(adr), "r"(pk[4 * kk]), "r"(pk[4 * kk + 1]), "r"(pk[4 * kk + 2]),
-                         "r"(pk[4 * kk + 3]) : "memory");
-        }
+        tmem_st16(padr + ch * 16, pk);
       }
+      l += l0 + l1;
+      // the scores of this buffer have been read: S of tile j+2 may land
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar + 8u * (kBarSFree + st));
+      if (lane == 0) mbar_arrive(bar + 8u * (kBarSFree + sb));
       // the output is rescaled only when some row of the warp needs it; P V
       // of tile j-1 must have completed first (P V of tile j-2 completed
       // before S of tile j, which this thread has seen)
@@ -493,7 +488,7 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
           if (!ok) break;
           tc_fence_after();
         }
-#pragma unroll
+#pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t v[32];
           tmem_ld32(tmem + lanes + kTcOCol + ch * 32, v);
@@ -501,22 +496,20 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
           for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
           tmem_st32(tmem + lanes + kTcOCol + ch * 32, v);
         }
-        const uint32_t lv = tmem_ld1(tmem + lanes + kTcLCol);
-        tmem_st1(tmem + lanes + kTcLCol, __float_as_uint(__uint_as_float(lv) * alpha));
-        tmem_wait_st();
       }
       // V rows that hold no token of this tile may contain anything (NaN
       // included) and 0 * NaN is NaN inside the MMA: clear them (row r)
       if (!whole) {
         // the V tile must have landed before its rows are cleared (its stage
         // is not refilled before P V of this tile, so the phase is current)
-        ok = mbar_wait_bounded(bar + 8u * (kBarVFull + st), (j >> 1) & 1, abort_flag,
+        const int vs = j % kTcStages;
+        ok = mbar_wait_bounded(bar + 8u * (kBarVFull + vs), (j / kTcStages) & 1, abort_flag,
                                kTcWaitCycles);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const bool row_ok = r < te - ts && ((pm >> (r >> rshift)) & 1u);
         if (!row_ok) {
-          const uint32_t vrow = s0 + Ly::V_OFF + st * Ly::KV_BYTES + r * 128;
+          const uint32_t vrow = s0 + Ly::V_OFF + vs * Ly::KV_BYTES + r * 128;
 #pragma unroll
           for (int h = 0; h < Ly::HALVES; ++h)
 #pragma unroll
@@ -524,8 +517,9 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
               asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
                            ::"r"(vrow + h * Ly::KV_HALF + k * 16), "r"(0u) : "memory");
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar + 8u * kBarPFull);
@@ -542,24 +536,27 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       const int count = rv ? (pos + a.partition) / a.partition : 0;
       const bool direct = rv && count == 1 && split == 0;
       const bool partial = rv && count > 1 && split < count;
-      const float l = __uint_as_float(tmem_ld1(tmem + lanes + kTcLCol));
       const float inv = l > 0.f ? 1.f / l : 0.f;
       T* out = reinterpret_cast<T*>(a.out);
       const int64_t slot = (t * Hq + head) * a.num_splits + split;
-#pragma unroll
+#pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t v[32];
         tmem_ld32(tmem + lanes + kTcOCol + ch * 32, v);
         if (direct) {
-          uint32_t* op = reinterpret_cast<uint32_t*>(out + (t * Hq + head) * D + ch * 32);
+          uint4* op = reinterpret_cast<uint4*>(out + (t * Hq + head) * D + ch * 32);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
-            w.x = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
-            w.y = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
-            w.z = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
-            w.w = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
-            reinterpret_cast<uint4*>(op)[q] = w;
+            w.x = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 0]) * inv,
+                                     __uint_as_float(v[8 * q + 1]) * inv);
+            w.y = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 2]) * inv,
+                                     __uint_as_float(v[8 * q + 3]) * inv);
+            w.z = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 4]) * inv,
+                                     __uint_as_float(v[8 * q + 5]) * inv);
+            w.w = Pack2<T>::pack_out(__uint_as_float(v[8 * q + 6]) * inv,
+                                     __uint_as_float(v[8 * q + 7]) * inv);
+            op[q] = w;
           }
         } else if (partial) {
           float4* acc = reinterpret_cast<float4*>(a.ws_acc + slot * D + ch * 32);
