@@ -21,12 +21,14 @@
 //     score buffers, and O += P V (M = 128, N = D, K = 128 tokens) with P
 //     read from TMEM and V read N-major straight from its token rows; each
 //     completes on an mbarrier (tcgen05.commit);
-//   * four softmax warps own one row each per thread (TMEM lane = row): they
+//   * eight softmax warps, two warpgroups, own half a row each per thread
+//     (TMEM lane = row; warpgroup h takes score columns 64h .. 64h+63): they
 //     read the scores with tcgen05.ld, apply the causal limit and the scale
-//     in the log2 domain, and write P (16-bit) to one of two TMEM P buffers
-//     with tcgen05.st. The output in TMEM is rescaled only when a row's
-//     running maximum grew by more than 2^8 (the weights stay below 256,
-//     and the final division uses the same reference).
+//     in the log2 domain, exchange the two half-row maxima through shared
+//     memory, and write P (16-bit) to one of two TMEM P buffers with
+//     tcgen05.st. The output in TMEM is rescaled only when a row's running
+//     maximum grew by more than 2^8 (the weights stay below 256, and the
+//     final division uses the same reference).
 // Keeping S and P out of shared memory leaves its bandwidth to the K/V
 // operands and their TMA loads. S of tile j+1 is computed while the softmax
 // warps work on tile j.
@@ -46,11 +48,12 @@ namespace {
 constexpr int kTcRows = 128;              // query rows per CTA (MMA M)
 constexpr int kTcKv = 128;                // KV tokens per tile
 constexpr int kTcStages = 3;              // K and V ring depth
-constexpr int kTcSoftmaxWarps = 4;
-constexpr int kTcKProducerWarp = 4;       // Q and K tiles
-constexpr int kTcMmaWarp = 5;
-constexpr int kTcVProducerWarp = 6;       // V tiles
-constexpr int kTcThreads = 7 * 32;
+constexpr int kTcSoftmaxWarps = 8;        // two warpgroups: columns 0-63, 64-127
+constexpr int kTcKProducerWarp = 8;       // Q and K tiles
+constexpr int kTcMmaWarp = 9;
+constexpr int kTcVProducerWarp = 10;      // V tiles
+constexpr int kTcThreads = 11 * 32;
+constexpr int kTcCols = kTcKv / 2;        // score columns per softmax thread
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,384), P0 [384,448), P1 [448,512)
 constexpr uint32_t kTcTmemCols = 512;
 constexpr uint32_t kTcOCol = 256;
@@ -74,7 +77,10 @@ struct TcLayout {
   // p_full, o_done, done
   static constexpr int NBARS = 20;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;     // tmem base, abort flag
-  static constexpr int SMEM = MISC_OFF + 32 + 1024;        // + alignment slack
+  // row maxima and row sums exchanged between the two softmax warpgroups
+  static constexpr int XCH_OFF = MISC_OFF + 32;            // float [2][128]
+  static constexpr int SMEM = XCH_OFF + 2 * kTcRows * 4 + 1024;   // + alignment slack
+  static_assert(SMEM <= 232448, "over the shared memory of one CTA");
 };
 
 enum : int {
@@ -97,6 +103,17 @@ __device__ __forceinline__ void fma2(float a0, float a1, float s, float t, float
   asm("mov.b64 %0, {%1, %1};" : "=l"(c) : "f"(t));
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(m), "l"(c));
   asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+
+// Barrier 1 over the eight softmax warps (256 threads) that also returns
+// whether every one of them passed `ok`, so they leave their loop together.
+__device__ __forceinline__ bool softmax_bar_and(bool ok) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
+      " barrier.cta.red.and.pred po, 1, 256, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(out) : "r"((uint32_t)ok) : "memory");
+  return out != 0;
 }
 
 // 2^x by the SFU's ex2.approx (inputs here are <= 8; -inf gives +0)
@@ -354,83 +371,107 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
     if (lane == 0) tc_issue<T, D>(ntiles, s0, bar, tmem, abort_flag);
     __syncwarp();
   } else {
-    // ---- softmax warps: thread = row (TMEM lane) r
-    const int r = warp * 32 + lane;
+    // ---- softmax warps: thread = (half hf, row r); TMEM lane r, score
+    // columns 64 hf .. 64 hf + 63
+    const int hf = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const int rr = r0 + r;
     const int i = rr / G;
     const bool rv = i < n;
     const int pos = rv ? L - n + i : -1;            // causal limit of this row
     const float sl2 = a.scale * kLog2e;
-    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+    float* xch = reinterpret_cast<float*>(smem + Ly::XCH_OFF);   // [2 halves][128]
     const int B = a.block_size;
     const int R = B < kTcKv ? B : kTcKv;
     const int rshift = __ffs(R) - 1;
-    const unsigned full_mask = (kTcKv / R) >= 32 ? 0xffffffffu : ((1u << (kTcKv / R)) - 1u);
+    const int npieces = kTcKv / R;
+    const unsigned full_mask = npieces >= 32 ? 0xffffffffu : ((1u << npieces) - 1u);
+    // table entry of this lane's block piece of tile t (-1: none), read one
+    // tile ahead so its latency hides behind the current tile
+    auto piece_entry = [&](int t) -> int {
+      const int ts = kv_lo + t * kTcKv;
+      const int tok = ts + lane * R;
+      if (lane < npieces && tok < min(kv_end, ts + kTcKv))
+        return trow[tok >> (__ffs(B) - 1)];
+      return -1;
+    };
+    int ent_next = piece_entry(0);
     float m_use = kNegInfT, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
       const int ts = kv_lo + j * kTcKv;
       const int te = min(kv_end, ts + kTcKv);
-      // which block pieces of the tile exist (the producers load exactly
-      // these); the table entries are read by this warp itself
-      int64_t blk_unused;
-      const unsigned pm = tc_piece_mask(a, trow, ts, te, lane, &blk_unused);
-      ok = mbar_wait_bounded(bar + 8u * (kBarSFull + sb), (j >> 1) & 1, abort_flag,
-                             kTcWaitCycles);
+      const int ent = ent_next;
+      if (j + 1 < ntiles) ent_next = piece_entry(j + 1);
+      // block pieces of the tile that exist (the producers load exactly these)
+      const unsigned pm = __ballot_sync(0xffffffffu, ent >= 0 && ent < a.num_blocks);
+      if (ok)
+        ok = mbar_wait_bounded(bar + 8u * (kBarSFull + sb), (j >> 1) & 1, abort_flag,
+                               kTcWaitCycles);
       // tcgen05.ld / st are warp-collective: the whole warp goes on or stops
       ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
       tc_fence_after();
       const bool whole = (pm == full_mask) && (te - ts == kTcKv);
-      const int lim = min(pos, te - 1) - ts;        // last column this row may use
-      // valid columns of 32-column chunk ch: causal / length limit and loaded
-      // pieces
+      const int lim = min(pos, te - 1) - ts - hf * kTcCols;   // last own column usable
+      // valid own columns of 32-column chunk ch: causal / length limit and
+      // loaded pieces
       auto chunk_mask = [&](int ch) -> uint32_t {
         const int c0 = ch * 32;
         uint32_t m = lim < c0 ? 0u : (lim >= c0 + 31 ? 0xffffffffu : ((2u << (lim - c0)) - 1u));
         if (!whole) {
+          const int g0 = hf * kTcCols + c0;         // tile column of bit 0
           uint32_t pmask = 0;
           if (R >= 32) {
-            pmask = ((pm >> (c0 >> rshift)) & 1u) ? 0xffffffffu : 0u;
+            pmask = ((pm >> (g0 >> rshift)) & 1u) ? 0xffffffffu : 0u;
           } else {
             for (int k = 0; k < 32 / R; ++k)
-              if ((pm >> ((c0 >> rshift) + k)) & 1u) pmask |= ((1u << R) - 1u) << (k * R);
+              if ((pm >> ((g0 >> rshift) + k)) & 1u) pmask |= ((1u << R) - 1u) << (k * R);
           }
           m &= pmask;
         }
         return m;
       };
-      // interior tiles (every column valid for every row of the warp) skip
-      // the per-column masks
-      const bool fast = __all_sync(0xffffffffu, whole && lim >= kTcKv - 1) && sl2 > 0.f;
-      const uint32_t sadr = tmem + lanes + sb * kTcKv;
-      // pass 1: row maximum of the valid scaled scores
+      // interior tiles (every own column valid for every row of the warp)
+      // skip the per-column masks
+      const bool fast = __all_sync(0xffffffffu, whole && lim >= kTcCols - 1) && sl2 > 0.f;
+      const uint32_t sadr = tmem + lanes + sb * kTcKv + hf * kTcCols;
+      // pass 1: maximum of the valid scaled scores of this half row
       float mx = kNegInfT;
-      if (fast) {
-        float mx0 = kNegInfT, mx1 = kNegInfT;
+      if (ok) {
+        if (fast) {
+          float mx0 = kNegInfT, mx1 = kNegInfT;
 #pragma unroll 1
-        for (int ch = 0; ch < kTcKv / 32; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(sadr + ch * 32, v);
+          for (int ch = 0; ch < kTcCols / 32; ++ch) {
+            uint32_t v[32];
+            tmem_ld32(sadr + ch * 32, v);
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            mx0 = fmax3(mx0, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-            mx1 = fmax3(mx1, __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            for (int e = 0; e < 32; e += 4) {
+              mx0 = fmax3(mx0, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+              mx1 = fmax3(mx1, __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            }
+          }
+          mx = fmaxf(mx0, mx1) * sl2;       // the scale is positive: max commutes
+        } else {
+#pragma unroll 1
+          for (int ch = 0; ch < kTcCols / 32; ++ch) {
+            const uint32_t m = chunk_mask(ch);
+            uint32_t v[32];
+            tmem_ld32(sadr + ch * 32, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              mx = fmaxf(mx, ((m >> e) & 1u) ? __uint_as_float(v[e]) * sl2 : kNegInfT);
           }
         }
-        mx = fmaxf(mx0, mx1) * sl2;       // the scale is positive: max commutes
-      } else {
-#pragma unroll 1
-        for (int ch = 0; ch < kTcKv / 32; ++ch) {
-          const uint32_t m = chunk_mask(ch);
-          uint32_t v[32];
-          tmem_ld32(sadr + ch * 32, v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            mx = fmaxf(mx, ((m >> e) & 1u) ? __uint_as_float(v[e]) * sl2 : kNegInfT);
-        }
       }
+      // the two halves of the row meet: exchange the maxima; the second
+      // barrier keeps the next tile's write behind this read
+      xch[hf * kTcRows + r] = mx;
+      ok = softmax_bar_and(ok);           // both warpgroups, all 256 threads
+      if (!ok) break;
+      mx = fmaxf(mx, xch[(hf ^ 1) * kTcRows + r]);
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       const float m_new = fmaxf(m_use, mx);
       float alpha = 1.f;
       bool resc = false;
@@ -448,10 +489,10 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       // the rounded weights the MMA multiplies
       const bool live = m_use != kNegInfT;
       const float nm = -m_use;
-      const uint32_t padr = tmem + lanes + kTcPCol + sb * (kTcKv / 2);
+      const uint32_t padr = tmem + lanes + kTcPCol + sb * (kTcKv / 2) + hf * (kTcCols / 2);
       float l0 = 0.f, l1 = 0.f;
 #pragma unroll 1
-      for (int ch = 0; ch < kTcKv / 32; ++ch) {
+      for (int ch = 0; ch < kTcCols / 32; ++ch) {
         const uint32_t vm = fast ? 0xffffffffu : (live ? chunk_mask(ch) : 0u);
         uint32_t v[32];
         tmem_ld32(sadr + ch * 32, v);
@@ -478,44 +519,43 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar + 8u * (kBarSFree + sb));
-      // the output is rescaled only when some row of the warp needs it; P V
-      // of tile j-1 must have completed first (P V of tile j-2 completed
-      // before S of tile j, which this thread has seen)
+      // the output is rescaled only when some row of the warp needs it (the
+      // other half row takes the same decision); P V of tile j-1 must have
+      // completed first (P V of tile j-2 completed before S of tile j, which
+      // this thread has seen)
       if (__any_sync(0xffffffffu, resc)) {
-        if (j >= 1) {
+        if (j >= 1)
           ok = mbar_wait_bounded(bar + 8u * kBarODone, (j - 1) & 1, abort_flag, kTcWaitCycles);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          tc_fence_after();
-        }
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+        if (ok) {
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lanes + kTcOCol + ch * 32, v);
+          for (int ch = 0; ch < D / 64; ++ch) {
+            const uint32_t oadr = tmem + lanes + kTcOCol + hf * (D / 2) + ch * 32;
+            uint32_t v[32];
+            tmem_ld32(oadr, v);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st32(tmem + lanes + kTcOCol + ch * 32, v);
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st32(oadr, v);
+          }
         }
       }
       // V rows that hold no token of this tile may contain anything (NaN
-      // included) and 0 * NaN is NaN inside the MMA: clear them (row r)
-      if (!whole) {
+      // included) and 0 * NaN is NaN inside the MMA: clear them (row r, the
+      // 64-column half hf of the head dim)
+      if (!whole && ok && hf < Ly::HALVES) {
         // the V tile must have landed before its rows are cleared (its stage
         // is not refilled before P V of this tile, so the phase is current)
         const int vs = j % kTcStages;
         ok = mbar_wait_bounded(bar + 8u * (kBarVFull + vs), (j / kTcStages) & 1, abort_flag,
                                kTcWaitCycles);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
         const bool row_ok = r < te - ts && ((pm >> (r >> rshift)) & 1u);
-        if (!row_ok) {
-          const uint32_t vrow = s0 + Ly::V_OFF + vs * Ly::KV_BYTES + r * 128;
+        if (ok && !row_ok) {
+          const uint32_t vrow = s0 + Ly::V_OFF + vs * Ly::KV_BYTES + hf * Ly::KV_HALF + r * 128;
 #pragma unroll
-          for (int h = 0; h < Ly::HALVES; ++h)
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
-                           ::"r"(vrow + h * Ly::KV_HALF + k * 16), "r"(0u) : "memory");
+          for (int k = 0; k < 8; ++k)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
+                         ::"r"(vrow + k * 16), "r"(0u) : "memory");
         }
         fence_proxy_async_smem();
       }
@@ -529,8 +569,13 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       ok = mbar_wait_bounded(bar + 8u * kBarDone, 0, abort_flag, kTcWaitCycles);
       tc_fence_after();
     }
-    ok = __all_sync(0xffffffffu, ok);
+    // the two half-row sums meet
+    float* lsum = xch;                              // [2 halves][128], tiles done
+    ok = softmax_bar_and(ok);
+    if (ok) lsum[hf * kTcRows + r] = l;
+    ok = softmax_bar_and(ok);
     if (ok) {
+      l += lsum[(hf ^ 1) * kTcRows + r];
       const int64_t t = q0 + i;
       const int head = kvh * G + rr % G;
       const int count = rv ? (pos + a.partition) / a.partition : 0;
@@ -540,11 +585,12 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       T* out = reinterpret_cast<T*>(a.out);
       const int64_t slot = (t * Hq + head) * a.num_splits + split;
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = 0; ch < D / 64; ++ch) {
+        const int c0 = hf * (D / 2) + ch * 32;      // output columns c0 .. c0+31
         uint32_t v[32];
-        tmem_ld32(tmem + lanes + kTcOCol + ch * 32, v);
+        tmem_ld32(tmem + lanes + kTcOCol + c0, v);
         if (direct) {
-          uint4* op = reinterpret_cast<uint4*>(out + (t * Hq + head) * D + ch * 32);
+          uint4* op = reinterpret_cast<uint4*>(out + (t * Hq + head) * D + c0);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
@@ -559,14 +605,14 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
             op[q] = w;
           }
         } else if (partial) {
-          float4* acc = reinterpret_cast<float4*>(a.ws_acc + slot * D + ch * 32);
+          float4* acc = reinterpret_cast<float4*>(a.ws_acc + slot * D + c0);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             acc[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                  __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
         }
       }
-      if (partial) {
+      if (partial && hf == 0) {
         a.ws_ml[2 * slot] = m_use;
         a.ws_ml[2 * slot + 1] = l;
       }
