@@ -437,32 +437,29 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       // skip the per-column masks
       const bool fast = __all_sync(0xffffffffu, whole && lim >= kTcCols - 1) && sl2 > 0.f;
       const uint32_t sadr = tmem + lanes + sb * kTcKv + hf * kTcCols;
+      // this thread's 64 scores, one load; they stay in registers for both
+      // passes
+      uint32_t v[kTcCols];
+      if (ok) tmem_ld64(sadr, v);
+      uint32_t vmask[kTcCols / 32];
+#pragma unroll
+      for (int ch = 0; ch < kTcCols / 32; ++ch) vmask[ch] = fast ? 0xffffffffu : chunk_mask(ch);
       // pass 1: maximum of the valid scaled scores of this half row
       float mx = kNegInfT;
       if (ok) {
         if (fast) {
           float mx0 = kNegInfT, mx1 = kNegInfT;
-#pragma unroll 1
-          for (int ch = 0; ch < kTcCols / 32; ++ch) {
-            uint32_t v[32];
-            tmem_ld32(sadr + ch * 32, v);
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              mx0 = fmax3(mx0, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-              mx1 = fmax3(mx1, __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-            }
+          for (int e = 0; e < kTcCols; e += 4) {
+            mx0 = fmax3(mx0, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
           }
           mx = fmaxf(mx0, mx1) * sl2;       // the scale is positive: max commutes
         } else {
-#pragma unroll 1
-          for (int ch = 0; ch < kTcCols / 32; ++ch) {
-            const uint32_t m = chunk_mask(ch);
-            uint32_t v[32];
-            tmem_ld32(sadr + ch * 32, v);
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              mx = fmaxf(mx, ((m >> e) & 1u) ? __uint_as_float(v[e]) * sl2 : kNegInfT);
-          }
+          for (int e = 0; e < kTcCols; ++e)
+            mx = fmaxf(mx, ((vmask[e >> 5] >> (e & 31)) & 1u) ? __uint_as_float(v[e]) * sl2
+                                                               : kNegInfT);
         }
       }
       // the two halves of the row meet: exchange the maxima; the second
@@ -491,16 +488,15 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       const float nm = -m_use;
       const uint32_t padr = tmem + lanes + kTcPCol + sb * (kTcKv / 2) + hf * (kTcCols / 2);
       float l0 = 0.f, l1 = 0.f;
-#pragma unroll 1
+#pragma unroll
       for (int ch = 0; ch < kTcCols / 32; ++ch) {
-        const uint32_t vm = fast ? 0xffffffffu : (live ? chunk_mask(ch) : 0u);
-        uint32_t v[32];
-        tmem_ld32(sadr + ch * 32, v);
+        const uint32_t vm = live ? vmask[ch] : 0u;
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float x0, x1;
-          fma2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), sl2, nm, x0, x1);
+          fma2(__uint_as_float(v[ch * 32 + e]), __uint_as_float(v[ch * 32 + e + 1]), sl2, nm,
+               x0, x1);
           float p0 = ex2_approx(x0);
           float p1 = ex2_approx(x1);
           if (!fast) {
