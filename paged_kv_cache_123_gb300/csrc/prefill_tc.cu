@@ -441,6 +441,10 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       // passes
       uint32_t v[kTcCols];
       if (ok) tmem_ld64(sadr, v);
+      // the scores of this buffer have been read: S of tile j+2 may land
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + 8u * (kBarSFree + sb));
       uint32_t vmask[kTcCols / 32];
 #pragma unroll
       for (int ch = 0; ch < kTcCols / 32; ++ch) vmask[ch] = fast ? 0xffffffffu : chunk_mask(ch);
@@ -511,10 +515,6 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
         tmem_st16(padr + ch * 16, pk);
       }
       l += l0 + l1;
-      // the scores of this buffer have been read: S of tile j+2 may land
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar + 8u * (kBarSFree + sb));
       // the output is rescaled only when some row of the warp needs it (the
       // other half row takes the same decision); P V of tile j-1 must have
       // completed first (P V of tile j-2 completed before S of tile j, which
