@@ -37,6 +37,7 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode attn: KV-read GB/s vs HBM peak; seq-tokens/s at Llama-7B shape"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 ELT = {"f32": 4, "f16": 2, "bf16": 2}
 CSRC = os.path.join(ROOT, "paged_kv_cache_123_gb300", "csrc")
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
@@ -103,12 +104,20 @@ def profiled_traffic(config):
     return None
 
 
-def measured_peak():
+def measured_peak(key="hbm_gbs", fallback=None):
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            return float(json.load(f)["hbm_gbs"]), "measured"
+            return float(json.load(f)[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return (FALLBACK_HBM_GBS if fallback is None else fallback), "fallback"
+
+
+def attention_flops(ctx_lens, new_tokens, num_q_heads, head_size):
+    """Algorithmic flops of causal multi-query attention: new token i of a
+    sequence with c cached tokens sees c + i + 1 keys; 2 flops per
+    multiply-add of q.k and of p.v over the head dim."""
+    keys = sum((c + 1) * new_tokens + new_tokens * (new_tokens - 1) // 2 for c in ctx_lens)
+    return 4 * head_size * num_q_heads * keys
 
 
 class ClockSampler:
@@ -591,6 +600,19 @@ def ours_arm(args):
         return
     peak, peak_kind = measured_peak()
     achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
+    # runs of more than 64 (token, head) rows per KV head go to the tcgen05
+    # kernel: a dense contraction, judged against the tensor-core peak
+    tensor_bound = N * (cfg.num_q_heads // Hkv) > 64
+    if tensor_bound:
+        ctx_lens = [int(L) - N for L in lens.tolist()]
+        flops = attention_flops(ctx_lens, N, cfg.num_q_heads, D)
+        t_peak, t_kind = measured_peak("bf16_tflops", FALLBACK_BF16_TFLOPS)
+        roof = {"bound": "tensor", "kernel": kernel_name,
+                "achieved": round(flops / (attn_ms * 1e-3) / 1e12, 1), "peak": t_peak,
+                "peak_kind": f"bf16_tflops (burst) of {t_kind}", "unit": "TFLOP/s",
+                "frac": round(flops / (attn_ms * 1e-3) / 1e12 / t_peak, 4),
+                "traffic": None, "avg_launch_us": round(attn_ms * 1e3, 2),
+                "algorithmic_flops_per_launch": flops}
     step_s = ms_total * 1e-3 / args.steps
     value = world * kv_bytes / step_s / 1e9
     line = {
@@ -615,7 +637,7 @@ def ours_arm(args):
                   "KV read per step %.3f GB fits in twice L2: L2-warm" % (kv_bytes / 1e9),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
-        "roofline": {"bound": "hbm", "kernel": kernel_name,
+        "roofline": roof if tensor_bound else {"bound": "hbm", "kernel": kernel_name,
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(label),
