@@ -48,8 +48,10 @@ constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 // V with two token rows byte-interleaved per head dim — so the products run
 // in fp16 without a widened copy in shared memory. k_scale / v_scale are
 // the pools' scales (1 for 16-bit pools).
+// fp8 pools: half the shared memory per stage and a register budget for
+// three CTAs per SM, so more warps hide the conversion latency.
 template <typename T, int D, int G, bool KV8>
-__global__ void __launch_bounds__(kMmaThreads, 2)
+__global__ void __launch_bounds__(kMmaThreads, KV8 ? 3 : 2)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, float k_scale, float v_scale) {
   constexpr int HALVES = D / 64;                 // 128-byte lines per 16-bit token row
