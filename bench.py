@@ -61,6 +61,9 @@ def parse():
                     help="fp8: E4M3 pools (one new token per sequence)")
     ap.add_argument("--new-tokens", type=int, default=1,
                     help="new tokens per sequence per step (>1: causal multi-query attention)")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="decode layers per step, each with its own KV pools (one-token decode); "
+                         "the whole multi-layer step is one CUDA graph")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window in tokens for one-new-token decode (0 = none); "
                          "blocks wholly before the window are released from the tables")
@@ -392,6 +395,9 @@ def ours_arm(args):
     W = max(0, args.window)
     if W and N > 1:
         raise SystemExit("--window runs one new token per sequence")
+    LAYERS = max(1, args.layers)
+    if LAYERS > 1 and N > 1:
+        raise SystemExit("--layers runs one new token per sequence")
     # orc_arrays: host copies for the CPU baseline, taken before any kernel
     # touches the pools (the 16-bit, one-new-token step only)
     orc_arrays = oracle_arrays(inp) if (rank == 0 and world == 1 and N == 1 and not fp8
@@ -403,6 +409,11 @@ def ours_arm(args):
         vc = (vc.float() / vscale).clamp_(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
         del inp.key_cache, inp.value_cache
         torch.cuda.empty_cache()
+    # one pair of pools per layer (layer 0: the generated pools)
+    kcs, vcs = [kc], [vc]
+    for _ in range(LAYERS - 1):
+        kcs.append(kc.clone())
+        vcs.append(vc.clone())
     elt = 1 if fp8 else inp.q.element_size()
     lens = inp.seq_lens.cpu()
     if W:   # attended tokens per sequence; skipped blocks' table entries -> -1
@@ -441,7 +452,7 @@ def ours_arm(args):
     slots = torch.empty(S * N, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream()
 
-    def attention(t):
+    def attention(t, kc=kc, vc=vc):
         if N > 1:
             pa.pa_multi_query_attention(t["q"], t["qsl"], kc, vc, t["tables"], t["lens"],
                                         inp.scale, Hkv, out, max_query_len=N, max_seq_len=max_len,
@@ -464,19 +475,23 @@ def ours_arm(args):
 
     def step(t, ev=None):
         pa.pa_compute_slot_mapping(t["qsl"], t["pos"], t["tables"], B, slot_mapping=slots)
-        if fp8:
-            pa.pa_reshape_and_cache_fp8(t["k_new"], t["v_new"], slots, kc, vc, kscale, vscale)
-        else:
-            pa.pa_reshape_and_cache(t["k_new"], t["v_new"], slots, kc, vc)
-        if ev is not None:
-            ev[0].record(stream)
-        attention(t)
-        if ev is not None:
-            ev[1].record(stream)
+        for layer in range(LAYERS):
+            kcl, vcl = kcs[layer], vcs[layer]
+            if fp8:
+                pa.pa_reshape_and_cache_fp8(t["k_new"], t["v_new"], slots, kcl, vcl, kscale,
+                                            vscale)
+            else:
+                pa.pa_reshape_and_cache(t["k_new"], t["v_new"], slots, kcl, vcl)
+            if ev is not None and layer == 0:
+                ev[0].record(stream)
+            attention(t, kcl, vcl)
+            if ev is not None and layer == 0:
+                ev[1].record(stream)
 
-    launches_per_step = 3 + (1 if splits > 1 else 0)
-    label = (cfg.name + ("_fp8" if fp8 else "") + (f"_q{N}" if N > 1 else "") +
-             (f"_w{W}" if W else ""))
+    launches_per_step = 1 + LAYERS * (2 + (1 if splits > 1 else 0))
+    launch_label = (cfg.name + ("_fp8" if fp8 else "") + (f"_q{N}" if N > 1 else "") +
+                    (f"_w{W}" if W else ""))     # one attention launch
+    label = launch_label + (f"_L{LAYERS}" if LAYERS > 1 else "")
     kernel_name = ("pa_multi_query_attention" if N > 1 else
                    "pa_decode_attention_fp8" if fp8 else "pa_decode_attention") + (
                        "_window" if W else "")
@@ -592,9 +607,9 @@ def ours_arm(args):
             e2e_step()
         torch.cuda.synchronize()
         e2e_s = max_over_ranks(time.perf_counter() - t0, world)
-        e2e = {"value": round(world * kv_bytes * args.steps / e2e_s / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "seq_tokens_per_s": round(world * tokens * args.steps / e2e_s, 1)}
+        e2e = {"value": round(world * LAYERS * kv_bytes * args.steps / e2e_s / 1e9, 2),
+               "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "seq_tokens_per_s": round(world * LAYERS * tokens * args.steps / e2e_s, 1)}
 
     if rank != 0:
         return
@@ -614,22 +629,23 @@ def ours_arm(args):
                 "traffic": None, "avg_launch_us": round(attn_ms * 1e3, 2),
                 "algorithmic_flops_per_launch": flops}
     step_s = ms_total * 1e-3 / args.steps
-    value = world * kv_bytes / step_s / 1e9
+    value = world * LAYERS * kv_bytes / step_s / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * step_s, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.dtype, "kv_dtype": "e4m3" if fp8 else cfg.dtype, "accum_dtype": "f32",
         "data": "synthetic",
-        "seq_tokens_per_s": round(world * tokens / step_s, 1),
+        "seq_tokens_per_s": round(world * LAYERS * tokens / step_s, 1),
         "config": {
             "workload": label,
             "new_tokens_per_seq": N,
+            "layers": LAYERS,
             "shape": f"{S} seqs, ctx U[{cfg.ctx_lo},{cfg.ctx_hi}]+1 new token, "
                      f"{cfg.num_q_heads}q/{Hkv}kv heads, D={D}, B={B}, {cfg.dtype}"
             if cfg.ctx_fixed is None else f"{S} seqs x {cfg.ctx_fixed[0]}+1, "
                                           f"{cfg.num_q_heads}q/{Hkv}kv heads, D={D}, B={B}",
-            "context_tokens": tokens, "kv_read_bytes_per_step": kv_bytes,
+            "context_tokens": tokens, "kv_read_bytes_per_step": LAYERS * kv_bytes,
             "pool_blocks": inp.num_blocks, "partitions": splits, "partition_tokens": ptoks,
             "l2": ("inputs larger than L2 (KV read per step %.2f GB, pool %.2f GB; "
                    "129 MB L2), no flush" % (kv_bytes / 1e9, 2 * kc.numel() * elt / 1e9))
@@ -640,7 +656,7 @@ def ours_arm(args):
         "roofline": roof if tensor_bound else {"bound": "hbm", "kernel": kernel_name,
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(label),
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(launch_label),
                      "avg_launch_us": round(attn_ms * 1e3, 2),
                      "algorithmic_bytes_per_launch": kv_bytes},
         "gpu_launches": launches_per_step * args.steps,
