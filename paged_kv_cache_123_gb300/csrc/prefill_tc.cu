@@ -25,10 +25,12 @@
 //     (TMEM lane = row; warpgroup h takes score columns 64h .. 64h+63): they
 //     read the scores with tcgen05.ld, apply the causal limit and the scale
 //     in the log2 domain, exchange the two half-row maxima through shared
-//     memory, and write P (16-bit) to one of two TMEM P buffers with
-//     tcgen05.st. The output in TMEM is rescaled only when a row's running
-//     maximum grew by more than 2^8 (the weights stay below 256, and the
-//     final division uses the same reference).
+//     memory, and write P (16-bit) over the scores they came from with
+//     tcgen05.st. Each V stage carries a constant group of ones after the
+//     head dims, so the P V MMA also produces the row sums of exactly the
+//     rounded weights. Output and sums in TMEM are rescaled only when a
+//     row's running maximum grew by more than 2^8 (the weights stay below
+//     256, and the final division uses the same reference).
 // Keeping S and P out of shared memory leaves its bandwidth to the K/V
 // operands and their TMA loads. S of tile j+1 is computed while the softmax
 // warps work on tile j.
@@ -47,17 +49,19 @@ namespace {
 
 constexpr int kTcRows = 128;              // query rows per CTA (MMA M)
 constexpr int kTcKv = 128;                // KV tokens per tile
-constexpr int kTcStages = 3;              // K and V ring depth
+constexpr int kTcStages = 3;              // K ring depth
+constexpr int kTcVStages = 2;             // V ring depth
 constexpr int kTcSoftmaxWarps = 8;        // two warpgroups: columns 0-63, 64-127
 constexpr int kTcKProducerWarp = 8;       // Q and K tiles
 constexpr int kTcMmaWarp = 9;
 constexpr int kTcVProducerWarp = 10;      // V tiles
 constexpr int kTcThreads = 11 * 32;
 constexpr int kTcCols = kTcKv / 2;        // score columns per softmax thread
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), P0 [384,448), P1 [448,512)
+// TMEM columns: S0 [0,128), S1 [128,256) (P of a tile is written over the
+// first 32 columns of each 64-column half of its S buffer), O [256, 256+D)
+// and the row sums l in column 256+D (the ones group of V, 16 columns)
 constexpr uint32_t kTcTmemCols = 512;
 constexpr uint32_t kTcOCol = 256;
-constexpr uint32_t kTcPCol = 384;
 constexpr long long kTcWaitCycles = 4000000000LL;
 constexpr float kTcRescaleLog2 = 8.f;
 #define kNegInfT (-__int_as_float(0x7f800000))
@@ -72,7 +76,10 @@ struct TcLayout {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + Q_BYTES;
   static constexpr int V_OFF = K_OFF + kTcStages * KV_BYTES;
-  static constexpr int BAR_OFF = V_OFF + kTcStages * KV_BYTES;
+  // a V stage is the tile's 64-column groups of the head dim plus one group
+  // of 16-bit ones: P x [V | 1] also gives the row sums of the weights
+  static constexpr int V_STAGE = KV_BYTES + KV_HALF;
+  static constexpr int BAR_OFF = V_OFF + kTcVStages * V_STAGE;
   // q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], s_free[2],
   // p_full, o_done, done
   static constexpr int NBARS = 20;
@@ -184,6 +191,8 @@ __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
   using Ly = TcLayout<D>;
   const int full = IS_V ? kBarVFull : kBarKFull;
   const int empty = IS_V ? kBarVEmpty : kBarKEmpty;
+  constexpr int NST = IS_V ? kTcVStages : kTcStages;
+  constexpr int STRIDE = IS_V ? Ly::V_STAGE : Ly::KV_BYTES;
   const uint32_t base = s0 + (IS_V ? Ly::V_OFF : Ly::K_OFF);
   if (lane == 0) {
     prefetch_tensormap(tm);
@@ -200,7 +209,7 @@ __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
   const int R = B < kTcKv ? B : kTcKv;
   int issued = 0;
   for (int i = 0; i < ntiles; ++i) {
-    const int st = i % kTcStages;
+    const int st = i % NST;
     const int ts = kv_lo + i * kTcKv;
     const int te = min(kv_end, ts + kTcKv);
     int64_t blk;
@@ -210,8 +219,8 @@ __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
       latch(a.err, PA_ERR_OUT_OF_RANGE);
     int ok = 1;
     if (lane == 0) {
-      if (i >= kTcStages)
-        ok = mbar_wait_bounded(bar + 8u * (empty + st), ((i / kTcStages) - 1) & 1, abort_flag,
+      if (i >= NST)
+        ok = mbar_wait_bounded(bar + 8u * (empty + st), ((i / NST) - 1) & 1, abort_flag,
                                kTcWaitCycles);
       if (ok)
         mbar_arrive_expect_tx(bar + 8u * (full + st),
@@ -222,7 +231,7 @@ __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
     if (mine) {
       const int z = (int)(blk * a.num_kv_heads + kvh);
       const int y = (ts + lane * R) & (B - 1);
-      const uint32_t d = base + st * Ly::KV_BYTES + lane * R * 128;
+      const uint32_t d = base + st * STRIDE + lane * R * 128;
 #pragma unroll
       for (int h = 0; h < Ly::HALVES; ++h)
         tma_load_3d(d + h * Ly::KV_HALF, tm, h * 64, y, z, bar + 8u * (full + st));
@@ -232,38 +241,38 @@ __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
   // let this warp's copies land before the CTA can leave
   if (lane == 0) {
     if (!IS_V) mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
-    for (int j = issued > kTcStages ? issued - kTcStages : 0; j < issued; ++j)
-      mbar_wait_bounded(bar + 8u * (full + j % kTcStages), (j / kTcStages) & 1, abort_flag,
-                        kTcWaitCycles);
+    for (int j = issued > NST ? issued - NST : 0; j < issued; ++j)
+      mbar_wait_bounded(bar + 8u * (full + j % NST), (j / NST) & 1, abort_flag, kTcWaitCycles);
   }
 }
 
 // MMA issue (one thread): S_j = Q K_j^T into TMEM score buffer j&1, then
-// O += P_{j-1} V_{j-1} (P from TMEM buffer (j-1)&1) once the softmax warps
-// have written P_{j-1}.
+// [O | l] += P_{j-1} [V_{j-1} | 1] (P from TMEM, over the scores of tile
+// j-1) once the softmax warps have written P_{j-1}.
 template <typename T, int D>
 __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
                          volatile int* abort_flag) {
   using Ly = TcLayout<D>;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t idS = idesc_f16(kBf16, kTcRows, kTcKv, false, false);
-  constexpr uint32_t idO = idesc_f16(kBf16, kTcRows, D, false, true);
+  constexpr uint32_t idO = idesc_f16(kBf16, kTcRows, D + 16, false, true);
   const uint32_t qa = s0 + Ly::Q_OFF;
   auto issue_pv = [&](int t) -> bool {
-    const int vs = t % kTcStages;
+    const int vs = t % kTcVStages;
     if (!mbar_wait_bounded(bar + 8u * kBarPFull, t & 1, abort_flag, kTcWaitCycles)) return false;
-    if (!mbar_wait_bounded(bar + 8u * (kBarVFull + vs), (t / kTcStages) & 1, abort_flag,
+    if (!mbar_wait_bounded(bar + 8u * (kBarVFull + vs), (t / kTcVStages) & 1, abort_flag,
                            kTcWaitCycles))
       return false;
     tc_fence_after();
-    const uint32_t vb = s0 + Ly::V_OFF + vs * Ly::KV_BYTES;
-    const uint32_t pt = tmem + kTcPCol + (t & 1) * (kTcKv / 2);
+    const uint32_t vb = s0 + Ly::V_OFF + vs * Ly::V_STAGE;
+    const uint32_t pt = tmem + (t & 1) * kTcKv;    // P: tokens 64h.. at column 64h
 #pragma unroll
     for (int ks = 0; ks < kTcKv / 16; ++ks) {
-      // V tile: token rows of 64 head dims per 128-byte line (N-major);
-      // 16 tokens per k-step, the second half of D at KV_HALF
+      // [V | 1] tile: token rows of 64 columns per 128-byte line (N-major);
+      // 16 tokens per k-step, the next 64-column group at KV_HALF
       const uint64_t bd = smem_desc_sw128(vb + ks * 2048, Ly::KV_HALF, 1024);
-      mma_f16_ts(tmem + kTcOCol, pt + ks * 8, bd, idO, (t > 0 || ks > 0) ? 1u : 0u);
+      mma_f16_ts(tmem + kTcOCol, pt + (ks >> 2) * (kTcKv / 2) + (ks & 3) * 8, bd, idO,
+                 (t > 0 || ks > 0) ? 1u : 0u);
     }
     mma_commit(bar + 8u * kBarODone);
     mma_commit(bar + 8u * (kBarVEmpty + vs));
@@ -274,9 +283,12 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
     const int sb = j & 1, ks_ = j % kTcStages;
     ok = mbar_wait_bounded(bar + 8u * (kBarKFull + ks_), (j / kTcStages) & 1, abort_flag,
                            kTcWaitCycles);
+    // S_j reuses the buffer of tile j-2: its scores read (s_free) and its P
+    // read by P V of tile j-2 (o_done; P V of tile j-1 is not issued yet)
     if (ok && j >= 2)
       ok = mbar_wait_bounded(bar + 8u * (kBarSFree + sb), ((j >> 1) - 1) & 1, abort_flag,
-                             kTcWaitCycles);
+                             kTcWaitCycles) &&
+           mbar_wait_bounded(bar + 8u * kBarODone, (j - 2) & 1, abort_flag, kTcWaitCycles);
     if (!ok) break;
     tc_fence_after();
     const uint32_t kb = s0 + Ly::K_OFF + ks_ * Ly::KV_BYTES;
@@ -355,6 +367,18 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
     tmem_alloc(s0 + Ly::MISC_OFF, kTcTmemCols);
     tmem_relinquish();
   }
+  {
+    // the ones group of every V stage (1.0 in either 16-bit type); TMA never
+    // writes it
+    const uint32_t one2 = std::is_same<T, __nv_bfloat16>::value ? 0x3f803f80u : 0x3c003c00u;
+    for (int i = threadIdx.x; i < kTcVStages * Ly::KV_HALF / 16; i += kTcThreads) {
+      const int st = i / (Ly::KV_HALF / 16), off = i % (Ly::KV_HALF / 16);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
+                   ::"r"(s0 + Ly::V_OFF + st * Ly::V_STAGE + Ly::KV_BYTES + off * 16), "r"(one2)
+                   : "memory");
+    }
+  }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -397,7 +421,7 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       return -1;
     };
     int ent_next = piece_entry(0);
-    float m_use = kNegInfT, l = 0.f;
+    float m_use = kNegInfT;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
@@ -482,16 +506,14 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
         alpha = exp2f(m_use - m_new);
         resc = true;
         m_use = m_new;
-        l *= alpha;
       }
       // pass 2: P = 2^(x - m_use) rounded to the input type, 16 columns of
-      // packed pairs per 32 scores, into TMEM P buffer j&1 (its previous
-      // reader, P V of tile j-2, completed before S of tile j did); l sums
-      // the rounded weights the MMA multiplies
+      // packed pairs per 32 scores, written over the first 32 columns of
+      // this half row's scores (already in registers); the row sums come
+      // from the MMA's ones group
       const bool live = m_use != kNegInfT;
       const float nm = -m_use;
-      const uint32_t padr = tmem + lanes + kTcPCol + sb * (kTcKv / 2) + hf * (kTcCols / 2);
-      float l0 = 0.f, l1 = 0.f;
+      const uint32_t padr = sadr;
 #pragma unroll
       for (int ch = 0; ch < kTcCols / 32; ++ch) {
         const uint32_t vm = live ? vmask[ch] : 0u;
@@ -507,14 +529,10 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
             p0 = ((vm >> e) & 1u) ? p0 : 0.f;
             p1 = ((vm >> (e + 1)) & 1u) ? p1 : 0.f;
           }
-          float q0r, q1r;
-          pk[e >> 1] = Pack2<T>::pack(p0, p1, q0r, q1r);
-          l0 += q0r;
-          l1 += q1r;
+          pk[e >> 1] = Pack2<T>::pack_out(p0, p1);
         }
         tmem_st16(padr + ch * 16, pk);
       }
-      l += l0 + l1;
       // the output is rescaled only when some row of the warp needs it (the
       // other half row takes the same decision); P V of tile j-1 must have
       // completed first (P V of tile j-2 completed before S of tile j, which
@@ -534,6 +552,10 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
             for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
             tmem_st32(oadr, v);
           }
+          if (hf == 0) {                // the row sums, once per row
+            const uint32_t ladr = tmem + lanes + kTcOCol + D;
+            tmem_st1(ladr, __float_as_uint(__uint_as_float(tmem_ld1(ladr)) * alpha));
+          }
         }
       }
       // V rows that hold no token of this tile may contain anything (NaN
@@ -542,12 +564,12 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       if (!whole && ok && hf < Ly::HALVES) {
         // the V tile must have landed before its rows are cleared (its stage
         // is not refilled before P V of this tile, so the phase is current)
-        const int vs = j % kTcStages;
-        ok = mbar_wait_bounded(bar + 8u * (kBarVFull + vs), (j / kTcStages) & 1, abort_flag,
+        const int vs = j % kTcVStages;
+        ok = mbar_wait_bounded(bar + 8u * (kBarVFull + vs), (j / kTcVStages) & 1, abort_flag,
                                kTcWaitCycles);
         const bool row_ok = r < te - ts && ((pm >> (r >> rshift)) & 1u);
         if (ok && !row_ok) {
-          const uint32_t vrow = s0 + Ly::V_OFF + vs * Ly::KV_BYTES + hf * Ly::KV_HALF + r * 128;
+          const uint32_t vrow = s0 + Ly::V_OFF + vs * Ly::V_STAGE + hf * Ly::KV_HALF + r * 128;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
@@ -565,13 +587,9 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       ok = mbar_wait_bounded(bar + 8u * kBarDone, 0, abort_flag, kTcWaitCycles);
       tc_fence_after();
     }
-    // the two half-row sums meet
-    float* lsum = xch;                              // [2 halves][128], tiles done
-    ok = softmax_bar_and(ok);
-    if (ok) lsum[hf * kTcRows + r] = l;
-    ok = softmax_bar_and(ok);
+    ok = __all_sync(0xffffffffu, ok);
     if (ok) {
-      l += lsum[(hf ^ 1) * kTcRows + r];
+      const float l = __uint_as_float(tmem_ld1(tmem + lanes + kTcOCol + D));
       const int64_t t = q0 + i;
       const int head = kvh * G + rr % G;
       const int count = rv ? (pos + a.partition) / a.partition : 0;
