@@ -57,11 +57,11 @@ constexpr int kTcMmaWarp = 9;
 constexpr int kTcVProducerWarp = 10;      // V tiles
 constexpr int kTcThreads = 11 * 32;
 constexpr int kTcCols = kTcKv / 2;        // score columns per softmax thread
-// TMEM columns: S0 [0,128), S1 [128,256) (P of a tile is written over the
-// first 32 columns of each 64-column half of its S buffer), O [256, 256+D)
-// and the row sums l in column 256+D (the ones group of V, 16 columns)
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D) and the row sums l
+// in column 256+D (the ones group of V, 16 columns), P [400, 464)
 constexpr uint32_t kTcTmemCols = 512;
 constexpr uint32_t kTcOCol = 256;
+constexpr uint32_t kTcPCol = 400;
 constexpr long long kTcWaitCycles = 4000000000LL;
 constexpr float kTcRescaleLog2 = 8.f;
 #define kNegInfT (-__int_as_float(0x7f800000))
@@ -246,9 +246,9 @@ __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
   }
 }
 
-// MMA issue (one thread): S_j = Q K_j^T into TMEM score buffer j&1, then
-// [O | l] += P_{j-1} [V_{j-1} | 1] (P from TMEM, over the scores of tile
-// j-1) once the softmax warps have written P_{j-1}.
+// MMA issue (one thread): S_j = Q K_j^T into TMEM score buffer j&1, two
+// tiles ahead, and [O | l] += P_j [V_j | 1] (P from TMEM) once the softmax
+// warps have written P_j.
 template <typename T, int D>
 __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
                          volatile int* abort_flag) {
@@ -265,31 +265,28 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
       return false;
     tc_fence_after();
     const uint32_t vb = s0 + Ly::V_OFF + vs * Ly::V_STAGE;
-    const uint32_t pt = tmem + (t & 1) * kTcKv;    // P: tokens 64h.. at column 64h
+    const uint32_t pt = tmem + kTcPCol;
 #pragma unroll
     for (int ks = 0; ks < kTcKv / 16; ++ks) {
       // [V | 1] tile: token rows of 64 columns per 128-byte line (N-major);
       // 16 tokens per k-step, the next 64-column group at KV_HALF
       const uint64_t bd = smem_desc_sw128(vb + ks * 2048, Ly::KV_HALF, 1024);
-      mma_f16_ts(tmem + kTcOCol, pt + (ks >> 2) * (kTcKv / 2) + (ks & 3) * 8, bd, idO,
-                 (t > 0 || ks > 0) ? 1u : 0u);
+      mma_f16_ts(tmem + kTcOCol, pt + ks * 8, bd, idO, (t > 0 || ks > 0) ? 1u : 0u);
     }
     mma_commit(bar + 8u * kBarODone);
     mma_commit(bar + 8u * (kBarVEmpty + vs));
     return true;
   };
-  bool ok = mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
-  for (int j = 0; ok && j < ntiles; ++j) {
-    const int sb = j & 1, ks_ = j % kTcStages;
-    ok = mbar_wait_bounded(bar + 8u * (kBarKFull + ks_), (j / kTcStages) & 1, abort_flag,
-                           kTcWaitCycles);
-    // S_j reuses the buffer of tile j-2: its scores read (s_free) and its P
-    // read by P V of tile j-2 (o_done; P V of tile j-1 is not issued yet)
-    if (ok && j >= 2)
-      ok = mbar_wait_bounded(bar + 8u * (kBarSFree + sb), ((j >> 1) - 1) & 1, abort_flag,
-                             kTcWaitCycles) &&
-           mbar_wait_bounded(bar + 8u * kBarODone, (j - 2) & 1, abort_flag, kTcWaitCycles);
-    if (!ok) break;
+  // S_t into score buffer t&1 once K_t has landed and the softmax warps
+  // have read S_{t-2} from that buffer
+  auto issue_s = [&](int t) -> bool {
+    const int sb = t & 1, ks_ = t % kTcStages;
+    if (!mbar_wait_bounded(bar + 8u * (kBarKFull + ks_), (t / kTcStages) & 1, abort_flag,
+                           kTcWaitCycles))
+      return false;
+    if (t >= 2 && !mbar_wait_bounded(bar + 8u * (kBarSFree + sb), ((t >> 1) - 1) & 1,
+                                      abort_flag, kTcWaitCycles))
+      return false;
     tc_fence_after();
     const uint32_t kb = s0 + Ly::K_OFF + ks_ * Ly::KV_BYTES;
 #pragma unroll
@@ -300,9 +297,17 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
     }
     mma_commit(bar + 8u * (kBarSFull + sb));
     mma_commit(bar + 8u * (kBarKEmpty + ks_));
-    if (j >= 1) ok = issue_pv(j - 1);
+    return true;
+  };
+  // S runs two tiles ahead: S_{j+2} is issued as soon as the softmax warps
+  // have read S_j, before P V of tile j, so the scores of the next tiles are
+  // ready when the softmax warps get to them
+  bool ok = mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
+  for (int t = 0; ok && t < 2 && t < ntiles; ++t) ok = issue_s(t);
+  for (int j = 0; ok && j < ntiles; ++j) {
+    if (j + 2 < ntiles) ok = issue_s(j + 2);
+    if (ok) ok = issue_pv(j);
   }
-  if (ok && ntiles > 0) issue_pv(ntiles - 1);
   // every MMA issued above has completed once this barrier fires
   mma_commit(bar + 8u * kBarDone);
   mbar_wait_bounded(bar + 8u * kBarDone, 0, abort_flag, kTcWaitCycles);
@@ -507,13 +512,20 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
         resc = true;
         m_use = m_new;
       }
+      // P V of tile j-1 has read the P buffer and finished adding to the
+      // output once o_done shows it (P V of tile j-2 completed before this
+      // warp's previous tile wrote P, so the phase is current)
+      if (j >= 1) {
+        ok = mbar_wait_bounded(bar + 8u * kBarODone, (j - 1) & 1, abort_flag, kTcWaitCycles);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+      }
       // pass 2: P = 2^(x - m_use) rounded to the input type, 16 columns of
-      // packed pairs per 32 scores, written over the first 32 columns of
-      // this half row's scores (already in registers); the row sums come
-      // from the MMA's ones group
+      // packed pairs per 32 scores, into the TMEM P buffer (tokens 64 hf ..
+      // at column 32 hf); the row sums come from the MMA's ones group
       const bool live = m_use != kNegInfT;
       const float nm = -m_use;
-      const uint32_t padr = sadr;
+      const uint32_t padr = tmem + lanes + kTcPCol + hf * (kTcCols / 2);
 #pragma unroll
       for (int ch = 0; ch < kTcCols / 32; ++ch) {
         const uint32_t vm = live ? vmask[ch] : 0u;
@@ -534,14 +546,9 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
         tmem_st16(padr + ch * 16, pk);
       }
       // the output is rescaled only when some row of the warp needs it (the
-      // other half row takes the same decision); P V of tile j-1 must have
-      // completed first (P V of tile j-2 completed before S of tile j, which
-      // this thread has seen)
+      // other half row takes the same decision); P V of tile j-1 has
+      // completed (waited for above)
       if (__any_sync(0xffffffffu, resc)) {
-        if (j >= 1)
-          ok = mbar_wait_bounded(bar + 8u * kBarODone, (j - 1) & 1, abort_flag, kTcWaitCycles);
-        ok = __all_sync(0xffffffffu, ok);
-        tc_fence_after();
         if (ok) {
 #pragma unroll 1
           for (int ch = 0; ch < D / 64; ++ch) {
