@@ -340,7 +340,8 @@ def reference_arm(args):
     workers = host_cores()
     timer = OracleTimer(oracle_arrays(inp), inp.cfg, inp.scale, workers)
     try:
-        timer.size_sample(max(0.5, 120.0 / max(1, args.steps + args.warmup)))
+        # about two minutes of oracle work over the whole run, whatever K and W
+        timer.size_sample(max(0.05, 120.0 / max(1, args.steps + args.warmup)))
         gbs_list, tps_list, dts = [], [], []
         desc = ""
         for i in range(args.warmup + args.steps):
