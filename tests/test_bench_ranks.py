@@ -52,3 +52,15 @@ def test_kv_read_bytes_counts_valid_tokens_only():
     import bench
     # 2 sequences of 3 and 5 tokens, 8 KV heads, head size 128, 2-byte dtype
     assert bench.kv_read_bytes([3, 5], 8, 128, 2) == 8 * 2 * 8 * 128 * 2
+
+
+def test_attention_flops_counts_visible_keys():
+    """The prefill roofline's algorithmic flops: new token i of a sequence
+    with c cached tokens sees c + i + 1 keys; 4 flops per key and head dim
+    (q.k and p.v) per query head. Checked against a direct count."""
+    import bench
+    for ctx, n, hq, d in (([0], 1, 1, 1), ([0, 5, 17], 3, 8, 128), ([1000, 0], 64, 64, 64)):
+        direct = sum(4 * d * hq * (c + i + 1) for c in ctx for i in range(n))
+        assert bench.attention_flops(ctx, n, hq, d) == direct
+    # one new token: decode, 4 * D * Hq per cached-or-new key
+    assert bench.attention_flops([9], 1, 2, 16) == 4 * 16 * 2 * 10
