@@ -272,10 +272,11 @@ int pa_decode_attention_window(const void* q, const void* key_cache, const void*
                     workspace, workspace_bytes, stream);
 }
 
-// Context partitions of the multi-query kernel. Only short query runs
-// (every sequence's rows fit one 64-row tile) are split: long prefill chunks
-// already give many row tiles. The length is picked as for the decode
-// tensor-core kernel (two waves of resident CTAs, 256..2048 tokens).
+// Context partitions of the multi-query kernels. Only short query runs (at
+// most 64 (token, head) rows per KV head, e.g. speculative tokens) are
+// split: longer runs already give many row tiles. The length is picked as
+// for the decode tensor-core kernel (two waves of resident CTAs, 256..2048
+// tokens).
 static void mq_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
                      int max_query_len, int max_seq_len, int partition_size, int sm_count,
                      int* splits, int* tokens) {

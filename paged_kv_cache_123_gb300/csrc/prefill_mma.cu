@@ -9,15 +9,12 @@
 // L_s tokens in the pool including them) sits at position L_s - n_s + i and
 // attends to positions 0 .. L_s - n_s + i, read through the block table.
 //
-// Rows are (new token, query head) pairs of one KV head, query-major
-// (row = i * G + g), so the G heads of a group share each K/V read. A CTA
-// owns 64 rows; each of its four consumer warps owns 16 rows and runs the
-// whole KV range up to its CTA's last position: S = Q K^T and O += P V with
-// mma.sync m16n8k16 (rows as M, 8 KV tokens or 8 head dims as N), online
-// softmax in the log2 domain, causal mask per row. K/V tiles of 64 tokens
-// arrive by the same TMA / mbarrier ring as the decode kernel (one 4-D box per
-// block, 128-byte swizzle). Tiles past every row of a warp are skipped by
-// that warp; V rows past the sequence end are cleared in registers before P V.
+// This file holds the short runs — at most 16 (token, head) columns per KV
+// head, e.g. one or two speculative tokens of a GQA group of 8 — on
+// mma.sync in the decode kernel's layout, and the log-sum-exp combine of KV
+// partitions shared with the tcgen05 kernel (prefill_tc.cu), which takes
+// every longer run. K/V tiles of 64 tokens arrive by the same TMA / mbarrier
+// ring as the decode kernel (one 4-D box per block, 128-byte swizzle).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -32,24 +29,15 @@ namespace {
 
 constexpr int kMqConsumers = 4;
 constexpr int kMqThreads = (kMqConsumers + 1) * 32;
-constexpr int kMqTile = 64;        // KV tokens per stage and rows per CTA
+constexpr int kMqTile = 64;        // KV tokens per stage
 constexpr int kMqStages = 3;
 constexpr long long kMqWaitCycles = 4000000000LL;
 #define kNegInfQ (-__int_as_float(0x7f800000))
 
-// Address of 16-byte chunk `dch` of token row `row` when each 64-column half
-// of the head dim is its own [64 rows][128 B] region with the 128-byte
-// swizzle: 8 consecutive rows at one chunk hit 8 different bank groups.
-__device__ __forceinline__ uint32_t swz_split(uint32_t base, int row, int dch) {
-  return base + (dch >> 3) * (kMqTile * 128) + row * 128 + (((dch & 7) ^ (row & 7)) << 4);
-}
-
 // Producer warp: fill the ring with the KV tiles [0, ntiles) of (sequence,
-// kv head): lane p issues the TMA loads of the tile's block-piece p.
-// SPLIT: the stage holds each 64-column half of the head dim as its own
-// [64 rows][128 B] region (one 3-D box per half); otherwise whole rows (one
-// 4-D box).
-template <int ROW_BYTES, int KV_BYTES, int STAGE_BYTES, bool SPLIT>
+// kv head): lane p issues the TMA loads (whole rows, one 4-D box per block
+// piece) of the tile's block-piece p.
+template <int ROW_BYTES, int KV_BYTES, int STAGE_BYTES>
 __device__ void mq_produce(const MultiQueryArgs& a, const CUtensorMap* tmK,
                            const CUtensorMap* tmV, const int32_t* trow, int kvh, int kv_lo,
                            int kv_end, int ntiles, uint32_t smem0, uint32_t bar0, unsigned* tile_mask,
@@ -92,17 +80,8 @@ __device__ void mq_produce(const MultiQueryArgs& a, const CUtensorMap* tmK,
       const uint32_t kdst = smem0 + st * STAGE_BYTES + lane * R * ROW_BYTES;
       const int z = (int)(blk * a.num_kv_heads + kvh);
       const int y = tok & (B - 1);
-      if (SPLIT) {
-        const uint32_t base = smem0 + st * STAGE_BYTES + lane * R * 128;
-#pragma unroll
-        for (int h = 0; h < ROW_BYTES / 128; ++h) {
-          tma_load_3d(base + h * kMqTile * 128, tmK, h * 64, y, z, bar0 + 8u * st);
-          tma_load_3d(base + KV_BYTES + h * kMqTile * 128, tmV, h * 64, y, z, bar0 + 8u * st);
-        }
-      } else {
-        tma_load_4d(kdst, tmK, 0, 0, y, z, bar0 + 8u * st);
-        tma_load_4d(kdst + KV_BYTES, tmV, 0, 0, y, z, bar0 + 8u * st);
-      }
+      tma_load_4d(kdst, tmK, 0, 0, y, z, bar0 + 8u * st);
+      tma_load_4d(kdst + KV_BYTES, tmV, 0, 0, y, z, bar0 + 8u * st);
     }
     issued = i + 1;
   }
@@ -110,252 +89,6 @@ __device__ void mq_produce(const MultiQueryArgs& a, const CUtensorMap* tmK,
     for (int j = issued > kMqStages ? issued - kMqStages : 0; j < issued; ++j)
       mbar_wait_bounded(bar0 + 8u * (j % kMqStages), (j / kMqStages) & 1, abort_flag,
                         kMqWaitCycles);
-}
-
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kMqThreads, 2)
-multi_query_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV) {
-  constexpr int HALVES = D / 64;
-  constexpr int ROW_BYTES = HALVES * 128;
-  constexpr int KV_BYTES = kMqTile * ROW_BYTES;
-  constexpr int STAGE_BYTES = 2 * KV_BYTES;
-  constexpr int KSTEPS = D / 16;        // k-steps of Q K^T
-  constexpr int DN = D / 8;             // 8-wide head-dim tiles of O
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kMqStages * STAGE_BYTES);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMqStages);
-  unsigned* tile_mask = reinterpret_cast<unsigned*>(bars + 2 * kMqStages) + 1;
-  const uint32_t smem0 = smem_u32(smem);
-  const uint32_t bar0 = smem_u32(bars);
-
-  const int s = blockIdx.z, kvh = blockIdx.y;
-  const int row_tiles = (a.max_query_len * G + kMqTile - 1) / kMqTile;
-  const int qt = blockIdx.x % row_tiles, split = blockIdx.x / row_tiles;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Hq = a.num_q_heads;
-  const int q0 = a.qsl[s];
-  const int n = a.qsl[s + 1] - q0;
-  const int L = a.seq_lens[s];
-  if (n < 0 || n > a.max_query_len || L < n || L > a.max_seq_len ||
-      (int64_t)L > a.table_stride * a.block_size || q0 < 0) {
-    if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) latch(a.err, PA_ERR_OUT_OF_RANGE);
-    return;
-  }
-  const int r0 = qt * kMqTile;                       // first row of this CTA
-  if (r0 >= n * G) return;
-  const int i_last = min(n - 1, (r0 + kMqTile - 1) / G);
-  const int kv_all = L - n + i_last + 1;             // keys any row here may see
-  const int kv_lo = split * a.partition;             // this CTA's partition
-  if (kv_lo >= kv_all) return;
-  const int kv_end = min(kv_all, kv_lo + a.partition);
-  const int ntiles = (kv_end - kv_lo + kMqTile - 1) / kMqTile;
-  const int32_t* trow = a.tables + (int64_t)s * a.table_stride;
-
-  if (threadIdx.x == 0) {
-    for (int st = 0; st < kMqStages; ++st) {
-      mbar_init(bar0 + 8u * st, 1);
-      mbar_init(bar0 + 8u * (kMqStages + st), kMqConsumers);
-    }
-    *abort_flag = 0;
-    mbar_fence_init();
-  }
-  __syncthreads();
-
-  if (warp == kMqConsumers) {
-    mq_produce<ROW_BYTES, KV_BYTES, STAGE_BYTES, true>(a, &tmK, &tmV, trow, kvh, kv_lo, kv_end,
-                                                       ntiles,
-                                                 smem0, bar0, tile_mask, abort_flag, lane);
-    __syncthreads();
-    if (*abort_flag && lane == 0) latch(a.err, PA_ERR_TIMEOUT);
-    return;
-  }
-
-  // ---- consumer warp: rows rw0 .. rw0+15; this lane holds rows n8 and n8+8
-  const int c = lane & 3, n8 = lane >> 2;
-  const int rw0 = r0 + warp * 16;
-  int pos[2];            // causal limit (last visible key) per held row; -1 = no row
-  bool rv[2];
-  uint32_t qa[KSTEPS][4];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = rw0 + n8 + 8 * h;
-    const int i = r / G;
-    rv[h] = i < n;
-    pos[h] = rv[h] ? L - n + i : -1;
-  }
-  {
-    const T* qb[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = rw0 + n8 + 8 * h;
-      qb[h] = reinterpret_cast<const T*>(a.q) +
-              ((int64_t)(q0 + r / G) * Hq + (int64_t)kvh * G + r % G) * D;
-    }
-#pragma unroll
-    for (int ks = 0; ks < KSTEPS; ++ks) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        qa[ks][h] = rv[h] ? *reinterpret_cast<const uint32_t*>(qb[h] + ks * 16 + 2 * c) : 0u;
-        qa[ks][h + 2] =
-            rv[h] ? *reinterpret_cast<const uint32_t*>(qb[h] + ks * 16 + 8 + 2 * c) : 0u;
-      }
-    }
-  }
-  // the largest causal limit among this warp's 16 rows
-  int warp_last = max(pos[0], pos[1]);
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1)
-    warp_last = max(warp_last, __shfl_xor_sync(0xffffffffu, warp_last, off));
-
-  float o[DN][4];
-#pragma unroll
-  for (int j = 0; j < DN; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m[2] = {kNegInfQ, kNegInfQ}, l[2] = {0.f, 0.f};
-  const float sl2 = a.scale * kLog2e;
-  const int B = a.block_size;
-  const int R = B < kMqTile ? B : kMqTile;
-  const int npieces = kMqTile / R;
-  const unsigned full_mask = npieces >= 32 ? 0xffffffffu : ((1u << npieces) - 1u);
-
-  for (int i = 0; i < ntiles; ++i) {
-    const int st = i % kMqStages;
-    if (!mbar_wait_bounded(bar0 + 8u * st, (i / kMqStages) & 1, abort_flag, kMqWaitCycles))
-      break;
-    const int ts = kv_lo + i * kMqTile;
-    const int te = min(kv_end, ts + kMqTile);
-    const uint32_t kst = smem0 + st * STAGE_BYTES;
-    const uint32_t vst = kst + KV_BYTES;
-    const unsigned pm = tile_mask[st];
-    const bool need_zero = !(te - ts == kMqTile && pm == full_mask);
-    if (ts <= warp_last) {
-      float sacc[8][4];
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-      for (int kp = 0; kp < KSTEPS / 2; ++kp) {
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          uint32_t kb[4];
-          ldsm_x4(kb, swz_split(kst, nt * 8 + (lane & 7), 4 * kp + (lane >> 3)));
-          MmaOps<T>::mma(sacc[nt], qa[2 * kp], kb[0], kb[1]);
-          MmaOps<T>::mma(sacc[nt], qa[2 * kp + 1], kb[2], kb[3]);
-        }
-      }
-      float mx[2] = {kNegInfQ, kNegInfQ};
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int rr = nt * 8 + 2 * c + (e & 1);
-          const int j = ts + rr;
-          const int h = e >> 1;
-          const bool ok = j <= pos[h] && j < te && ((pm >> (rr / R)) & 1u);
-          sacc[nt][e] = ok ? sacc[nt][e] * sl2 : kNegInfQ;
-          mx[h] = fmaxf(mx[h], sacc[nt][e]);
-        }
-      }
-      float al[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-        const float mn = fmaxf(m[h], mx[h]);
-        const bool live = mn != kNegInfQ;
-        al[h] = live ? exp2f(m[h] - mn) : 1.f;
-        m[h] = mn;
-        l[h] *= al[h];
-      }
-      uint32_t pa[4][4];
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        float p[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h = e >> 1;
-          p[e] = (m[h] != kNegInfQ) ? exp2f(sacc[nt][e] - m[h]) : 0.f;
-        }
-        const uint32_t lo = MmaOps<T>::pack(p[0], p[1]);   // row n8
-        const uint32_t hi = MmaOps<T>::pack(p[2], p[3]);   // row n8 + 8
-        const float2 flo = MmaOps<T>::unpack(lo), fhi = MmaOps<T>::unpack(hi);
-        l[0] += flo.x + flo.y;
-        l[1] += fhi.x + fhi.y;
-        pa[nt >> 1][(nt & 1) * 2 + 0] = lo;
-        pa[nt >> 1][(nt & 1) * 2 + 1] = hi;
-      }
-#pragma unroll
-      for (int j = 0; j < DN; ++j) {
-        o[j][0] *= al[0]; o[j][1] *= al[0]; o[j][2] *= al[1]; o[j][3] *= al[1];
-      }
-      // V rows that hold no token of this sequence may contain anything (NaN
-      // included); their weight is 0, but 0 * NaN is NaN, so the fragment
-      // halves of those rows are cleared in registers before the product.
-      uint32_t vm[4][2];
-#pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int rr = kt * 16 + hh * 8 + 2 * c;
-          const bool v0 = !need_zero || ((ts + rr < te) && ((pm >> (rr / R)) & 1u));
-          const bool v1 = !need_zero || ((ts + rr + 1 < te) && ((pm >> ((rr + 1) / R)) & 1u));
-          vm[kt][hh] = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
-        }
-      }
-#pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
-#pragma unroll
-        for (int dp = 0; dp < DN / 2; ++dp) {
-          uint32_t vb[4];
-          ldsm_x4_trans(vb, swz_split(vst, kt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7),
-                                      2 * dp + (lane >> 4)));
-          vb[0] &= vm[kt][0]; vb[1] &= vm[kt][1]; vb[2] &= vm[kt][0]; vb[3] &= vm[kt][1];
-          MmaOps<T>::mma(o[2 * dp], pa[kt], vb[0], vb[1]);
-          MmaOps<T>::mma(o[2 * dp + 1], pa[kt], vb[2], vb[3]);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar0 + 8u * (kMqStages + st));
-  }
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
-    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
-  }
-  __syncthreads();
-  if (*abort_flag) return;
-  T* out = reinterpret_cast<T*>(a.out);
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    if (!rv[h]) continue;
-    const int r = rw0 + n8 + 8 * h;
-    const int64_t t = q0 + r / G;
-    const int head = kvh * G + r % G;
-    const int count = (pos[h] + a.partition) / a.partition;   // partitions holding its keys
-    if (count == 1) {
-      if (split != 0) continue;
-      const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
-      T* op = out + (t * Hq + head) * D;
-#pragma unroll
-      for (int j = 0; j < DN; ++j) {
-        const uint32_t v = MmaOps<T>::pack(o[j][2 * h] * inv, o[j][2 * h + 1] * inv);
-        *reinterpret_cast<uint32_t*>(op + j * 8 + 2 * c) = v;
-      }
-    } else if (split < count) {
-      const int64_t slot = (t * Hq + head) * a.num_splits + split;
-      float* acc = a.ws_acc + slot * D;
-#pragma unroll
-      for (int j = 0; j < DN; ++j)
-        *reinterpret_cast<float2*>(acc + j * 8 + 2 * c) = make_float2(o[j][2 * h], o[j][2 * h + 1]);
-      if (c == 0) {
-        a.ws_ml[2 * slot] = m[h];
-        a.ws_ml[2 * slot + 1] = l[h];
-      }
-    }
-  }
 }
 
 // Log-sum-exp merge of the partitions of one (new token, query head) row;
@@ -473,7 +206,7 @@ multi_query_cols_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensor
   }
 
   if (warp == kMqConsumers) {
-    mq_produce<ROW_BYTES, KV_BYTES, STAGE_BYTES, false>(a, &tmK, &tmV, trow, kvh, kv_lo, kv_end,
+    mq_produce<ROW_BYTES, KV_BYTES, STAGE_BYTES>(a, &tmK, &tmV, trow, kvh, kv_lo, kv_end,
                                                         ntiles, smem0, bar0, tile_mask, abort_flag,
                                                  lane);
   } else {
@@ -652,38 +385,6 @@ multi_query_cols_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensor
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode_halves = nullptr;
-std::once_flag g_encode_halves_once;
-
-// Pool [NB][Hkv][B][D] (16-bit dtype) as a 3-D tensor {D, B, NB*Hkv} with
-// boxes of one 64-column half of min(B, 64) rows, 128-byte swizzle.
-bool encode_pool_halves_map(CUtensorMap* map, const void* base, int dtype, int64_t num_blocks,
-                            int num_kv_heads, int block_size, int head_size) {
-  std::call_once(g_encode_halves_once, []() {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode_halves = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  if (!g_encode_halves) return false;
-  const uint64_t D = head_size, B = block_size;
-  const uint64_t planes = (uint64_t)num_blocks * num_kv_heads;
-  if (planes == 0 || planes > 0x7fffffffull || D % 64 != 0) return false;
-  cuuint64_t dims[3] = {D, B, planes};
-  cuuint64_t strides[2] = {D * 2, B * D * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)(B < 64 ? B : 64), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return g_encode_halves(map,
-                         dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                         3, const_cast<void*>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 constexpr int mq_smem_bytes() {
   return 1024 + kMqStages * 2 * kMqTile * (D / 64) * 128 + 2 * kMqStages * 8 + 4 +
@@ -692,36 +393,23 @@ constexpr int mq_smem_bytes() {
 
 template <typename T, int D, int G>
 cudaError_t launch_mq_tdg(const MultiQueryArgs& a, cudaStream_t st) {
-  const int64_t rows_ = (int64_t)a.max_query_len * G;
-  const bool cols_kernel = (rows_ + kMqsCols - 1) / kMqsCols <= 2;
-  // the row kernel reads every K/V row many times: conflict-free halves; the
-  // column kernel streams: whole-row boxes
-  CUtensorMap tk, tv;
-  const bool ok =
-      cols_kernel
-          ? encode_kv_pool_map(&tk, a.kc, a.dtype, a.num_blocks, a.num_kv_heads, a.block_size,
-                               a.head_size) &&
-                encode_kv_pool_map(&tv, a.vc, a.dtype, a.num_blocks, a.num_kv_heads,
-                                   a.block_size, a.head_size)
-          : encode_pool_halves_map(&tk, a.kc, a.dtype, a.num_blocks, a.num_kv_heads,
-                                   a.block_size, a.head_size) &&
-                encode_pool_halves_map(&tv, a.vc, a.dtype, a.num_blocks, a.num_kv_heads,
-                                       a.block_size, a.head_size);
-  if (!ok) return cudaErrorInvalidValue;
-  constexpr int smem = mq_smem_bytes<D>();
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, []() {
-    attr = cudaFuncSetAttribute(multi_query_kernel<T, D, G>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  });
-  if (attr != cudaSuccess) return attr;
-  const int64_t rows = (int64_t)a.max_query_len * G;
-  const int64_t tiles = (rows + kMqTile - 1) / kMqTile;
-  if (tiles == 0 || a.num_seqs == 0) return cudaSuccess;
-  const int64_t col_tiles = (rows + kMqsCols - 1) / kMqsCols;
-  if (col_tiles <= 2) {
+  const int64_t rows = (int64_t)a.max_query_len * G;   // (token, head) rows per KV head
+  if (rows == 0 || a.num_seqs == 0) return cudaSuccess;
+  if (rows > kMqsCols) {
+    // more than 16 rows per KV head (prefill chunks, and speculative runs
+    // such as 4 tokens x 8 heads): the tcgen05 kernel, 128 rows per CTA;
+    // even mostly empty row tiles keep it ahead of mma.sync
+    cudaError_t e = launch_multi_query_tc(a, st);
+    if (e != cudaSuccess) return e;
+  } else {
     // a few new tokens per sequence: columns as N, KV tokens as M
+    CUtensorMap tk, tv;
+    if (!encode_kv_pool_map(&tk, a.kc, a.dtype, a.num_blocks, a.num_kv_heads, a.block_size,
+                            a.head_size) ||
+        !encode_kv_pool_map(&tv, a.vc, a.dtype, a.num_blocks, a.num_kv_heads, a.block_size,
+                            a.head_size))
+      return cudaErrorInvalidValue;
+    constexpr int smem = mq_smem_bytes<D>();
     static std::once_flag once_cols;
     static cudaError_t attr_cols = cudaSuccess;
     std::call_once(once_cols, []() {
@@ -729,15 +417,8 @@ cudaError_t launch_mq_tdg(const MultiQueryArgs& a, cudaStream_t st) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_cols != cudaSuccess) return attr_cols;
-    dim3 grid((unsigned)(col_tiles * a.num_splits), a.num_kv_heads, a.num_seqs);
+    dim3 grid((unsigned)a.num_splits, a.num_kv_heads, a.num_seqs);
     multi_query_cols_kernel<T, D, G><<<grid, kMqThreads, smem, st>>>(a, tk, tv);
-  } else if (rows > kMqTile) {
-    // long runs (prefill chunks): the tcgen05 kernel, 128 rows per CTA
-    cudaError_t e = launch_multi_query_tc(a, st);
-    if (e != cudaSuccess) return e;
-  } else {
-    dim3 grid((unsigned)(tiles * a.num_splits), a.num_kv_heads, a.num_seqs);
-    multi_query_kernel<T, D, G><<<grid, kMqThreads, smem, st>>>(a, tk, tv);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.num_splits <= 1) return e;
