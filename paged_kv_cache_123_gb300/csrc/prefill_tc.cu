@@ -313,7 +313,9 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
   mbar_wait_bounded(bar + 8u * kBarDone, 0, abort_flag, kTcWaitCycles);
 }
 
-template <typename T, int D, int G>
+// SKIP_IDLE: runs shorter than a row tile leave whole warps without a token
+// row; that instantiation lets such warps skip the score work.
+template <typename T, int D, int G, bool SKIP_IDLE>
 __global__ void __launch_bounds__(kTcThreads, 1)
 multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -408,6 +410,10 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
     const int i = rr / G;
     const bool rv = i < n;
     const int pos = rv ? L - n + i : -1;            // causal limit of this row
+    // a warp none of whose rows holds a token (short runs: 4 tokens x 8
+    // heads fill 32 of the 128 rows) skips the score work; its P rows are
+    // written as zeros once and its V-row clearing duty stays
+    const bool idle = SKIP_IDLE && __all_sync(0xffffffffu, !rv);
     const float sl2 = a.scale * kLog2e;
     const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
     float* xch = reinterpret_cast<float*>(smem + Ly::XCH_OFF);   // [2 halves][128]
@@ -469,7 +475,12 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       // this thread's 64 scores, one load; they stay in registers for both
       // passes
       uint32_t v[kTcCols];
-      if (ok) tmem_ld64(sadr, v);
+      if (ok && !idle) {
+        tmem_ld64(sadr, v);
+      } else if (SKIP_IDLE) {
+#pragma unroll
+        for (int e = 0; e < kTcCols; ++e) v[e] = 0u;
+      }
       // the scores of this buffer have been read: S of tile j+2 may land
       tc_fence_before();
       __syncwarp();
@@ -479,7 +490,7 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       for (int ch = 0; ch < kTcCols / 32; ++ch) vmask[ch] = fast ? 0xffffffffu : chunk_mask(ch);
       // pass 1: maximum of the valid scaled scores of this half row
       float mx = kNegInfT;
-      if (ok) {
+      if (ok && !idle) {
         if (fast) {
           float mx0 = kNegInfT, mx1 = kNegInfT;
 #pragma unroll
@@ -528,7 +539,8 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       const uint32_t padr = tmem + lanes + kTcPCol + hf * (kTcCols / 2);
 #pragma unroll
       for (int ch = 0; ch < kTcCols / 32; ++ch) {
-        const uint32_t vm = live ? vmask[ch] : 0u;
+        if (idle && j > 0) break;          // zero P rows stay zero
+        const uint32_t vm = (live && !idle) ? vmask[ch] : 0u;
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -701,15 +713,22 @@ cudaError_t launch_tc(const MultiQueryArgs& a, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, []() {
-    attr = cudaFuncSetAttribute(multi_query_tc_kernel<T, D, G>,
+    attr = cudaFuncSetAttribute(multi_query_tc_kernel<T, D, G, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(multi_query_tc_kernel<T, D, G, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
   });
   if (attr != cudaSuccess) return attr;
   const int64_t tiles = ((int64_t)a.max_query_len * G + kTcRows - 1) / kTcRows;
   if (tiles == 0 || a.num_seqs == 0) return cudaSuccess;
   if (tiles * a.num_splits > 0x7fffffffll) return cudaErrorInvalidValue;
   dim3 grid((unsigned)(tiles * a.num_splits), a.num_kv_heads, a.num_seqs);
-  multi_query_tc_kernel<T, D, G><<<grid, kTcThreads, Ly::SMEM, st>>>(a, tq, tk, tv);
+  // runs shorter than one row tile: warps without rows skip their work
+  if ((int64_t)a.max_query_len * G < kTcRows)
+    multi_query_tc_kernel<T, D, G, true><<<grid, kTcThreads, Ly::SMEM, st>>>(a, tq, tk, tv);
+  else
+    multi_query_tc_kernel<T, D, G, false><<<grid, kTcThreads, Ly::SMEM, st>>>(a, tq, tk, tv);
   return cudaGetLastError();
 }
 

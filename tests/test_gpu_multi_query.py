@@ -151,14 +151,17 @@ SHORT = [(dt, D, G, B) for dt in ("bf16", "f16") for D in (64, 128) for G in (1,
          for B in (16,)] + [("bf16", 128, 8, 8), ("bf16", 128, 4, 128), ("f16", 128, 1, 64)]
 
 
+@pytest.mark.parametrize("rows", [16, 32, 96])
 @pytest.mark.parametrize("dtype,D,G,B", SHORT)
-def test_short_runs_column_kernel(dtype, D, G, B):
-    """At most 32 (token, head) columns per sequence and KV head: the
-    column kernel (KV tokens as M), with and without KV partitions."""
-    n_max = max(1, 32 // G)
+def test_short_runs(dtype, D, G, B, rows):
+    """Short runs, with and without KV partitions: at most 16 (token, head)
+    rows per KV head go to the column kernel (KV tokens as M), longer ones to
+    the tcgen05 kernel, whose row tile is then partly empty (warps without a
+    row skip their work)."""
+    n_max = max(1, rows // G)
     n_new = [1, n_max, max(1, n_max // 2), n_max]
     ctx = [0, 17, 700, 1500]
-    b = make_batch(dtype, D, 2 * G, 2, B, ctx, n_new, 900 + 13 * G + D + B)
+    b = make_batch(dtype, D, 2 * G, 2, B, ctx, n_new, 900 + 13 * G + D + B + rows)
     for partition in (0, 128):
         out, want, _ = run_both(b, partition)
         assert torch.isfinite(out.float()).all()
