@@ -1,6 +1,7 @@
-// Causal paged attention for long runs of new tokens (prefill chunks) on the
-// fifth-generation tensor cores: tcgen05.mma with fp32 accumulators, scores
-// and softmax weights in tensor memory (TMEM).
+// Causal paged attention for runs of more than 16 (token, head) rows per KV
+// head (prefill chunks, speculative runs) on the fifth-generation tensor
+// cores: tcgen05.mma with fp32 accumulators, scores and softmax weights in
+// tensor memory (TMEM).
 //
 // What is computed is the multi-query attention of prefill_mma.cu: new token
 // i of sequence s (n_s new tokens, L_s tokens in the pool including them)
@@ -12,28 +13,28 @@
 // One CTA owns 128 rows — (new token, query head) pairs of one KV head,
 // query-major — and walks its causal KV range in tiles of 128 tokens:
 //   * producer warps load the CTA's Q tile once (3-D TMA straight from the
-//     [tokens][heads][D] query tensor) and the K and V tiles into two
-//     separate three-stage rings by 3-D TMA boxes of one 64-column half of
-//     one block's rows (128-byte swizzle); a K stage is released as soon as
-//     S of its tile is computed, a V stage when P V is;
+//     [tokens][heads][D] query tensor) and the K and V tiles by 3-D TMA
+//     boxes of one 64-column half of one block's rows (128-byte swizzle),
+//     into a three-stage K ring and a two-stage V ring; a K stage is
+//     released as soon as S of its tile is computed, a V stage when P V is;
 //   * one thread of the MMA warp issues S = Q K^T (M = 128 rows, N = 128
 //     tokens, K = D; both operands in shared memory) into one of two TMEM
-//     score buffers, and O += P V (M = 128, N = D, K = 128 tokens) with P
-//     read from TMEM and V read N-major straight from its token rows; each
-//     completes on an mbarrier (tcgen05.commit);
+//     score buffers, two tiles ahead, and [O | l] += P [V | 1] (M = 128,
+//     N = D + 16, K = 128 tokens) with P read from TMEM and V read N-major
+//     straight from its token rows; each V stage carries a constant group
+//     of ones after the head dims, so column D of the output holds the row
+//     sums of exactly the rounded weights; each group of MMAs completes on
+//     an mbarrier (tcgen05.commit);
 //   * eight softmax warps, two warpgroups, own half a row each per thread
 //     (TMEM lane = row; warpgroup h takes score columns 64h .. 64h+63): they
 //     read the scores with tcgen05.ld, apply the causal limit and the scale
 //     in the log2 domain, exchange the two half-row maxima through shared
-//     memory, and write P (16-bit) over the scores they came from with
-//     tcgen05.st. Each V stage carries a constant group of ones after the
-//     head dims, so the P V MMA also produces the row sums of exactly the
-//     rounded weights. Output and sums in TMEM are rescaled only when a
-//     row's running maximum grew by more than 2^8 (the weights stay below
-//     256, and the final division uses the same reference).
+//     memory, and write P (16-bit) to the TMEM P buffer with tcgen05.st.
+//     Output and sums in TMEM are rescaled only when a row's running
+//     maximum grew by more than 2^8 (the weights stay below 256, and the
+//     final division uses the same reference).
 // Keeping S and P out of shared memory leaves its bandwidth to the K/V
-// operands and their TMA loads. S of tile j+1 is computed while the softmax
-// warps work on tile j.
+// operands and their TMA loads.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -130,19 +131,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// two fp32 weights packed to the 16-bit input type (round to nearest), and
-// the rounded values
+// two fp32 values packed to the 16-bit input type (round to nearest)
 template <typename T>
 struct Pack2;
 template <>
 struct Pack2<__nv_bfloat16> {
-  __device__ __forceinline__ static uint32_t pack(float a, float b, float& ra, float& rb) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    const uint32_t u = *reinterpret_cast<uint32_t*>(&h);
-    ra = __uint_as_float(u << 16);
-    rb = __uint_as_float(u & 0xffff0000u);
-    return u;
-  }
   __device__ __forceinline__ static uint32_t pack_out(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -150,13 +143,6 @@ struct Pack2<__nv_bfloat16> {
 };
 template <>
 struct Pack2<__half> {
-  __device__ __forceinline__ static uint32_t pack(float a, float b, float& ra, float& rb) {
-    __half2 h = __floats2half2_rn(a, b);
-    const float2 f = __half22float2(h);
-    ra = f.x;
-    rb = f.y;
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
   __device__ __forceinline__ static uint32_t pack_out(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
