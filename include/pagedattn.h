@@ -395,6 +395,21 @@ PA_API int pa_map_to_kernel_blocks(const int32_t* manager_table, int64_t num_row
                                    int64_t kernel_stride, void* stream);
 
 /*
+ * pa_selftest_bounded_wait — exercises the bounded mbarrier wait that every
+ * asynchronous kernel of this library relies on (no counterpart on the
+ * pages; a failure-detection check). One CTA waits on a barrier phase that
+ * nothing completes: warp 0 with a limit of timeout_cycles SM clocks, warp 1
+ * with a 1000x longer one. Warp 0 must give up and raise the CTA's abort
+ * flag, and warp 1 must leave through that flag. The kernel writes, to the
+ * caller's device buffer status[3] (int32): status[0], status[1] =
+ * PA_ERR_TIMEOUT for each warp that gave up (PA_OK if its wait completed),
+ * status[2] = the abort flag (1). Nothing faults and both waits end by
+ * themselves; the context stays usable. 0 < timeout_cycles <= 2^40/1000,
+ * else PA_ERR_SHAPE; NULL status is PA_ERR_NULL. Asynchronous on stream.
+ */
+PA_API int pa_selftest_bounded_wait(int* status, long long timeout_cycles, void* stream);
+
+/*
  * Read (and clear) the device-side error word that the kernels latch on bad
  * indices. Synchronises `stream` first. *code_out receives PA_OK or the
  * first latched error (PA_ERR_OUT_OF_RANGE). The word is per device and

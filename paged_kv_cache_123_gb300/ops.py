@@ -331,3 +331,13 @@ def pa_decode_attention_fp8_window(q: torch.Tensor, key_cache: torch.Tensor,
     return _window_call("pa_decode_attention_fp8_window", q, key_cache, value_cache,
                         block_tables, seq_lens, scale, num_kv_heads, (k_scale, v_scale),
                         window, out, max_seq_len, partition_size, workspace, stream)
+
+
+def pa_selftest_bounded_wait(timeout_cycles: int = 2_000_000, stream=None) -> list:
+    """Run the bounded-wait self-test; returns [status of warp 0, status of
+    warp 1, abort flag] (expected: [PA_ERR_TIMEOUT, PA_ERR_TIMEOUT, 1])."""
+    status = torch.full((3,), 12345, dtype=torch.int32, device="cuda")
+    check("pa_selftest_bounded_wait", lib().pa_selftest_bounded_wait(
+        ptr(status), int(timeout_cycles), stream_handle(stream)))
+    torch.cuda.synchronize()
+    return status.cpu().tolist()
