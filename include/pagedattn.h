@@ -324,6 +324,19 @@ PA_API int pa_decode_attention_fp8(const void* q, const void* key_cache,
  * Other arguments, layouts and errors as in the unwindowed calls; window < 0
  * is PA_ERR_SHAPE.
  */
+/*
+ * pa_decode_window_partitioning — pa_decode_partitioning for the windowed
+ * calls with the same arguments. When 0 < window < max_seq_len every
+ * sequence at least window long covers window .. window + 63 tokens (the
+ * window's first tile is read whole), so with partition_size == 0 the
+ * partitions are sized for one wave of resident CTAs (the most splits per
+ * (sequence, KV head) pair that still fit, at least 256 tokens each) rather
+ * than the two waves of the unwindowed calls. window < 0 is PA_ERR_SHAPE.
+ */
+PA_API int pa_decode_window_partitioning(int num_seqs, int num_q_heads, int num_kv_heads,
+                                         int block_size, int max_seq_len, int window,
+                                         int partition_size, int* num_splits_out,
+                                         int* partition_tokens_out);
 PA_API int64_t pa_decode_window_workspace_bytes(int num_seqs, int num_q_heads,
                                                 int num_kv_heads, int head_size,
                                                 int block_size, int max_seq_len, int window,

@@ -72,9 +72,16 @@ int check_launch(cudaError_t e) {
 // per SM) and 512 for the CUDA-core kernel (many small CTAs per SM, where
 // shorter partitions even out ragged lengths). Both caps were the fastest of
 // 512..4096 on the Llama-7B and GQA batches on GB300.
+// uniform = every long sequence covers about max_seq_len tokens (a sliding
+// window shorter than the longest sequence): equal work per (sequence, KV
+// head), so the partitions are sized for ONE wave of resident CTAs — the
+// most splits per pair that still fit — instead of two; a second, partial
+// wave would run a few CTAs alone at a fraction of the bandwidth
+// (longctx-shaped window of 4096: 0.68 -> 0.80 of the copy bandwidth; a
+// 333-token window over the Llama-7B batch: 0.85 -> 0.92).
 void partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
-                  int max_seq_len, int partition_size, int sm_count, int* splits,
-                  int* tokens) {
+                  int max_seq_len, int partition_size, int sm_count, bool uniform,
+                  int* splits, int* tokens) {
   const int64_t tile = block_size > 64 ? block_size : 64;
   const int64_t len = max_seq_len > 0 ? max_seq_len : 1;
   auto round_up = [tile](int64_t x) { return (x + tile - 1) / tile * tile; };
@@ -86,12 +93,19 @@ void partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_siz
     const bool tc = g >= 2 && block_size >= 8;
     const int64_t per_sm = tc ? 2 : 8;
     const int64_t cap = round_up(tc ? 2048 : 512);
-    const int64_t pairs = (int64_t)num_seqs * num_kv_heads;
-    const int64_t target = 2 * (int64_t)sm_count * per_sm;
-    P = round_up((len * (pairs > 0 ? pairs : 1) + target - 1) / target);
+    const int64_t pairs = num_seqs > 0 ? (int64_t)num_seqs * num_kv_heads : 1;
     const int64_t floor_p = round_up(256);
-    if (P < floor_p) P = floor_p;
-    if (P > cap) P = cap;
+    if (uniform) {
+      int64_t k = (int64_t)sm_count * per_sm / pairs;   // splits per pair in one wave
+      if (k < 1) k = 1;
+      P = round_up((len + k - 1) / k);
+      if (P < floor_p) P = floor_p;
+    } else {
+      const int64_t target = 2 * (int64_t)sm_count * per_sm;
+      P = round_up((len * pairs + target - 1) / target);
+      if (P < floor_p) P = floor_p;
+      if (P > cap) P = cap;
+    }
   }
   if (P > len) P = round_up(len);
   if (P > (int64_t)1 << 30) P = (int64_t)1 << 30;
@@ -116,6 +130,14 @@ int covered_len(int max_seq_len, int window) {
   return std::min<int64_t>(max_seq_len, (int64_t)window + 63);
 }
 
+// A window that cuts the longest sequence: every sequence at least that long
+// covers window .. window + 63 tokens.
+bool windowed(int max_seq_len, int window) { return window > 0 && window < max_seq_len; }
+
+int decode_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
+                        int max_seq_len, int window, int partition_size, int* splits,
+                        int* tokens);
+
 // Validation, partitioning and launch shared by the decode entry points
 // (16-bit/fp32 pools or E4M3 pools, with or without a window).
 int run_decode(const void* q, const void* key_cache, const void* value_cache,
@@ -136,6 +158,27 @@ int check_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head
   const int g = num_q_heads / num_kv_heads;
   if (g != 1 && g != 2 && g != 4 && g != 8) return PA_ERR_SHAPE;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_SHAPE;
+  return PA_OK;
+}
+
+// Partitioning of a decode call over max_seq_len (and a window, 0 = none),
+// with the device's SM count.
+int decode_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
+                        int max_seq_len, int window, int partition_size, int* splits,
+                        int* tokens) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 ||
+      num_q_heads % num_kv_heads != 0 || !pow2(block_size) || block_size > 256 ||
+      max_seq_len < 0 || partition_size < 0 || window < 0)
+    return PA_ERR_SHAPE;
+  int dev;
+  int st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  int sp, tk;
+  partitioning(num_seqs, num_q_heads, num_kv_heads, block_size,
+               covered_len(max_seq_len, window), partition_size, g_sm_count[dev],
+               windowed(max_seq_len, window), &sp, &tk);
+  if (splits) *splits = sp;
+  if (tokens) *tokens = tk;
   return PA_OK;
 }
 
@@ -205,19 +248,17 @@ int pa_reshape_and_cache(const void* k, const void* v, int64_t num_tokens,
 int pa_decode_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
                            int max_seq_len, int partition_size,
                            int* num_splits_out, int* partition_tokens_out) {
-  if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 ||
-      num_q_heads % num_kv_heads != 0 || !pow2(block_size) || block_size > 256 ||
-      max_seq_len < 0 || partition_size < 0)
-    return PA_ERR_SHAPE;
-  int dev;
-  int st = device_setup(&dev);
-  if (st != PA_OK) return st;
-  int splits, tokens;
-  partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size,
-               g_sm_count[dev], &splits, &tokens);
-  if (num_splits_out) *num_splits_out = splits;
-  if (partition_tokens_out) *partition_tokens_out = tokens;
-  return PA_OK;
+  return decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, 0,
+                             partition_size, num_splits_out, partition_tokens_out);
+}
+
+int pa_decode_window_partitioning(int num_seqs, int num_q_heads, int num_kv_heads,
+                                  int block_size, int max_seq_len, int window,
+                                  int partition_size, int* num_splits_out,
+                                  int* partition_tokens_out) {
+  if (window < 0) return PA_ERR_SHAPE;
+  return decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len,
+                             window, partition_size, num_splits_out, partition_tokens_out);
 }
 
 int64_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
@@ -228,8 +269,8 @@ int64_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
   if (st != PA_OK) return st;
   if (partition_size < 0) return PA_ERR_SHAPE;
   int splits, tokens;
-  st = pa_decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len,
-                              partition_size, &splits, &tokens);
+  st = decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, 0,
+                           partition_size, &splits, &tokens);
   if (st != PA_OK) return st;
   return workspace_for(num_seqs, num_q_heads, head_size, splits);
 }
@@ -254,8 +295,12 @@ int64_t pa_decode_window_workspace_bytes(int num_seqs, int num_q_heads, int num_
   int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size,
                               block_size, max_seq_len);
   if (st != PA_OK) return st;
-  return pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
-                                   covered_len(max_seq_len, window), partition_size);
+  if (partition_size < 0) return PA_ERR_SHAPE;
+  int splits, tokens;
+  st = decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, window,
+                           partition_size, &splits, &tokens);
+  if (st != PA_OK) return st;
+  return workspace_for(num_seqs, num_q_heads, head_size, splits);
 }
 
 int pa_decode_attention_window(const void* q, const void* key_cache, const void* value_cache,
@@ -526,7 +571,7 @@ int run_decode(const void* q, const void* key_cache, const void* value_cache,
   a.dtype = dtype; a.scale = scale; a.max_seq_len = max_seq_len; a.window = window;
   partitioning(num_seqs, num_q_heads, num_kv_heads, block_size,
                covered_len(max_seq_len, window), partition_size, g_sm_count[dev],
-               &a.num_splits, &a.partition);
+               windowed(max_seq_len, window), &a.num_splits, &a.partition);
   const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);
   a.ws_acc = nullptr; a.ws_ml = nullptr;
   if (need > 0) {

@@ -81,6 +81,17 @@ def pa_decode_partitioning(num_seqs: int, num_q_heads: int, num_kv_heads: int,
     return s.value, p.value
 
 
+def pa_decode_window_partitioning(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                  block_size: int, max_seq_len: int, window: int,
+                                  partition_size: int = 0):
+    """(num_splits, partition_tokens) the windowed attention calls will use."""
+    s, p = ctypes.c_int(0), ctypes.c_int(0)
+    check("pa_decode_window_partitioning", lib().pa_decode_window_partitioning(
+        num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, window, partition_size,
+        ctypes.byref(s), ctypes.byref(p)))
+    return s.value, p.value
+
+
 def pa_decode_attention(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
                         block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
                         num_kv_heads: int, out: Optional[torch.Tensor] = None, *,

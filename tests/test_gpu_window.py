@@ -98,6 +98,21 @@ def test_window_workspace_and_argument_errors():
     assert pa.pa_decode_window_workspace_bytes(64, 64, 8, 128, 16, 32768, 0, 0) == n_full
     with pytest.raises(pa.PagedAttnError):
         pa.pa_decode_window_workspace_bytes(64, 64, 8, 128, 16, 32768, -1, 0)
+    # a window shorter than the longest sequence: one wave of resident CTAs
+    # (two per SM for this tensor-core shape), partitions of >= 256 tokens
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    splits, tok = pa.pa_decode_window_partitioning(16, 32, 8, 16, 32768, 4096, 0)
+    assert 16 * 8 * splits <= 2 * sms and splits * tok >= 4096 + 63 and tok % 64 == 0
+    assert (splits - 1) * tok < 4096 + 63
+    assert pa.pa_decode_window_workspace_bytes(16, 32, 8, 128, 16, 32768, 4096, 0) == (
+        0 if splits == 1 else 16 * 32 * splits * (128 * 4 + 8))
+    # no window, or one covering every sequence: the unwindowed partitioning
+    for W in (0, 32768, 40000):
+        assert pa.pa_decode_window_partitioning(16, 32, 8, 16, 32768, W, 0) == \
+            pa.pa_decode_partitioning(16, 32, 8, 16, 32768, 0)
+    assert pa.pa_decode_window_partitioning(16, 32, 8, 16, 32768, 4096, 1000) == (5, 1024)
+    with pytest.raises(pa.PagedAttnError):
+        pa.pa_decode_window_partitioning(16, 32, 8, 16, 32768, -1, 0)
     cfg = workloads.DecodeConfig("we", 2, 8, 2, 128, 16, "bf16", seed=1)
     inp = workloads.make_decode_inputs(cfg, context_lens=[10, 20])
     with pytest.raises(pa.PagedAttnError):
