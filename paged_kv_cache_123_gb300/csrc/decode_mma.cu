@@ -244,10 +244,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
           for (int ks = 0; ks < KSTEPS; ++ks) {
             uint32_t af[4];
-            af[0] = e4m3x2_to_f16x2(wa[ks] & 0xffffu);
-            af[1] = e4m3x2_to_f16x2(wb[ks] & 0xffffu);
-            af[2] = e4m3x2_to_f16x2(wa[ks] >> 16);
-            af[3] = e4m3x2_to_f16x2(wb[ks] >> 16);
+            e4m3x4_to_f16x2x2(wa[ks], af[0], af[2]);
+            e4m3x4_to_f16x2x2(wb[ks], af[1], af[3]);
             MmaOps<MT>::mma(sacc, af, qf[ks][0], qf[ks][1]);
           }
         } else {
@@ -304,10 +302,15 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int row = warp * 16 + 2 * c + (r & 1) + (r >> 1) * 8;
-            const bool rok = (okm >> (row - warp * 16)) & 1u;
             const uint4 v = *reinterpret_cast<const uint4*>(vbase + row * 128 + ((n ^ (row & 7)) << 4));
-            w[r][0] = rok ? v.x : 0u; w[r][1] = rok ? v.y : 0u;
-            w[r][2] = rok ? v.z : 0u; w[r][3] = rok ? v.w : 0u;
+            w[r][0] = v.x; w[r][1] = v.y; w[r][2] = v.z; w[r][3] = v.w;
+          }
+          if (okm != 0xffffu) {   // warp-uniform: only partial tiles pay the masking
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              if (!((okm >> (2 * c + (r & 1) + (r >> 1) * 8)) & 1u))
+                w[r][0] = w[r][1] = w[r][2] = w[r][3] = 0u;
+            }
           }
           uint32_t p01[16], p23[16];      // (token pair, head dim j) as f16x2
 #pragma unroll
@@ -316,14 +319,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
             const uint32_t hi01 = __byte_perm(w[0][q4], w[1][q4], 0x7362);
             const uint32_t lo23 = __byte_perm(w[2][q4], w[3][q4], 0x5140);
             const uint32_t hi23 = __byte_perm(w[2][q4], w[3][q4], 0x7362);
-            p01[4 * q4 + 0] = e4m3x2_to_f16x2(lo01 & 0xffffu);
-            p01[4 * q4 + 1] = e4m3x2_to_f16x2(lo01 >> 16);
-            p01[4 * q4 + 2] = e4m3x2_to_f16x2(hi01 & 0xffffu);
-            p01[4 * q4 + 3] = e4m3x2_to_f16x2(hi01 >> 16);
-            p23[4 * q4 + 0] = e4m3x2_to_f16x2(lo23 & 0xffffu);
-            p23[4 * q4 + 1] = e4m3x2_to_f16x2(lo23 >> 16);
-            p23[4 * q4 + 2] = e4m3x2_to_f16x2(hi23 & 0xffffu);
-            p23[4 * q4 + 3] = e4m3x2_to_f16x2(hi23 >> 16);
+            e4m3x4_to_f16x2x2(lo01, p01[4 * q4 + 0], p01[4 * q4 + 1]);
+            e4m3x4_to_f16x2x2(hi01, p01[4 * q4 + 2], p01[4 * q4 + 3]);
+            e4m3x4_to_f16x2x2(lo23, p23[4 * q4 + 0], p23[4 * q4 + 1]);
+            e4m3x4_to_f16x2x2(hi23, p23[4 * q4 + 2], p23[4 * q4 + 3]);
           }
 #pragma unroll
           for (int mt = 0; mt < KSTEPS; ++mt) {

@@ -16,6 +16,7 @@
 
 #include "common.cuh"
 #include "launchers.h"
+#include "mma_util.cuh"
 
 namespace pa {
 
@@ -44,11 +45,11 @@ __device__ __forceinline__ void e4m3x8_to_f32(uint2 u, float* f) {
   const uint32_t w[2] = {u.x, u.y};
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
+    uint32_t h[2];
+    e4m3x4_to_f16x2x2(w[i], h[0], h[1]);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[i] >> (16 * j)) & 0xffffu);
-      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
-      const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+      const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h[j]));
       f[4 * i + 2 * j] = v.x;
       f[4 * i + 2 * j + 1] = v.y;
     }

@@ -85,31 +85,6 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int dch) {
 
 namespace pa {
 
-// 16 E4M3 codes -> 16 values of T (f16 or bf16), exactly (every E4M3 value
-// is representable in both), as two 16-byte words of 8 values.
-template <typename T>
-__device__ __forceinline__ void widen_e4m3x16(const uint4 codes, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[i] >> (16 * j)) & 0xffffu);
-      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
-      uint32_t bits = (uint32_t)hr.x | ((uint32_t)hr.y << 16);
-      if constexpr (!std::is_same<T, __half>::value) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&bits));
-        const __nv_bfloat162 b = __float22bfloat162_rn(f);
-        bits = *reinterpret_cast<const uint32_t*>(&b);
-      }
-      o[2 * i + j] = bits;
-    }
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
 }  // namespace pa
 
 namespace pa {
@@ -130,10 +105,17 @@ __device__ __forceinline__ uint32_t to_mma_pair(uint32_t v) {
 
 namespace pa {
 
-// Two E4M3 codes (low byte first) -> an fp16 pair, exactly.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-  return (uint32_t)hr.x | ((uint32_t)hr.y << 16);
+// Four E4M3 codes (one 32-bit word, lowest byte first) -> two fp16 pairs,
+// exactly (every E4M3 value is an fp16 value): lo holds bytes 0 and 1 (byte 0
+// in the low half), hi bytes 2 and 3. One PTX conversion per 16-bit half of
+// the word, with no masking, shifting or repacking around it.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 c0, c1;\n\t"
+      "mov.b32 {c0, c1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, c0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 }  // namespace pa
