@@ -11,7 +11,7 @@
 //
 // Data movement: a producer warp walks the partition's block table and issues
 // one 4-D tiled TMA load (cp.async.bulk.tensor) per block (up to 64 whole
-// token rows, one contiguous run in HBM) for K and for V into a 3-stage ring
+// token rows, one contiguous run in HBM) for K and for V into a 3-stage ring (4 stages for fp8 pools)
 // of 64-token tiles, with the 128-byte swizzle so ldmatrix reads hit at most
 // two rows per bank group. Four
 // consumer warps take 16 tokens of each tile each, keep their own running
@@ -36,7 +36,11 @@ namespace pa {
 constexpr int kMmaConsumers = 4;
 constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
 constexpr int kTile = 64;
-constexpr int kStages = 3;
+// stages of the K/V ring: four for fp8 pools (16 KB stages, three CTAs per
+// SM: 192 KB in flight per SM, as the 16-bit ring's three 32 KB stages at two
+// CTAs per SM), three for 16-bit pools
+template <bool KV8>
+constexpr int ring_stages() { return KV8 ? 4 : 3; }
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 #define kNegInfM (-__int_as_float(0x7f800000))
 
@@ -60,6 +64,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   constexpr int KV_BYTES = kTile * IN_ROW;       // K (or V) part of a stage
   constexpr int STAGE_BYTES = 2 * KV_BYTES;
   constexpr int PRIV_BYTES = 0;
+  constexpr int kSt = ring_stages<KV8>();
   static_assert(!KV8 || D == 128, "fp8 pools: head size 128 (one 128-byte line per row)");
   // fp8 pools run the products in fp16 whatever the query type: codes widen
   // to fp16 in one conversion, and bf16 queries of ordinary magnitude
@@ -71,16 +76,16 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * STAGE_BYTES +
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSt * STAGE_BYTES +
                                                 kMmaConsumers * PRIV_BYTES);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kSt);
   // bit p set = piece p of the stage's tile was loaded (written by the
   // producer before it arms the stage's full barrier)
-  unsigned* tile_mask = reinterpret_cast<unsigned*>(bars + 2 * kStages) + 1;
+  unsigned* tile_mask = reinterpret_cast<unsigned*>(bars + 2 * kSt) + 1;
   const uint32_t smem0 = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int st) { return bar0 + 8u * st; };
-  auto empty_bar = [&](int st) { return bar0 + 8u * (kStages + st); };
+  auto empty_bar = [&](int st) { return bar0 + 8u * (kSt + st); };
 
   const int s = blockIdx.z, kvh = blockIdx.y, split = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -109,7 +114,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   const int32_t* trow = a.tables + (int64_t)s * a.table_stride;
 
   if (threadIdx.x == 0) {
-    for (int st = 0; st < kStages; ++st) {
+    for (int st = 0; st < kSt; ++st) {
       mbar_init(full_bar(st), 1);
       mbar_init(empty_bar(st), kMmaConsumers);
     }
@@ -135,7 +140,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     const int npieces = kTile / R;             // <= 8 (R >= 8)
     int issued = 0;
     for (int i = 0; i < ntiles; ++i) {
-      const int st = i % kStages;
+      const int st = i % kSt;
       const int ts = t0 + i * kTile;
       const int te = min(t1, ts + kTile);
       const int tok = ts + lane * R;
@@ -149,8 +154,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       const unsigned pm = __ballot_sync(0xffffffffu, mine);
       int ok = 1;
       if (lane == 0) {
-        if (i >= kStages)
-          ok = mbar_wait_bounded(empty_bar(st), ((i / kStages) - 1) & 1, abort_flag, kWaitCycles);
+        if (i >= kSt)
+          ok = mbar_wait_bounded(empty_bar(st), ((i / kSt) - 1) & 1, abort_flag, kWaitCycles);
         if (ok) {
           tile_mask[st] = pm;
           mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * IN_ROW);
@@ -175,8 +180,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     }
     // let the loads this CTA issued land before it can leave
     if (lane == 0)
-      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-        mbar_wait_bounded(full_bar(j % kStages), (j / kStages) & 1, abort_flag, kWaitCycles);
+      for (int j = issued > kSt ? issued - kSt : 0; j < issued; ++j)
+        mbar_wait_bounded(full_bar(j % kSt), (j / kSt) & 1, abort_flag, kWaitCycles);
   } else {
     // ---------------- consumers
     const int n = lane >> 2, c = lane & 3;
@@ -200,8 +205,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     }
     const float sl2 = a.scale * kLog2e * k_scale;
     for (int i = 0; i < ntiles; ++i) {
-      const int st = i % kStages;
-      if (!mbar_wait_bounded(full_bar(st), (i / kStages) & 1, abort_flag, kWaitCycles)) break;
+      const int st = i % kSt;
+      if (!mbar_wait_bounded(full_bar(st), (i / kSt) & 1, abort_flag, kWaitCycles)) break;
       const int ts = t0 + i * kTile;
       const int te = min(t1, ts + kTile);
       const int r0 = ts + warp * 16;   // first token of this warp's 16 rows
@@ -468,7 +473,8 @@ bool encode_pool_map_fp8(CUtensorMap* map, const void* base, const DecodeArgs& a
 
 template <int D, bool KV8>
 constexpr int mma_smem_bytes() {
-  return 1024 + kStages * 2 * kTile * (KV8 ? D : 2 * D) + 2 * kStages * 8 + 4 + 4 * kStages +
+  constexpr int kSt = ring_stages<KV8>();
+  return 1024 + kSt * 2 * kTile * (KV8 ? D : 2 * D) + 2 * kSt * 8 + 4 + 4 * kSt +
          16;
 }
 
@@ -481,7 +487,7 @@ cudaError_t launch_mma_tdg(const DecodeArgs& a, float ks, float vs, cudaStream_t
                          encode_pool_map(&tv, a.vc, MmaOps<T>::kTmaType, a));
   if (!ok) return cudaErrorInvalidValue;
   constexpr int smem = mma_smem_bytes<D, KV8>();
-  static_assert(kStages * 2 * kTile * (KV8 ? D : 2 * D) >=
+  static_assert(ring_stages<KV8>() * 2 * kTile * (KV8 ? D : 2 * D) >=
                     kMmaConsumers * 8 * D * 4 + 2 * kMmaConsumers * 8 * 4,
                 "merge area must fit in the stage ring");
   static std::once_flag attr_once;
