@@ -19,20 +19,23 @@
 //     released as soon as S of its tile is computed, a V stage when P V is;
 //   * one thread of the MMA warp issues S = Q K^T (M = 128 rows, N = 128
 //     tokens, K = D; both operands in shared memory) into one of two TMEM
-//     score buffers, two tiles ahead, and [O | l] += P [V | 1] (M = 128,
-//     N = D + 16, K = 128 tokens) with P read from TMEM and V read N-major
-//     straight from its token rows; each V stage carries a constant group
-//     of ones after the head dims, so column D of the output holds the row
-//     sums of exactly the rounded weights; each group of MMAs completes on
-//     an mbarrier (tcgen05.commit);
+//     score buffers and [O | l] += P [V | 1] (M = 128, N = D + 16, K = 128
+//     tokens) with P read from TMEM and V read N-major straight from its
+//     token rows; each V stage carries a constant group of ones after the
+//     head dims, so column D of the output holds the row sums of exactly
+//     the rounded weights; each group of MMAs completes on an mbarrier
+//     (tcgen05.commit). P of tile j lives in score buffer j&1, so S of tile
+//     j+2 follows the completion of P V of tile j, while the softmax warps
+//     work on tile j+1;
 //   * eight softmax warps, two warpgroups, own half a row each per thread
 //     (TMEM lane = row; warpgroup h takes score columns 64h .. 64h+63): they
 //     read the scores with tcgen05.ld, apply the causal limit and the scale
 //     in the log2 domain, exchange the two half-row maxima through shared
-//     memory, and write P (16-bit) to the TMEM P buffer with tcgen05.st.
+//     memory, and write P (16-bit) over their own scores with tcgen05.st.
 //     Output and sums in TMEM are rescaled only when a row's running
 //     maximum grew by more than 2^8 (the weights stay below 256, and the
-//     final division uses the same reference).
+//     final division uses the same reference); only then does a softmax
+//     warp wait for the previous tile's P V.
 // Keeping S and P out of shared memory leaves its bandwidth to the K/V
 // operands and their TMA loads.
 #include <cudaTypedefs.h>
@@ -58,11 +61,12 @@ constexpr int kTcMmaWarp = 9;
 constexpr int kTcVProducerWarp = 10;      // V tiles
 constexpr int kTcThreads = 11 * 32;
 constexpr int kTcCols = kTcKv / 2;        // score columns per softmax thread
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D) and the row sums l
-// in column 256+D (the ones group of V, 16 columns), P [400, 464)
+// TMEM columns: score buffers S0 [0,128) and S1 [128,256), O [256, 256+D)
+// and the row sums l in column 256+D (the ones group of V, 16 columns). The
+// 16-bit weights P of tile j overwrite the scores of their own half row in
+// buffer j&1 (half h: columns 64h .. 64h+31 of the buffer)
 constexpr uint32_t kTcTmemCols = 512;
 constexpr uint32_t kTcOCol = 256;
-constexpr uint32_t kTcPCol = 400;
 constexpr long long kTcWaitCycles = 4000000000LL;
 constexpr float kTcRescaleLog2 = 8.f;
 #define kNegInfT (-__int_as_float(0x7f800000))
@@ -81,9 +85,9 @@ struct TcLayout {
   // of 16-bit ones: P x [V | 1] also gives the row sums of the weights
   static constexpr int V_STAGE = KV_BYTES + KV_HALF;
   static constexpr int BAR_OFF = V_OFF + kTcVStages * V_STAGE;
-  // q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], s_free[2],
-  // p_full, o_done, done
-  static constexpr int NBARS = 20;
+  // q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], p_full,
+  // o_done, done
+  static constexpr int NBARS = 18;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;     // tmem base, abort flag
   // row maxima and row sums exchanged between the two softmax warpgroups
   static constexpr int XCH_OFF = MISC_OFF + 32;            // float [2][128]
@@ -93,7 +97,7 @@ struct TcLayout {
 
 enum : int {
   kBarQ = 0, kBarKFull = 1, kBarKEmpty = 4, kBarVFull = 7, kBarVEmpty = 10,
-  kBarSFull = 13, kBarSFree = 15, kBarPFull = 17, kBarODone = 18, kBarDone = 19
+  kBarSFull = 13, kBarPFull = 15, kBarODone = 16, kBarDone = 17
 };
 
 // max of three floats (one instruction)
@@ -232,9 +236,10 @@ __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
   }
 }
 
-// MMA issue (one thread): S_j = Q K_j^T into TMEM score buffer j&1, two
-// tiles ahead, and [O | l] += P_j [V_j | 1] (P from TMEM) once the softmax
-// warps have written P_j.
+// MMA issue (one thread): S_j = Q K_j^T into TMEM score buffer j&1, and
+// [O | l] += P_j [V_j | 1] (P_j from the same buffer) once the softmax warps
+// have written P_j. S_{j+2} reuses the buffer, so it is issued once P_j V_j
+// has completed; S_{j+1} is already in place for the softmax warps.
 template <typename T, int D>
 __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
                          volatile int* abort_flag) {
@@ -251,27 +256,26 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
       return false;
     tc_fence_after();
     const uint32_t vb = s0 + Ly::V_OFF + vs * Ly::V_STAGE;
-    const uint32_t pt = tmem + kTcPCol;
+    const uint32_t pt = tmem + (uint32_t)(t & 1) * kTcKv;
 #pragma unroll
     for (int ks = 0; ks < kTcKv / 16; ++ks) {
       // [V | 1] tile: token rows of 64 columns per 128-byte line (N-major);
-      // 16 tokens per k-step, the next 64-column group at KV_HALF
+      // 16 tokens per k-step, the next 64-column group at KV_HALF. P of
+      // tokens 16 ks .. 16 ks + 15: half ks / 4 of the row, 8 columns
       const uint64_t bd = smem_desc_sw128(vb + ks * 2048, Ly::KV_HALF, 1024);
-      mma_f16_ts(tmem + kTcOCol, pt + ks * 8, bd, idO, (t > 0 || ks > 0) ? 1u : 0u);
+      mma_f16_ts(tmem + kTcOCol, pt + (ks >> 2) * kTcCols + (ks & 3) * 8, bd, idO,
+                 (t > 0 || ks > 0) ? 1u : 0u);
     }
     mma_commit(bar + 8u * kBarODone);
     mma_commit(bar + 8u * (kBarVEmpty + vs));
     return true;
   };
-  // S_t into score buffer t&1 once K_t has landed and the softmax warps
-  // have read S_{t-2} from that buffer
+  // S_t into score buffer t&1 once K_t has landed (the caller has seen
+  // P_{t-2} V_{t-2} complete, so nothing reads the buffer any more)
   auto issue_s = [&](int t) -> bool {
     const int sb = t & 1, ks_ = t % kTcStages;
     if (!mbar_wait_bounded(bar + 8u * (kBarKFull + ks_), (t / kTcStages) & 1, abort_flag,
                            kTcWaitCycles))
-      return false;
-    if (t >= 2 && !mbar_wait_bounded(bar + 8u * (kBarSFree + sb), ((t >> 1) - 1) & 1,
-                                      abort_flag, kTcWaitCycles))
       return false;
     tc_fence_after();
     const uint32_t kb = s0 + Ly::K_OFF + ks_ * Ly::KV_BYTES;
@@ -285,14 +289,15 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
     mma_commit(bar + 8u * (kBarKEmpty + ks_));
     return true;
   };
-  // S runs two tiles ahead: S_{j+2} is issued as soon as the softmax warps
-  // have read S_j, before P V of tile j, so the scores of the next tiles are
-  // ready when the softmax warps get to them
+  // the softmax warps work on tile j+1 while P_j V_j and then S_{j+2} run
   bool ok = mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
   for (int t = 0; ok && t < 2 && t < ntiles; ++t) ok = issue_s(t);
   for (int j = 0; ok && j < ntiles; ++j) {
-    if (j + 2 < ntiles) ok = issue_s(j + 2);
-    if (ok) ok = issue_pv(j);
+    ok = issue_pv(j);
+    if (ok && j + 2 < ntiles) {
+      ok = mbar_wait_bounded(bar + 8u * kBarODone, j & 1, abort_flag, kTcWaitCycles);
+      if (ok) ok = issue_s(j + 2);
+    }
   }
   // every MMA issued above has completed once this barrier fires
   mma_commit(bar + 8u * kBarDone);
@@ -346,10 +351,7 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       mbar_init(bar + 8u * (kBarVFull + i), 1);
       mbar_init(bar + 8u * (kBarVEmpty + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar + 8u * (kBarSFull + i), 1);
-      mbar_init(bar + 8u * (kBarSFree + i), kTcSoftmaxWarps);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(bar + 8u * (kBarSFull + i), 1);
     mbar_init(bar + 8u * kBarPFull, kTcSoftmaxWarps);
     mbar_init(bar + 8u * kBarODone, 1);
     mbar_init(bar + 8u * kBarDone, 1);
@@ -467,10 +469,6 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
 #pragma unroll
         for (int e = 0; e < kTcCols; ++e) v[e] = 0u;
       }
-      // the scores of this buffer have been read: S of tile j+2 may land
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar + 8u * (kBarSFree + sb));
       uint32_t vmask[kTcCols / 32];
 #pragma unroll
       for (int ch = 0; ch < kTcCols / 32; ++ch) vmask[ch] = fast ? 0xffffffffu : chunk_mask(ch);
@@ -509,25 +507,25 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
         resc = true;
         m_use = m_new;
       }
-      // P V of tile j-1 has read the P buffer and finished adding to the
-      // output once o_done shows it (P V of tile j-2 completed before this
-      // warp's previous tile wrote P, so the phase is current)
-      if (j >= 1) {
-        ok = mbar_wait_bounded(bar + 8u * kBarODone, (j - 1) & 1, abort_flag, kTcWaitCycles);
-        ok = __all_sync(0xffffffffu, ok);
-        tc_fence_after();
-      }
       // pass 2: P = 2^(x - m_use) rounded to the input type, 16 columns of
-      // packed pairs per 32 scores, into the TMEM P buffer (tokens 64 hf ..
-      // at column 32 hf); the row sums come from the MMA's ones group
+      // packed pairs per 32 scores, over this thread's own (already loaded)
+      // scores in buffer j&1 (both halves have passed the exchange barrier,
+      // so every score of the buffer is in registers); the row sums come
+      // from the MMA's ones group. Rows of idle warps get zeros every tile:
+      // S of tile j+2 overwrites the buffer.
       const bool live = m_use != kNegInfT;
       const float nm = -m_use;
-      const uint32_t padr = tmem + lanes + kTcPCol + hf * (kTcCols / 2);
+      const uint32_t padr = sadr;
 #pragma unroll
       for (int ch = 0; ch < kTcCols / 32; ++ch) {
-        if (idle && j > 0) break;          // zero P rows stay zero
         const uint32_t vm = (live && !idle) ? vmask[ch] : 0u;
         uint32_t pk[16];
+        if (idle) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = 0u;
+          tmem_st16(padr + ch * 16, pk);
+          continue;
+        }
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float x0, x1;
@@ -544,9 +542,15 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
         tmem_st16(padr + ch * 16, pk);
       }
       // the output is rescaled only when some row of the warp needs it (the
-      // other half row takes the same decision); P V of tile j-1 has
-      // completed (waited for above)
+      // other half row takes the same decision), after P V of tile j-1 has
+      // completed (P V of tile j waits for this warp's P, so the phase is
+      // current)
       if (__any_sync(0xffffffffu, resc)) {
+        if (j >= 1) {
+          ok = mbar_wait_bounded(bar + 8u * kBarODone, (j - 1) & 1, abort_flag, kTcWaitCycles);
+          ok = __all_sync(0xffffffffu, ok);
+          tc_fence_after();
+        }
         if (ok) {
 #pragma unroll 1
           for (int ch = 0; ch < D / 64; ++ch) {
