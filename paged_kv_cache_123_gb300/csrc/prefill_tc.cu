@@ -469,13 +469,27 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
 #pragma unroll
         for (int e = 0; e < kTcCols; ++e) v[e] = 0u;
       }
-      uint32_t vmask[kTcCols / 32];
+      // positive scale (the usual case): the invalid scores of a boundary
+      // tile become -inf in place, so both passes below run without masks
+      // (-inf times the scale stays -inf, and 2^-inf is 0); a zero or
+      // negative scale takes the general, per-element masked path
+      const bool pscale = sl2 > 0.f;
+      auto own_mask = [&](int ch) -> uint32_t { return fast ? 0xffffffffu : chunk_mask(ch); };
+      if (ok && !idle && pscale && !fast) {
 #pragma unroll
-      for (int ch = 0; ch < kTcCols / 32; ++ch) vmask[ch] = fast ? 0xffffffffu : chunk_mask(ch);
+        for (int ch = 0; ch < kTcCols / 32; ++ch) {
+          const uint32_t m = chunk_mask(ch);
+          if (m != 0xffffffffu) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (!((m >> e) & 1u)) v[ch * 32 + e] = __float_as_uint(kNegInfT);
+          }
+        }
+      }
       // pass 1: maximum of the valid scaled scores of this half row
       float mx = kNegInfT;
       if (ok && !idle) {
-        if (fast) {
+        if (pscale) {
           float mx0 = kNegInfT, mx1 = kNegInfT;
 #pragma unroll
           for (int e = 0; e < kTcCols; e += 4) {
@@ -485,9 +499,12 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
           mx = fmaxf(mx0, mx1) * sl2;       // the scale is positive: max commutes
         } else {
 #pragma unroll
-          for (int e = 0; e < kTcCols; ++e)
-            mx = fmaxf(mx, ((vmask[e >> 5] >> (e & 31)) & 1u) ? __uint_as_float(v[e]) * sl2
-                                                               : kNegInfT);
+          for (int ch = 0; ch < kTcCols / 32; ++ch) {
+            const uint32_t m = own_mask(ch);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              mx = fmaxf(mx, ((m >> e) & 1u) ? __uint_as_float(v[ch * 32 + e]) * sl2 : kNegInfT);
+          }
         }
       }
       // the two halves of the row meet: exchange the maxima; the second
@@ -516,30 +533,41 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       const bool live = m_use != kNegInfT;
       const float nm = -m_use;
       const uint32_t padr = sadr;
+      // tcgen05.st is warp-collective: the branch is taken by whole warps
+      if (pscale && !idle && __all_sync(0xffffffffu, live)) {
 #pragma unroll
-      for (int ch = 0; ch < kTcCols / 32; ++ch) {
-        const uint32_t vm = (live && !idle) ? vmask[ch] : 0u;
-        uint32_t pk[16];
-        if (idle) {
+        for (int ch = 0; ch < kTcCols / 32; ++ch) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pk[e] = 0u;
-          tmem_st16(padr + ch * 16, pk);
-          continue;
-        }
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float x0, x1;
-          fma2(__uint_as_float(v[ch * 32 + e]), __uint_as_float(v[ch * 32 + e + 1]), sl2, nm,
-               x0, x1);
-          float p0 = ex2_approx(x0);
-          float p1 = ex2_approx(x1);
-          if (!fast) {
-            p0 = ((vm >> e) & 1u) ? p0 : 0.f;
-            p1 = ((vm >> (e + 1)) & 1u) ? p1 : 0.f;
+          for (int e = 0; e < 32; e += 2) {
+            float x0, x1;
+            fma2(__uint_as_float(v[ch * 32 + e]), __uint_as_float(v[ch * 32 + e + 1]), sl2, nm,
+                 x0, x1);
+            pk[e >> 1] = Pack2<T>::pack_out(ex2_approx(x0), ex2_approx(x1));
           }
-          pk[e >> 1] = Pack2<T>::pack_out(p0, p1);
+          tmem_st16(padr + ch * 16, pk);
         }
-        tmem_st16(padr + ch * 16, pk);
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < kTcCols / 32; ++ch) {
+          uint32_t pk[16];
+          if (idle) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+          } else {
+            const uint32_t vm = live ? own_mask(ch) : 0u;
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float x0, x1;
+              fma2(__uint_as_float(v[ch * 32 + e]), __uint_as_float(v[ch * 32 + e + 1]), sl2,
+                   nm, x0, x1);
+              const float p0 = ((vm >> e) & 1u) ? ex2_approx(x0) : 0.f;
+              const float p1 = ((vm >> (e + 1)) & 1u) ? ex2_approx(x1) : 0.f;
+              pk[e >> 1] = Pack2<T>::pack_out(p0, p1);
+            }
+          }
+          tmem_st16(padr + ch * 16, pk);
+        }
       }
       // the output is rescaled only when some row of the warp needs it (the
       // other half row takes the same decision), after P V of tile j-1 has
