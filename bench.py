@@ -444,8 +444,12 @@ def ours_arm(args):
         splits = 1 if ws_bytes == 0 else 2
         ptoks = None
     else:
-        splits, ptoks = pa.pa_decode_window_partitioning(S, cfg.num_q_heads, Hkv, B, max_len, W,
-                                                         P)
+        if fp8:
+            splits, ptoks = pa.pa_decode_fp8_partitioning(S, cfg.num_q_heads, Hkv, D, B,
+                                                          inp.q.dtype, max_len, W, P)
+        else:
+            splits, ptoks = pa.pa_decode_window_partitioning(S, cfg.num_q_heads, Hkv, B,
+                                                             max_len, W, P)
         ws_bytes = pa.pa_decode_window_workspace_bytes(S, cfg.num_q_heads, Hkv, D, B, max_len,
                                                        W, P)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)

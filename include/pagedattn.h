@@ -292,8 +292,12 @@ PA_API int pa_reshape_and_cache_fp8(const void* k, const void* v, int64_t num_to
 
 /*
  * pa_decode_attention_fp8 — pa_decode_attention over fp8 pools: q and out of
- * `dtype`, K = code * k_scale, V = code * v_scale. Same partitioning and
- * workspace as pa_decode_attention (pa_decode_workspace_bytes applies).
+ * `dtype`, K = code * k_scale, V = code * v_scale. The workspace is sized by
+ * pa_decode_workspace_bytes with the same arguments. The call may use fewer,
+ * longer partitions than pa_decode_attention (16-bit queries, head size 128
+ * and blocks of at least 8 tokens run the tensor-core kernel, which takes
+ * the tensor-core partition sizes for every group size); never more, so
+ * that workspace suffices. pa_decode_fp8_partitioning reports the choice.
  * k_scale and v_scale must be positive (else PA_ERR_SHAPE).
  */
 PA_API int pa_decode_attention_fp8(const void* q, const void* key_cache,
@@ -337,6 +341,17 @@ PA_API int pa_decode_window_partitioning(int num_seqs, int num_q_heads, int num_
                                          int block_size, int max_seq_len, int window,
                                          int partition_size, int* num_splits_out,
                                          int* partition_tokens_out);
+/*
+ * pa_decode_fp8_partitioning — the partition count and length that
+ * pa_decode_attention_fp8 (window = 0) or pa_decode_attention_fp8_window
+ * uses with the same sizes; head_size and dtype (the query type) select
+ * the kernel. Either output pointer (host) may be NULL. Invalid sizes give
+ * PA_ERR_SHAPE, an unknown dtype PA_ERR_DTYPE.
+ */
+PA_API int pa_decode_fp8_partitioning(int num_seqs, int num_q_heads, int num_kv_heads,
+                                      int head_size, int block_size, int dtype,
+                                      int max_seq_len, int window, int partition_size,
+                                      int* num_splits_out, int* partition_tokens_out);
 PA_API int64_t pa_decode_window_workspace_bytes(int num_seqs, int num_q_heads,
                                                 int num_kv_heads, int head_size,
                                                 int block_size, int max_seq_len, int window,

@@ -79,9 +79,15 @@ int check_launch(cudaError_t e) {
 // wave would run a few CTAs alone at a fraction of the bandwidth
 // (longctx-shaped window of 4096: 0.68 -> 0.80 of the copy bandwidth; a
 // 333-token window over the Llama-7B batch: 0.85 -> 0.92).
+// mma_fp8 = the call runs the tensor-core kernel over fp8 pools, which takes
+// the tensor-core class for every group size (group 1 included: one
+// 2,048-token partition per Llama-7B sequence ran at 0.81 of the copy
+// bandwidth, 512-token ones at 0.69). Its partitions are never shorter than
+// those of the 16-bit call with the same sizes, so the 16-bit workspace
+// query sizes its scratch too.
 void partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
                   int max_seq_len, int partition_size, int sm_count, bool uniform,
-                  int* splits, int* tokens) {
+                  bool mma_fp8, int* splits, int* tokens) {
   const int64_t tile = block_size > 64 ? block_size : 64;
   const int64_t len = max_seq_len > 0 ? max_seq_len : 1;
   auto round_up = [tile](int64_t x) { return (x + tile - 1) / tile * tile; };
@@ -90,7 +96,7 @@ void partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_siz
     P = round_up(partition_size);
   } else {
     const int g = num_q_heads / num_kv_heads;
-    const bool tc = g >= 2 && block_size >= 8;
+    const bool tc = (g >= 2 && block_size >= 8) || mma_fp8;
     const int64_t per_sm = tc ? 2 : 8;
     const int64_t cap = round_up(tc ? 2048 : 512);
     const int64_t pairs = num_seqs > 0 ? (int64_t)num_seqs * num_kv_heads : 1;
@@ -135,8 +141,8 @@ int covered_len(int max_seq_len, int window) {
 bool windowed(int max_seq_len, int window) { return window > 0 && window < max_seq_len; }
 
 int decode_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
-                        int max_seq_len, int window, int partition_size, int* splits,
-                        int* tokens);
+                        int max_seq_len, int window, int partition_size, bool mma_fp8,
+                        int* splits, int* tokens);
 
 // Validation, partitioning and launch shared by the decode entry points
 // (16-bit/fp32 pools or E4M3 pools, with or without a window).
@@ -164,8 +170,8 @@ int check_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head
 // Partitioning of a decode call over max_seq_len (and a window, 0 = none),
 // with the device's SM count.
 int decode_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
-                        int max_seq_len, int window, int partition_size, int* splits,
-                        int* tokens) {
+                        int max_seq_len, int window, int partition_size, bool mma_fp8,
+                        int* splits, int* tokens) {
   if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 ||
       num_q_heads % num_kv_heads != 0 || !pow2(block_size) || block_size > 256 ||
       max_seq_len < 0 || partition_size < 0 || window < 0)
@@ -176,7 +182,7 @@ int decode_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int blo
   int sp, tk;
   partitioning(num_seqs, num_q_heads, num_kv_heads, block_size,
                covered_len(max_seq_len, window), partition_size, g_sm_count[dev],
-               windowed(max_seq_len, window), &sp, &tk);
+               windowed(max_seq_len, window), mma_fp8, &sp, &tk);
   if (splits) *splits = sp;
   if (tokens) *tokens = tk;
   return PA_OK;
@@ -249,7 +255,7 @@ int pa_decode_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int 
                            int max_seq_len, int partition_size,
                            int* num_splits_out, int* partition_tokens_out) {
   return decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, 0,
-                             partition_size, num_splits_out, partition_tokens_out);
+                             partition_size, false, num_splits_out, partition_tokens_out);
 }
 
 int pa_decode_window_partitioning(int num_seqs, int num_q_heads, int num_kv_heads,
@@ -258,7 +264,21 @@ int pa_decode_window_partitioning(int num_seqs, int num_q_heads, int num_kv_head
                                   int* partition_tokens_out) {
   if (window < 0) return PA_ERR_SHAPE;
   return decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len,
-                             window, partition_size, num_splits_out, partition_tokens_out);
+                             window, partition_size, false, num_splits_out, partition_tokens_out);
+}
+
+int pa_decode_fp8_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+                               int block_size, int dtype, int max_seq_len, int window,
+                               int partition_size, int* num_splits_out,
+                               int* partition_tokens_out) {
+  if (elt_bytes(dtype) == 0) return PA_ERR_DTYPE;
+  if (window < 0 || num_kv_heads <= 0) return PA_ERR_SHAPE;
+  pa::DecodeArgs a{};
+  a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size; a.block_size = block_size; a.dtype = dtype;
+  return decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len,
+                             window, partition_size, pa::mma_fp8_path_applies(a),
+                             num_splits_out, partition_tokens_out);
 }
 
 int64_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
@@ -270,7 +290,7 @@ int64_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
   if (partition_size < 0) return PA_ERR_SHAPE;
   int splits, tokens;
   st = decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, 0,
-                           partition_size, &splits, &tokens);
+                           partition_size, false, &splits, &tokens);
   if (st != PA_OK) return st;
   return workspace_for(num_seqs, num_q_heads, head_size, splits);
 }
@@ -298,7 +318,7 @@ int64_t pa_decode_window_workspace_bytes(int num_seqs, int num_q_heads, int num_
   if (partition_size < 0) return PA_ERR_SHAPE;
   int splits, tokens;
   st = decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, window,
-                           partition_size, &splits, &tokens);
+                           partition_size, false, &splits, &tokens);
   if (st != PA_OK) return st;
   return workspace_for(num_seqs, num_q_heads, head_size, splits);
 }
@@ -571,7 +591,8 @@ int run_decode(const void* q, const void* key_cache, const void* value_cache,
   a.dtype = dtype; a.scale = scale; a.max_seq_len = max_seq_len; a.window = window;
   partitioning(num_seqs, num_q_heads, num_kv_heads, block_size,
                covered_len(max_seq_len, window), partition_size, g_sm_count[dev],
-               windowed(max_seq_len, window), &a.num_splits, &a.partition);
+               windowed(max_seq_len, window), fp8 && pa::mma_fp8_path_applies(a),
+               &a.num_splits, &a.partition);
   const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);
   a.ws_acc = nullptr; a.ws_ml = nullptr;
   if (need > 0) {

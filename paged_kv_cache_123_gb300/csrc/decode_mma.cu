@@ -71,7 +71,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   // ([6.1e-5, 65504]) are exact in fp16
   using MT = typename std::conditional<KV8, __half, T>::type;
   constexpr int KSTEPS = D / 16;
-  static_assert(G == 2 || G == 4 || G == 8, "group");
+  static_assert(G == 2 || G == 4 || G == 8 || (KV8 && G == 1), "group");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -507,6 +507,9 @@ cudaError_t launch_mma_tdg(const DecodeArgs& a, float ks, float vs, cudaStream_t
 template <typename T, int D, bool KV8>
 cudaError_t launch_mma_td(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
   switch (a.num_q_heads / a.num_kv_heads) {
+    case 1:
+      if constexpr (KV8) return launch_mma_tdg<T, D, 1, KV8>(a, ks, vs, st);
+      return cudaErrorInvalidValue;
     case 2: return launch_mma_tdg<T, D, 2, KV8>(a, ks, vs, st);
     case 4: return launch_mma_tdg<T, D, 4, KV8>(a, ks, vs, st);
     case 8: return launch_mma_tdg<T, D, 8, KV8>(a, ks, vs, st);
@@ -542,6 +545,17 @@ bool mma_path_applies(const DecodeArgs& a) {
   const int g = a.num_q_heads / a.num_kv_heads;
   return (a.dtype == PA_F16 || a.dtype == PA_BF16) && (g == 2 || g == 4 || g == 8) &&
          a.block_size >= 8 && (a.head_size == 64 || a.head_size == 128);
+}
+
+// fp8 pools: the same kernel for every group size with 16-bit queries and
+// head size 128, group 1 included (the group is the N = 8 side of the
+// products, zero-padded; widening the codes costs the same per byte whatever
+// the group, and on the CUDA cores a group of 1 pays a 16-lane reduction per
+// token)
+bool mma_fp8_path_applies(const DecodeArgs& a) {
+  const int g = a.num_q_heads / a.num_kv_heads;
+  return (a.dtype == PA_F16 || a.dtype == PA_BF16) && (g == 1 || g == 2 || g == 4 || g == 8) &&
+         a.block_size >= 8 && a.head_size == 128;
 }
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st) {

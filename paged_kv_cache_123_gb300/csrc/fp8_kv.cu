@@ -334,9 +334,10 @@ cudaError_t launch_fp8_t(const DecodeArgs& a, float ks, float vs, cudaStream_t s
 
 cudaError_t launch_decode_fp8(const DecodeArgs& a, float k_scale, float v_scale,
                               cudaStream_t st) {
-  // 16-bit queries in groups of 2, 4 or 8 with head size 128: the
-  // tensor-core kernel; everything else stays on the CUDA cores
-  if (mma_path_applies(a) && a.head_size == 128)
+  // 16-bit queries in groups of 1, 2, 4 or 8 with head size 128 and blocks
+  // of at least 8 tokens: the tensor-core kernel; everything else stays on
+  // the CUDA cores
+  if (mma_fp8_path_applies(a))
     return launch_decode_mma_fp8(a, k_scale, v_scale, st);
   switch (a.dtype) {
     case PA_F32: return launch_fp8_t<float>(a, k_scale, v_scale, st);

@@ -69,6 +69,7 @@ cudaError_t launch_decode_fp8(const DecodeArgs& a, float k_scale, float v_scale,
 cudaError_t launch_decode_mma_fp8(const DecodeArgs& a, float k_scale, float v_scale,
                                   cudaStream_t st);
 bool mma_path_applies(const DecodeArgs& a);
+bool mma_fp8_path_applies(const DecodeArgs& a);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
 // log-sum-exp combine of the partitions (no-op when num_splits == 1)

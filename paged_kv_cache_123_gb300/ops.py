@@ -92,6 +92,18 @@ def pa_decode_window_partitioning(num_seqs: int, num_q_heads: int, num_kv_heads:
     return s.value, p.value
 
 
+def pa_decode_fp8_partitioning(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                               head_size: int, block_size: int, dtype: torch.dtype,
+                               max_seq_len: int, window: int = 0, partition_size: int = 0):
+    """(num_splits, partition_tokens) the fp8-pool attention calls will use;
+    dtype is the query type."""
+    s, p = ctypes.c_int(0), ctypes.c_int(0)
+    check("pa_decode_fp8_partitioning", lib().pa_decode_fp8_partitioning(
+        num_seqs, num_q_heads, num_kv_heads, head_size, block_size, DTYPE_CODE[dtype],
+        max_seq_len, window, partition_size, ctypes.byref(s), ctypes.byref(p)))
+    return s.value, p.value
+
+
 def pa_decode_attention(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
                         block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
                         num_kv_heads: int, out: Optional[torch.Tensor] = None, *,

@@ -46,7 +46,8 @@ def test_quantising_kv_write_bit_exact(dtype, k_scale, v_scale):
 
 
 CASES = [(dt, G, 16, 0) for dt in ("f32", "f16", "bf16") for G in (1, 2, 4, 8)]
-CASES += [("bf16", 8, 1, 0), ("bf16", 8, 128, 0), ("f16", 1, 64, 192), ("bf16", 4, 16, 64)]
+CASES += [("bf16", 8, 1, 0), ("bf16", 8, 128, 0), ("f16", 1, 64, 192), ("bf16", 4, 16, 64),
+          ("bf16", 1, 8, 0), ("f16", 1, 128, 0), ("bf16", 1, 4, 0)]
 
 
 @pytest.mark.parametrize("dtype,G,B,partition", CASES)
@@ -97,3 +98,30 @@ def test_fp8_full_step_against_oracle():
     torch.cuda.synchronize()
     assert np.array_equal(kd.cpu().numpy(), ko) and np.array_equal(vd.cpu().numpy(), vo)
     assert max_abs_err(out, want) <= TOL["bf16"]
+
+
+def test_fp8_partitioning_query():
+    """Tensor-core fp8 calls take the tensor-core partition sizes for every
+    group size (group 1 included); never more partitions than the 16-bit
+    call, whose workspace query therefore sizes the fp8 scratch too."""
+    bf = torch.bfloat16
+    # Llama-7B shape over fp8 pools: one partition per sequence
+    assert pa.pa_decode_fp8_partitioning(64, 32, 32, 128, 16, bf, 2000) == (1, 2048)
+    assert pa.pa_decode_partitioning(64, 32, 32, 16, 2000)[0] > 1
+    for args in [(64, 32, 32, 128, 16), (128, 64, 8, 128, 16), (16, 32, 8, 128, 64),
+                 (8, 8, 8, 64, 16), (8, 8, 8, 128, 4)]:
+        S, Hq, Hkv, D, B = args
+        for dt in (bf, torch.float16, torch.float32):
+            for L, W in ((2049, 0), (8193, 0), (32768, 4096), (5000, 333)):
+                f8 = pa.pa_decode_fp8_partitioning(S, Hq, Hkv, D, B, dt, L, W)
+                sixteen = pa.pa_decode_window_partitioning(S, Hq, Hkv, B, L, W)
+                assert f8[0] <= sixteen[0], (args, dt, L, W, f8, sixteen)
+    # the CUDA-core cases (fp32 queries, head size 64, blocks below 8) keep
+    # the 16-bit call's partitioning
+    assert pa.pa_decode_fp8_partitioning(64, 32, 32, 128, 16, torch.float32, 2049) == \
+        pa.pa_decode_partitioning(64, 32, 32, 16, 2049)
+    assert pa.pa_decode_fp8_partitioning(64, 32, 32, 128, 4, bf, 2049) == \
+        pa.pa_decode_partitioning(64, 32, 32, 4, 2049)
+    with pytest.raises(pa.PagedAttnError):
+        pa.pa_decode_fp8_partitioning(64, 32, 32, 128, 16, bf, 2049, -1)
+
