@@ -193,26 +193,60 @@ def _orc_init(spec):
 
 
 def _orc_run(job):
+    import numpy as np
+
     import oracle
-    seqs, scale, hkv, bs, dtype = job
+    kind, units, p = job
     A = _ORC
-    oracle.decode_attention(A["q"], A["kc"], A["vc"], A["tables"], A["lens"], scale, hkv, bs,
-                            dtype, seqs=seqs)
-    return len(seqs)
+    if kind == "decode":
+        oracle.decode_attention(A["q"], A["kc"], A["vc"], A["tables"], A["lens"], p["scale"],
+                                p["hkv"], p["bs"], p["dtype"], seqs=units, window=p["window"])
+    elif kind == "fp8":
+        oracle.decode_attention_fp8(A["q"], A["kc"], A["vc"], A["tables"], A["lens"],
+                                    p["scale"], p["hkv"], p["bs"], p["dtype"], p["ks"], p["vs"],
+                                    seqs=units, window=p["window"])
+    else:   # "mq": units are (sequence, KV head) pairs of N new tokens each
+        N, g = p["N"], p["g"]
+        for s, kvh in units:
+            oracle.multi_query_attention(
+                A["q"][s * N:(s + 1) * N, kvh * g:(kvh + 1) * g], A["kc"][:, kvh:kvh + 1],
+                A["vc"][:, kvh:kvh + 1], A["tables"][s:s + 1], np.array([0, N]),
+                A["lens"][s:s + 1], p["scale"], 1, p["bs"], p["dtype"])
+    return len(units)
 
 
 class OracleTimer:
     """The CPU oracle, as it stands, over a spawn pool of single-threaded
-    workers that map the inputs from files in a temporary directory. `arrays` are numpy
-    copies of the step's inputs taken before any kernel ran."""
+    workers that map the inputs from files in a temporary directory. `arrays`
+    are numpy copies of the step's inputs taken before any kernel ran.
+    kind "decode" (16-bit pools) or "fp8" (E4M3 pools, scales ks / vs) times
+    decode attention, with a sliding window when window > 0, on whole
+    sequences; kind "mq" times the causal attention of N new tokens per
+    sequence on (sequence, KV head) units."""
 
-    def __init__(self, arrays, cfg, scale, workers):
+    def __init__(self, arrays, cfg, scale, workers, kind="decode", window=0, ks=1.0, vs=1.0,
+                 N=1):
         import multiprocessing as mp
         import tempfile
 
         import numpy as np
         self.cfg, self.scale, self.workers = cfg, scale, workers
-        self.lens = [int(x) for x in arrays["lens"].tolist()]
+        self.kind, self.window, self.N = kind, window, N
+        self.params = {"scale": scale, "hkv": cfg.num_kv_heads, "bs": cfg.block_size,
+                       "dtype": cfg.dtype, "window": window, "ks": ks, "vs": vs, "N": N,
+                       "g": cfg.num_q_heads // cfg.num_kv_heads}
+        lens = [int(x) for x in arrays["lens"].tolist()]
+        self.lens = lens
+        att = [min(L, window) if window > 0 else L for L in lens]
+        if kind == "mq":
+            self.units = [(s, h) for s in range(len(lens)) for h in range(cfg.num_kv_heads)]
+            self.unit_tok = [lens[s] for s, _ in self.units]
+            self.bytes_per_tok = 2 * cfg.head_size * ELT[cfg.dtype]
+        else:
+            self.units = list(range(len(lens)))
+            self.unit_tok = att
+            self.bytes_per_tok = 2 * cfg.num_kv_heads * cfg.head_size * (
+                1 if kind == "fp8" else ELT[cfg.dtype])
         self.dir = tempfile.mkdtemp(prefix="pa_oracle_")
         spec = {}
         for k, a in arrays.items():
@@ -227,32 +261,30 @@ class OracleTimer:
         self.pool = mp.get_context("spawn").Pool(workers, initializer=_orc_init, initargs=(spec,))
         self.sample = None
 
-    def run(self, seqs):
-        cfg = self.cfg
-        chunks = [seqs[i::self.workers] for i in range(self.workers)]
-        jobs = [(c, self.scale, cfg.num_kv_heads, cfg.block_size, cfg.dtype)
-                for c in chunks if c]
+    def run(self, idx):
+        chunks = [[self.units[i] for i in idx[k::self.workers]] for k in range(self.workers)]
+        jobs = [(self.kind, c, self.params) for c in chunks if c]
         t0 = time.perf_counter()
         self.pool.map(_orc_run, jobs)
         return time.perf_counter() - t0
 
     def size_sample(self, budget_s):
-        """A sample worth about budget_s of oracle time: the first n
-        sequences, or the whole batch repeated when one pass is shorter."""
-        lens, w = self.lens, self.workers
-        probe = list(range(min(len(lens), w)))
+        """A sample worth about budget_s of oracle time: the first n units,
+        or the whole batch repeated when one pass is shorter."""
+        tok, w = self.unit_tok, self.workers
+        probe = list(range(min(len(tok), w)))
         self.run(probe)                      # warm the workers
         dt = self.run(probe)
-        per_tok = dt * w / max(1, sum(lens[i] for i in probe))
+        per_tok = dt * w / max(1, sum(tok[i] for i in probe))
         want_tok = budget_s * w / max(per_tok, 1e-12)
-        n, tok = 0, 0
-        while n < len(lens) and (tok < want_tok or n < w):
-            tok += lens[n]
+        n, t = 0, 0
+        while n < len(tok) and (t < want_tok or n < w):
+            t += tok[n]
             n += 1
         self.sample = list(range(n))
         self.repeats = 1
-        if n == len(lens) and tok < want_tok:
-            self.repeats = max(1, int(round(want_tok / max(1, tok))))
+        if n == len(tok) and t < want_tok:
+            self.repeats = max(1, int(round(want_tok / max(1, t))))
         return self.sample
 
     def measure(self):
@@ -261,12 +293,24 @@ class OracleTimer:
         dt = 0.0
         for _ in range(self.repeats):
             dt += self.run(self.sample)
-        sl = [self.lens[i] for i in self.sample]
-        byts = self.repeats * kv_read_bytes(sl, cfg.num_kv_heads, cfg.head_size, ELT[cfg.dtype])
-        desc = (f"first {len(sl)} of {len(self.lens)} sequences of the {cfg.name} batch, "
-                f"all {cfg.num_q_heads} query heads ({sum(sl)} context tokens)"
-                + (f", {self.repeats} passes" if self.repeats > 1 else ""))
-        return byts / dt / 1e9, self.repeats * sum(sl) / dt, desc, dt
+        st = [self.unit_tok[i] for i in self.sample]
+        byts = self.repeats * sum(st) * self.bytes_per_tok
+        what = {"decode": "decode attention", "fp8": "decode attention over fp8 pools",
+                "mq": f"causal attention of {self.N} new tokens per sequence"}[self.kind]
+        if self.window > 0:
+            what += f", window {self.window}"
+        if self.kind == "mq":
+            seqs = sorted({self.units[i][0] for i in self.sample})
+            desc = (f"{what}: first {len(self.sample)} of {len(self.units)} (sequence, KV head) "
+                    f"units of the {cfg.name} batch ({len(seqs)} sequences)")
+            toks = self.repeats * sum(st) / cfg.num_kv_heads
+        else:
+            desc = (f"{what}: first {len(st)} of {len(self.lens)} sequences of the {cfg.name} "
+                    f"batch, all {cfg.num_q_heads} query heads ({sum(st)} context tokens)")
+            toks = self.repeats * sum(st)
+        if self.repeats > 1:
+            desc += f", {self.repeats} passes"
+        return byts / dt / 1e9, toks / dt, desc, dt
 
     def close(self):
         self.pool.close()
@@ -399,10 +443,6 @@ def ours_arm(args):
     LAYERS = max(1, args.layers)
     if LAYERS > 1 and N > 1:
         raise SystemExit("--layers runs one new token per sequence")
-    # orc_arrays: host copies for the CPU baseline, taken before any kernel
-    # touches the pools (the 16-bit, one-new-token step only)
-    orc_arrays = oracle_arrays(inp) if (rank == 0 and world == 1 and N == 1 and not fp8
-                                        and not W and not args.no_cpu_baseline) else None
     kc, vc = inp.key_cache, inp.value_cache
     kscale = vscale = 1.0 / 48
     if fp8:   # E4M3 pools holding the same N(0,1) draws at scale 1/48
@@ -452,6 +492,13 @@ def ours_arm(args):
                                                              max_len, W, P)
         ws_bytes = pa.pa_decode_window_workspace_bytes(S, cfg.num_q_heads, Hkv, D, B, max_len,
                                                        W, P)
+    # host copies of the step's inputs for the CPU baseline, taken before any
+    # kernel touches the pools (fp8 pools as codes, windowed tables with their
+    # released entries, the N new tokens' queries)
+    orc_arrays = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        orc_arrays = {"q": np_(g["q"]), "kc": np_(kc), "vc": np_(vc),
+                      "tables": np_(g["tables"]), "lens": np_(g["lens"])}
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     out = torch.empty_like(g["q"])
     slots = torch.empty(S * N, dtype=torch.int64, device=dev)
@@ -707,7 +754,9 @@ def ours_arm(args):
     }
     if orc_arrays is not None:
         workers = host_cores()
-        timer = OracleTimer(orc_arrays, cfg, inp.scale, workers)
+        timer = OracleTimer(orc_arrays, cfg, inp.scale, workers,
+                            kind="mq" if N > 1 else ("fp8" if fp8 else "decode"), window=W,
+                            ks=kscale, vs=vscale, N=N)
         try:
             timer.size_sample(args.cpu_baseline_seconds)
             gbs, tps, desc, dt = timer.measure()
