@@ -9,15 +9,20 @@
 // so it runs on mma.sync m16n8k16 with the group as the N = 8 side (groups of
 // 2 or 4 are zero-padded) and 16 tokens or 16 head dims as the M side.
 //
-// Data movement: a producer warp walks the partition's block table and issues
-// one 4-D tiled TMA load (cp.async.bulk.tensor) per block (up to 64 whole
-// token rows, one contiguous run in HBM) for K and for V into a 3-stage ring (4 stages for fp8 pools)
-// of 64-token tiles, with the 128-byte swizzle so ldmatrix reads hit at most
-// two rows per bank group. Four
-// consumer warps take 16 tokens of each tile each, keep their own running
-// softmax state (log2 domain), and free the stage through an mbarrier. Every
-// wait is bounded: a stuck barrier raises an abort flag, the CTA drains and
-// leaves, and PA_ERR_TIMEOUT is latched.
+// Work items are (partition, KV head, sequence). Data movement: a producer
+// warp walks an item's block table and issues one 4-D tiled TMA load
+// (cp.async.bulk.tensor) per block (up to 64 whole token rows, one
+// contiguous run in HBM) for K and for V into a ring of 64-token tiles (3
+// stages; 4 for fp8 pools), with the 128-byte swizzle so ldmatrix reads hit
+// at most two rows per bank group. Four consumer warps take 16 tokens of
+// each tile each, keep their own running softmax state (log2 domain), and
+// free the stage through an mbarrier; at the end of an item they merge in
+// the stage of its last tile and release it afterwards. A CTA takes one
+// item, or (windowed batches, where every item has about the same work)
+// several in turn, its producer running ahead into the next. Every wait is
+// bounded: a stuck barrier raises an abort flag, the CTA lets its copies in
+// flight land (with its own limit) and leaves, and PA_ERR_TIMEOUT is
+// latched.
 //
 // Rows past the end of the sequence (the tail of the last block, blocks not
 // loaded) are masked to -inf in S and zeroed in the V tile before the P*V
@@ -45,6 +50,20 @@ constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 #define kNegInfM (-__int_as_float(0x7f800000))
 
 
+// Named barrier 1 over the four consumer warps (128 threads); the _and form
+// also returns whether every one of them passed `ok`.
+__device__ __forceinline__ void consumers_bar() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+__device__ __forceinline__ bool consumers_bar_and(bool ok) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
+      " barrier.cta.red.and.pred po, 1, 128, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(out) : "r"((uint32_t)ok) : "memory");
+  return out != 0;
+}
+
 // KV8 = the pools hold fp8 (E4M3) codes (head size 128): TMA brings the
 // codes (128-byte rows, 128-byte swizzle) and each lane widens the codes it
 // needs straight into fp16 mma fragments — K with the head dims of a k-step
@@ -54,7 +73,9 @@ constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 // the pools' scales (1 for 16-bit pools).
 // fp8 pools: half the shared memory per stage and a register budget for
 // three CTAs per SM, so more warps hide the conversion latency.
-template <typename T, int D, int G, bool KV8>
+// MULTI: each CTA walks several work items (items_per_cta > 1); the one-item
+// instantiation compiles to a single pass.
+template <typename T, int D, int G, bool KV8, bool MULTI>
 __global__ void __launch_bounds__(kMmaThreads, KV8 ? 3 : 2)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, float k_scale, float v_scale) {
@@ -87,31 +108,45 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   auto full_bar = [&](int st) { return bar0 + 8u * st; };
   auto empty_bar = [&](int st) { return bar0 + 8u * (kSt + st); };
 
-  const int s = blockIdx.z, kvh = blockIdx.y, split = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
-  const int L = a.seq_lens[s];
-  const bool bad_len =
-      L < 0 || L > a.max_seq_len || (int64_t)L > a.table_stride * a.block_size;
-  if (bad_len || L == 0) {
-    if (split == 0) {
-      if (L != 0 && threadIdx.x == 0) latch(a.err, PA_ERR_OUT_OF_RANGE);
-      T* out = reinterpret_cast<T*>(a.out);
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-        out[((int64_t)s * Hq + (int64_t)kvh * G) * D + i] = Vec<T>::cvt_out(0.f);
-    }
-    return;
-  }
-  const int lo = window_lo(L, a.window);
-  const int t0 = window_base(lo) + split * a.partition;
-  if (t0 >= L) return;
-  const int t1 = min(L, t0 + a.partition);
-  const int nsplit = (L - window_base(lo) + a.partition - 1) / a.partition;
-  const int ntiles = (t1 - t0 + kTile - 1) / kTile;
   const int B = a.block_size;
   const int bshift = __ffs(B) - 1;
   const int R = B < kTile ? B : kTile;           // rows per TMA box
-  const int32_t* trow = a.tables + (int64_t)s * a.table_stride;
+  // work items (partition, KV head, sequence), partition fastest; a CTA
+  // takes items blockIdx.x, blockIdx.x + gridDim.x, ... (exactly one when
+  // the grid covers them all). Producer and consumers walk the same items
+  // and carry the ring position across them.
+  const int n_items = a.num_splits * Hkv * a.num_seqs;
+  // per-warp row maxima and sums for the merge of an item ([4][8] each)
+  float* sm_m = reinterpret_cast<float*>(tile_mask + kSt);
+  float* sm_l = sm_m + kMmaConsumers * 8;
+  struct Item {
+    int s, kvh, split, L, lo, t0, t1, nsplit, ntiles;
+    bool bad, zero_out;
+  };
+  auto item_at = [&](int idx) {
+    Item im;
+    im.split = idx % a.num_splits;
+    const int rest = idx / a.num_splits;
+    im.kvh = rest % Hkv;
+    im.s = rest / Hkv;
+    im.L = a.seq_lens[im.s];
+    im.bad = im.L < 0 || im.L > a.max_seq_len || (int64_t)im.L > a.table_stride * a.block_size;
+    // an empty or invalid sequence: its first partition writes zeros
+    im.zero_out = (im.bad || im.L == 0) && im.split == 0;
+    im.lo = 0; im.t0 = 0; im.t1 = 0; im.nsplit = 1; im.ntiles = 0;
+    if (!im.bad && im.L > 0) {
+      im.lo = window_lo(im.L, a.window);
+      im.t0 = window_base(im.lo) + im.split * a.partition;
+      if (im.t0 < im.L) {
+        im.t1 = min(im.L, im.t0 + a.partition);
+        im.nsplit = (im.L - window_base(im.lo) + a.partition - 1) / a.partition;
+        im.ntiles = (im.t1 - im.t0 + kTile - 1) / kTile;
+      }
+    }
+    return im;
+  };
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < kSt; ++st) {
@@ -123,12 +158,6 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   }
   __syncthreads();
 
-  // merge state, per consumer warp; heads 2c and 2c+1 of this lane
-  float m0 = kNegInfM, m1 = kNegInfM, l0 = 0.f, l1 = 0.f;
-  float o[KSTEPS][4];
-#pragma unroll
-  for (int i = 0; i < KSTEPS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-
   if (warp == kMmaConsumers) {
     // ---------------- producer warp: lane p owns piece p (R rows of one
     // block) of each tile; the table entries of a tile are read in parallel
@@ -138,9 +167,15 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       prefetch_tensormap(&tmV);
     }
     const int npieces = kTile / R;             // <= 8 (R >= 8)
-    int issued = 0;
-    for (int i = 0; i < ntiles; ++i) {
-      const int st = i % kSt;
+    int it = 0;                                // tiles issued so far: the ring position
+    bool run = true;
+    for (int idx = blockIdx.x; run && idx < n_items;
+         idx = MULTI ? idx + (int)gridDim.x : n_items) {
+    const Item im = item_at(idx);
+    const int kvh = im.kvh, lo = im.lo, t0 = im.t0, t1 = im.t1;
+    const int32_t* trow = a.tables + (int64_t)im.s * a.table_stride;
+    for (int i = 0; i < im.ntiles; ++i) {
+      const int st = it % kSt;
       const int ts = t0 + i * kTile;
       const int te = min(t1, ts + kTile);
       const int tok = ts + lane * R;
@@ -154,15 +189,18 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       const unsigned pm = __ballot_sync(0xffffffffu, mine);
       int ok = 1;
       if (lane == 0) {
-        if (i >= kSt)
-          ok = mbar_wait_bounded(empty_bar(st), ((i / kSt) - 1) & 1, abort_flag, kWaitCycles);
+        if (it >= kSt)
+          ok = mbar_wait_bounded(empty_bar(st), ((it / kSt) - 1) & 1, abort_flag, kWaitCycles);
         if (ok) {
           tile_mask[st] = pm;
           mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * IN_ROW);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (!ok) {
+        run = false;
+        break;
+      }
       if (mine) {
         const uint32_t kdst = smem0 + st * STAGE_BYTES + lane * R * IN_ROW;
         const uint32_t vdst = kdst + KV_BYTES;
@@ -176,18 +214,25 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           tma_load_4d(vdst, &tmV, 0, 0, y, z, full_bar(st));
         }
       }
-      issued = i + 1;
+      ++it;
     }
-    // let the loads this CTA issued land before it can leave
+    }
+    // let the loads this CTA issued land before it can leave (also after a
+    // timeout: this wait has its own limit and ignores the abort flag)
     if (lane == 0)
-      for (int j = issued > kSt ? issued - kSt : 0; j < issued; ++j)
-        mbar_wait_bounded(full_bar(j % kSt), (j / kSt) & 1, abort_flag, kWaitCycles);
+      for (int j = it > kSt ? it - kSt : 0; j < it; ++j)
+        mbar_wait_drain(full_bar(j % kSt), (j / kSt) & 1, kWaitCycles);
   } else {
     // ---------------- consumers
     const int n = lane >> 2, c = lane & 3;
-    uint32_t qf[KSTEPS][2];
-    {
-      const T* qb = reinterpret_cast<const T*>(a.q) + ((int64_t)s * Hq + (int64_t)kvh * G) * D;
+    const float sl2 = a.scale * kLog2e * k_scale;
+    T* out = reinterpret_cast<T*>(a.out);
+    int it = 0;                                // tiles consumed so far: the ring position
+    bool run = true;
+    // query fragments of item idx (its sequence and KV head)
+    auto q_frags = [&](int idx, uint32_t (&qd)[KSTEPS][2]) {
+      const int kv = (idx / a.num_splits) % Hkv, sq = idx / a.num_splits / Hkv;
+      const T* qb = reinterpret_cast<const T*>(a.q) + ((int64_t)sq * Hq + (int64_t)kv * G) * D;
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
         if (n < G) {
@@ -196,17 +241,54 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           // applied to K the same way) so a lane's codes are contiguous
           const int d0 = KV8 ? c * (D / 4) + ks * 4 : ks * 16 + 2 * c;
           const int d1 = KV8 ? d0 + 2 : d0 + 8;
-          qf[ks][0] = to_mma_pair<T, MT>(*reinterpret_cast<const uint32_t*>(qb + n * D + d0));
-          qf[ks][1] = to_mma_pair<T, MT>(*reinterpret_cast<const uint32_t*>(qb + n * D + d1));
+          qd[ks][0] = to_mma_pair<T, MT>(*reinterpret_cast<const uint32_t*>(qb + n * D + d0));
+          qd[ks][1] = to_mma_pair<T, MT>(*reinterpret_cast<const uint32_t*>(qb + n * D + d1));
         } else {
-          qf[ks][0] = qf[ks][1] = 0u;
+          qd[ks][0] = qd[ks][1] = 0u;
         }
       }
+    };
+    // MULTI: the next item's query is loaded one item ahead, so its latency
+    // hides behind the current item's tiles
+    uint32_t qn[KSTEPS][2];
+    if (MULTI && (int)blockIdx.x < n_items) q_frags(blockIdx.x, qn);
+    for (int idx = blockIdx.x; run && idx < n_items;
+         idx = MULTI ? idx + (int)gridDim.x : n_items) {
+    const Item im = item_at(idx);
+    uint32_t qf[KSTEPS][2];
+    if (MULTI) {
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        qf[ks][0] = qn[ks][0];
+        qf[ks][1] = qn[ks][1];
+      }
+      if (idx + (int)gridDim.x < n_items) q_frags(idx + (int)gridDim.x, qn);
     }
-    const float sl2 = a.scale * kLog2e * k_scale;
-    for (int i = 0; i < ntiles; ++i) {
-      const int st = i % kSt;
-      if (!mbar_wait_bounded(full_bar(st), (i / kSt) & 1, abort_flag, kWaitCycles)) break;
+    if (im.zero_out) {
+      if (im.L != 0 && threadIdx.x == 0) latch(a.err, PA_ERR_OUT_OF_RANGE);
+      for (int i = threadIdx.x; i < G * D; i += kMmaConsumers * 32)
+        out[((int64_t)im.s * Hq + (int64_t)im.kvh * G) * D + i] = Vec<T>::cvt_out(0.f);
+      continue;
+    }
+    if (im.ntiles == 0) continue;
+    const int s = im.s, kvh = im.kvh, split = im.split, lo = im.lo;
+    const int t0 = im.t0, t1 = im.t1, nsplit = im.nsplit, ntiles = im.ntiles;
+    // merge state, per consumer warp; heads 2c and 2c+1 of this lane
+    float m0 = kNegInfM, m1 = kNegInfM, l0 = 0.f, l1 = 0.f;
+    float o[KSTEPS][4];
+#pragma unroll
+    for (int i = 0; i < KSTEPS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    if (!MULTI) q_frags(idx, qf);
+    bool ok = true;
+    for (int i = 0; i < ntiles; ++i, ++it) {
+      const int st = it % kSt;
+      // the stage of an item's last tile is released after the merge, which
+      // uses it
+      const bool last = i + 1 == ntiles;
+      if (!mbar_wait_bounded(full_bar(st), (it / kSt) & 1, abort_flag, kWaitCycles)) {
+        ok = false;
+        break;
+      }
       const int ts = t0 + i * kTile;
       const int te = min(t1, ts + kTile);
       const int r0 = ts + warp * 16;   // first token of this warp's 16 rows
@@ -347,11 +429,18 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         }
         if (!KV8 && okm != 0xffffu) fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(st));
+        if (lane == 0 && !last) mbar_arrive(empty_bar(st));
       } else {
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(st));
+        if (lane == 0 && !last) mbar_arrive(empty_bar(st));
       }
+    }
+    // the four warps agree that every tile of the item arrived (a timed-out
+    // wait anywhere stops the CTA; every warp gets here either way) and
+    // that all of them have read the last tile's stage
+    if (!consumers_bar_and(ok)) {
+      run = false;
+      break;
     }
     // sum the per-lane denominators over the 8 lanes that share a head pair
 #pragma unroll
@@ -359,20 +448,11 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
       l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-  }
-  __syncthreads();
-  if (*abort_flag) {
-    if (threadIdx.x == 0) latch(a.err, PA_ERR_TIMEOUT);
-    return;
-  }
-
-  // merge the four consumer warps through shared memory (the stage ring is
-  // free now)
-  float* sm_o = reinterpret_cast<float*>(smem);                  // [4][8][D]
-  float* sm_m = sm_o + kMmaConsumers * 8 * D;                    // [4][8]
-  float* sm_l = sm_m + kMmaConsumers * 8;                        // [4][8]
-  if (warp < kMmaConsumers) {
-    const int n = lane >> 2, c = lane & 3;
+    // merge the four consumer warps in the stage of the item's last tile
+    // (16 KB of fp32 partial outputs; maxima and sums beside the barriers)
+    const int st_last = (it - 1) % kSt;
+    float* sm_o = reinterpret_cast<float*>(smem + st_last * STAGE_BYTES);   // [4][8][D]
+    {
 #pragma unroll
     for (int mt = 0; mt < KSTEPS; ++mt) {
       float* base = sm_o + warp * 8 * D;
@@ -390,11 +470,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       sm_l[warp * 8 + 2 * c] = l0;
       sm_l[warp * 8 + 2 * c + 1] = l1;
     }
-  }
-  __syncthreads();
-  T* out = reinterpret_cast<T*>(a.out);
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int g = idx / D, d = idx - g * D;
+    }
+    consumers_bar();
+    for (int e = threadIdx.x; e < G * D; e += kMmaConsumers * 32) {
+    const int g = e / D, d = e - g * D;
     float M = kNegInfM;
 #pragma unroll
     for (int w = 0; w < kMmaConsumers; ++w) M = fmaxf(M, sm_m[w * 8 + g]);
@@ -415,7 +494,16 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       a.ws_acc[slot * D + d] = O;
       if (d == 0) { a.ws_ml[2 * slot] = M; a.ws_ml[2 * slot + 1] = Ls; }
     }
+    }
+    // the merge area has been read: the stage may be refilled by TMA
+    consumers_bar();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar(st_last));
+    }
   }
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) latch(a.err, PA_ERR_TIMEOUT);
 }
 
 // ---------------------------------------------------------------- host side
@@ -475,11 +563,12 @@ template <int D, bool KV8>
 constexpr int mma_smem_bytes() {
   constexpr int kSt = ring_stages<KV8>();
   return 1024 + kSt * 2 * kTile * (KV8 ? D : 2 * D) + 2 * kSt * 8 + 4 + 4 * kSt +
+         2 * kMmaConsumers * 8 * 4 +
          16;
 }
 
-template <typename T, int D, int G, bool KV8>
-cudaError_t launch_mma_tdg(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
+template <typename T, int D, int G, bool KV8, bool MULTI>
+cudaError_t launch_mma_tdgm(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
   if (!get_encode()) return cudaErrorNotSupported;
   CUtensorMap tk, tv;
   const bool ok = KV8 ? (encode_pool_map_fp8(&tk, a.kc, a) && encode_pool_map_fp8(&tv, a.vc, a))
@@ -487,21 +576,34 @@ cudaError_t launch_mma_tdg(const DecodeArgs& a, float ks, float vs, cudaStream_t
                          encode_pool_map(&tv, a.vc, MmaOps<T>::kTmaType, a));
   if (!ok) return cudaErrorInvalidValue;
   constexpr int smem = mma_smem_bytes<D, KV8>();
-  static_assert(ring_stages<KV8>() * 2 * kTile * (KV8 ? D : 2 * D) >=
-                    kMmaConsumers * 8 * D * 4 + 2 * kMmaConsumers * 8 * 4,
-                "merge area must fit in the stage ring");
+  static_assert(2 * kTile * (KV8 ? D : 2 * D) >= kMmaConsumers * 8 * D * 4,
+                "an item's merge must fit in one stage");
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, []() {
-    attr_err = cudaFuncSetAttribute(decode_mma_kernel<T, D, G, KV8>,
+    attr_err = cudaFuncSetAttribute(decode_mma_kernel<T, D, G, KV8, MULTI>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  dim3 grid(a.num_splits, a.num_kv_heads, a.num_seqs);
-  decode_mma_kernel<T, D, G, KV8><<<grid, kMmaThreads, smem, st>>>(a, tk, tv, ks, vs);
+  // one CTA per work item, or items_per_cta items each (a CTA walks its
+  // items while its producer runs ahead into the next one)
+  const int64_t n_items = (int64_t)a.num_splits * a.num_kv_heads * a.num_seqs;
+  const int per = (MULTI && a.items_per_cta > 1) ? a.items_per_cta : 1;
+  const int64_t grid = (n_items + per - 1) / per;
+  if (n_items > 0x7fffffff) return cudaErrorInvalidValue;
+  decode_mma_kernel<T, D, G, KV8, MULTI><<<(unsigned)grid, kMmaThreads, smem, st>>>(a, tk, tv,
+                                                                                   ks, vs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_combine(a, st);
+}
+
+template <typename T, int D, int G, bool KV8>
+cudaError_t launch_mma_tdg(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
+  if constexpr (D == 128 && !KV8) {
+    if (a.items_per_cta > 1) return launch_mma_tdgm<T, D, G, KV8, true>(a, ks, vs, st);
+  }
+  return launch_mma_tdgm<T, D, G, KV8, false>(a, ks, vs, st);
 }
 
 template <typename T, int D, bool KV8>

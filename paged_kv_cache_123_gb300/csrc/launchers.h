@@ -47,6 +47,7 @@ struct DecodeArgs {
   int window;        // sliding window in tokens; 0 = the whole sequence
   int partition;     // tokens per split (multiple of max(64, block_size))
   int num_splits;    // ceil(max_seq_len / partition), >= 1
+  int items_per_cta; // tensor-core decode: work items per CTA (<= 1: one each)
   void* out;
   float* ws_acc;     // [S][Hq][num_splits][D]   (num_splits > 1)
   float* ws_ml;      // [S][Hq][num_splits][2]   (num_splits > 1)

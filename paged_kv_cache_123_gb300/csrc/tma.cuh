@@ -58,6 +58,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Wait for a phase with a cycle limit only (no abort flag): a CTA that is
+// leaving lets its own copies in flight land first, also after a timeout.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
+                                                long long timeout_cycles) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > timeout_cycles) return false;
+  return true;
+}
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) writes to the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -216,3 +216,27 @@ def test_full_size_window_sampled(name, W):
                                    cfg.dtype, seqs, heads, window=W)
     assert max_abs_err(out, want, seqs, heads) <= TOL[cfg.dtype]
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("dtype,G,S", [("bf16", 8, 600), ("f16", 4, 700), ("bf16", 2, 640)])
+def test_window_many_items_per_cta(dtype, G, S):
+    """More (sequence, KV head) items than resident CTAs with a window: each
+    CTA of the tensor-core kernel walks several items. Ragged lengths (some
+    shorter than the window, some empty), released blocks, every output
+    against the oracle."""
+    Hkv, B, W = 2, 16, 200
+    cfg = workloads.DecodeConfig("wmany", S, Hkv * G, Hkv, 128, B, dtype, seed=40 + G)
+    rng = np.random.default_rng(G)
+    ctx = rng.integers(0, 900, S).tolist()
+    inp = workloads.make_decode_inputs(cfg, context_lens=ctx)
+    inp.seq_lens[::97] = 0
+    tab = _released(inp, W, B)
+    want = _oracle(inp, cfg, W, tab)
+    out = _gpu(inp, W, tab)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    assert max_abs_err(out, want) <= TOL[dtype]
+    splits, _ = pa.pa_decode_window_partitioning(S, Hkv * G, Hkv, B, inp.max_seq_len, W, 0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert splits * Hkv * S > 2 * sms          # more items than resident CTAs
+
