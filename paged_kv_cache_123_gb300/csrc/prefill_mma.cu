@@ -85,10 +85,11 @@ __device__ void mq_produce(const MultiQueryArgs& a, const CUtensorMap* tmK,
     }
     issued = i + 1;
   }
+  // let this warp's copies land before the CTA can leave (also after a
+  // timeout: this wait has its own limit and ignores the abort flag)
   if (lane == 0)
     for (int j = issued > kMqStages ? issued - kMqStages : 0; j < issued; ++j)
-      mbar_wait_bounded(bar0 + 8u * (j % kMqStages), (j / kMqStages) & 1, abort_flag,
-                        kMqWaitCycles);
+      mbar_wait_drain(bar0 + 8u * (j % kMqStages), (j / kMqStages) & 1, kMqWaitCycles);
 }
 
 // Log-sum-exp merge of the partitions of one (new token, query head) row;

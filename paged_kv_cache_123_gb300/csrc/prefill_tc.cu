@@ -228,11 +228,12 @@ __device__ void tc_produce(const MultiQueryArgs& a, const CUtensorMap* tmQ,
     }
     issued = i + 1;
   }
-  // let this warp's copies land before the CTA can leave
+  // let this warp's copies land before the CTA can leave (also after a
+  // timeout: these waits have their own limit and ignore the abort flag)
   if (lane == 0) {
-    if (!IS_V) mbar_wait_bounded(bar + 8u * kBarQ, 0, abort_flag, kTcWaitCycles);
+    if (!IS_V) mbar_wait_drain(bar + 8u * kBarQ, 0, kTcWaitCycles);
     for (int j = issued > NST ? issued - NST : 0; j < issued; ++j)
-      mbar_wait_bounded(bar + 8u * (full + j % NST), (j / NST) & 1, abort_flag, kTcWaitCycles);
+      mbar_wait_drain(bar + 8u * (full + j % NST), (j / NST) & 1, kTcWaitCycles);
   }
 }
 
@@ -299,9 +300,10 @@ __device__ void tc_issue(int ntiles, uint32_t s0, uint32_t bar, uint32_t tmem,
       if (ok) ok = issue_s(j + 2);
     }
   }
-  // every MMA issued above has completed once this barrier fires
+  // every MMA issued above has completed once this barrier fires (waited
+  // for also after a timeout, before the CTA frees its TMEM)
   mma_commit(bar + 8u * kBarDone);
-  mbar_wait_bounded(bar + 8u * kBarDone, 0, abort_flag, kTcWaitCycles);
+  mbar_wait_drain(bar + 8u * kBarDone, 0, kTcWaitCycles);
 }
 
 // SKIP_IDLE: runs shorter than a row tile leave whole warps without a token
