@@ -459,8 +459,13 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
         return m;
       };
       // interior tiles (every own column valid for every row of the warp)
-      // skip the per-column masks
-      const bool fast = __all_sync(0xffffffffu, whole && lim >= kTcCols - 1) && sl2 > 0.f;
+      // skip the per-column masks. Rows that hold no token (a run shorter
+      // than the row tile, e.g. 3 tokens x 8 heads = 24 of 32 rows) do not
+      // count: an MMA row only feeds its own output row, which is never
+      // written, so whatever their weights are (finite here: a whole tile
+      // has no stale K rows) they change nothing
+      const bool fast =
+          __all_sync(0xffffffffu, whole && (lim >= kTcCols - 1 || !rv)) && sl2 > 0.f;
       const uint32_t sadr = tmem + lanes + sb * kTcKv + hf * kTcCols;
       // this thread's 64 scores, one load; they stay in registers for both
       // passes
@@ -477,7 +482,7 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
       // negative scale takes the general, per-element masked path
       const bool pscale = sl2 > 0.f;
       auto own_mask = [&](int ch) -> uint32_t { return fast ? 0xffffffffu : chunk_mask(ch); };
-      if (ok && !idle && pscale && !fast) {
+      if (ok && !idle && pscale && !fast && rv) {
 #pragma unroll
         for (int ch = 0; ch < kTcCols / 32; ++ch) {
           const uint32_t m = chunk_mask(ch);

@@ -170,6 +170,28 @@ def test_short_runs(dtype, D, G, B, rows):
     assert pa.pa_get_device_error() == 0
 
 
+@pytest.mark.parametrize("n,B", [(3, 16), (5, 8), (7, 64), (3, 128)])
+def test_partial_warp_runs_with_garbage_pool(n, B):
+    """Runs whose (token, head) rows leave a warp partly without tokens (3, 5
+    or 7 tokens x 8 heads): those rows take no part in choosing the
+    mask-free path and are not masked. Every pool row outside the sequences
+    holds NaN, contexts are ragged (tiles with a tail and whole tiles), and
+    all written outputs must match the oracle and be finite."""
+    ctx = [0, 5, 130, 700, 1029]
+    b = make_batch("bf16", 128, 16, 2, B, ctx, [n] * len(ctx), 1200 + 7 * n + B)
+    used = torch.zeros(b["kc"].shape[0], B, dtype=torch.bool)
+    for s, L in enumerate(b["lens"].tolist()):
+        for j in range(L):
+            used[int(b["tables"][s, j // B]), j % B] = True
+    for cache in (b["kc"], b["vc"]):
+        cache.permute(0, 2, 1, 3)[~used] = float("nan")
+    for partition in (0, 256):
+        out, want, _ = run_both(b, partition)
+        assert torch.isfinite(out.float()).all(), partition
+        assert max_abs_err(out, want) <= TOL["bf16"], partition
+    assert pa.pa_get_device_error() == 0
+
+
 def test_short_runs_with_garbage_rows():
     b = make_batch("bf16", 128, 16, 2, 16, [3, 40, 0], [2, 4, 1], 43)
     used = torch.zeros(b["kc"].shape[0], 16, dtype=torch.bool)
