@@ -344,9 +344,9 @@ int pa_decode_attention_window(const void* q, const void* key_cache, const void*
 // neighbour: partitions only as short as needed for one CTA per SM (4 and 8
 // speculative tokens over the GQA-72B batch: 0.82 / 0.74 of the copy
 // bandwidth with 2,048-token partitions, 0.94 / 0.92 unsplit). Runs of at
-// most 16 rows (the mma.sync column kernel, several CTAs per SM) take the
-// decode tensor-core kernel's length (two waves of resident CTAs,
-// 256..2048 tokens).
+// most 16 rows (the mma.sync column kernel, two CTAs per SM) are split only
+// as far as one wave of those needs (2 speculative tokens: 0.87 with
+// 2,048-token partitions, 0.90 unsplit).
 static void mq_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
                      int max_query_len, int max_seq_len, int partition_size, int sm_count,
                      int* splits, int* tokens) {
@@ -359,16 +359,12 @@ static void mq_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int
     P = round_up(partition_size);
   } else if ((int64_t)max_query_len * g > 64) {
     P = round_up(len);
-  } else if ((int64_t)max_query_len * g > 16) {
-    const int64_t ctas = num_seqs > 0 ? (int64_t)num_seqs * num_kv_heads : 1;
-    P = round_up((len * ctas + sm_count - 1) / sm_count);
-    if (P < round_up(256)) P = round_up(256);
   } else {
-    const int64_t ctas = (int64_t)num_seqs * num_kv_heads;
-    const int64_t target = 2 * (int64_t)sm_count * 2;
-    P = round_up((len * (ctas > 0 ? ctas : 1) + target - 1) / target);
+    // one wave: one tcgen05 CTA per SM, or two column-kernel CTAs per SM
+    const int64_t ctas = num_seqs > 0 ? (int64_t)num_seqs * num_kv_heads : 1;
+    const int64_t slots = (int64_t)sm_count * ((int64_t)max_query_len * g > 16 ? 1 : 2);
+    P = round_up((len * ctas + slots - 1) / slots);
     if (P < round_up(256)) P = round_up(256);
-    if (P > round_up(2048)) P = round_up(2048);
   }
   if (P > len) P = round_up(len);
   *tokens = (int)P;
