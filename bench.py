@@ -78,17 +78,15 @@ def kv_read_bytes(seq_lens, num_kv_heads, head_size, elt):
     return int(sum(int(L) for L in seq_lens)) * 2 * num_kv_heads * head_size * elt
 
 
-# the sources a decode-attention launch is built from (kernels, shared device
-# helpers, host dispatch and partitioning)
-DECODE_SOURCES = ("api.cu", "common.cuh", "decode_mma.cu", "decode_simt.cu", "launchers.h",
-                  "mma_util.cuh", "tma.cuh")
-
-
 def kernel_sources_digest():
+    """Digest of every source the library is built from (kernels, shared
+    device helpers, host dispatch and partitioning): a profiled traffic row
+    is used only while none of them has changed."""
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
-        with open(os.path.join(CSRC, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
