@@ -710,8 +710,10 @@ def ours_arm(args):
                 "achieved": round(flops / (attn_ms * 1e-3) / 1e12, 1), "peak": t_peak,
                 "peak_kind": f"bf16_tflops (burst) of {t_kind}", "unit": "TFLOP/s",
                 "frac": round(flops / (attn_ms * 1e-3) / 1e12 / t_peak, 4),
-                "traffic": None, "avg_launch_us": round(attn_ms * 1e3, 2),
-                "algorithmic_flops_per_launch": flops}
+                "traffic": profiled_traffic(launch_label),
+                "avg_launch_us": round(attn_ms * 1e3, 2),
+                "algorithmic_flops_per_launch": flops,
+                "algorithmic_kv_bytes_per_launch": kv_bytes}
     step_s = ms_total * 1e-3 / args.steps
     value = world * LAYERS * kv_bytes / step_s / 1e9
     line = {
