@@ -9,7 +9,10 @@
 // pool layout is the 16-bit one with 1-byte elements, so a slot, a block and
 // the block table mean the same thing; half the bytes per token are read.
 //
-// Attention runs on the CUDA cores: lane groups own token rows (8 codes per
+// Attention over fp8 pools runs on the tensor-core kernel of decode_mma.cu
+// for 16-bit queries, head size 128 and blocks of at least 8 tokens (any
+// group size); the kernel here covers the rest (fp32 queries, head size 64,
+// smaller blocks) on the CUDA cores: lane groups own token rows (8 codes per
 // lane, 8-byte loads), scores and the softmax as in decode_simt.cu; k_scale is
 // folded into q and v_scale into the result, so codes are only widened.
 #include <cuda_fp8.h>

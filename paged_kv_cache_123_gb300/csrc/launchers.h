@@ -59,7 +59,10 @@ struct DecodeArgs {
 // CUDA-core kernel (decode_simt.cu) otherwise; then the split combine.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 // fp8 (E4M3) pools: quantising KV write, and decode attention (q/out dtype
-// in a.dtype, caches of 1-byte codes)
+// in a.dtype, caches of 1-byte codes): the tensor-core kernel when
+// mma_fp8_path_applies (16-bit queries, head size 128, blocks of at least 8
+// tokens, groups of 1, 2, 4 or 8), the CUDA-core kernel of fp8_kv.cu
+// otherwise
 cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, int64_t num_tokens,
                                          int num_kv_heads, int head_size, int dtype,
                                          const int64_t* slots, void* kc, void* vc,
