@@ -80,13 +80,17 @@ def kv_read_bytes(seq_lens, num_kv_heads, head_size, elt):
 
 def kernel_sources_digest():
     """Digest of every source the library is built from (kernels, shared
-    device helpers, host dispatch and partitioning): a profiled traffic row
-    is used only while none of them has changed."""
+    device helpers, host dispatch and partitioning) and of the workload
+    generator (the batches' lengths and tables): a profiled traffic row is
+    used only while none of them has changed."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(CSRC, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    paths = [os.path.join(CSRC, n) for n in sorted(os.listdir(CSRC))
+             if n.endswith((".cu", ".cuh", ".h"))]
+    paths.append(os.path.join(os.path.dirname(CSRC), "workloads.py"))
+    for path in paths:
+        if os.path.exists(path):
+            with open(path, "rb") as f:
+                h.update(os.path.basename(path).encode() + f.read())
     return h.hexdigest()[:16]
 
 

@@ -101,21 +101,25 @@ def randn_into(out: torch.Tensor, gen: torch.Generator, chunk_rows: int = 1 << 1
 def make_decode_inputs(cfg: DecodeConfig | str, device: str = "cpu",
                        seed: Optional[int] = None,
                        context_lens: Optional[list] = None) -> DecodeInputs:
-    """Draw one decode step's inputs. Everything is generated on `device`
-    with a torch.Generator seeded from the config (or `seed`)."""
+    """Draw one decode step's inputs from torch.Generators seeded from the
+    config (or `seed`). The batch's structure — context lengths and the
+    block permutation — comes from a CPU generator, so it is the same on
+    every device (the GPU bench and the CPU oracle time the same batch); the
+    values (q, new K/V, pool contents) are drawn on `device`."""
     if isinstance(cfg, str):
         cfg = CONFIGS[cfg]
     seed = cfg.seed if seed is None else seed
+    gcpu = torch.Generator().manual_seed(seed)
     gen = torch.Generator(device=device)
-    gen.manual_seed(seed)
+    gen.manual_seed(seed + 1)
     S, B = cfg.num_seqs, cfg.block_size
     if context_lens is not None:
         ctx = torch.tensor(context_lens, dtype=torch.int64)
     elif cfg.ctx_fixed is not None:
         ctx = torch.tensor(cfg.ctx_fixed, dtype=torch.int64)
     else:
-        ctx = torch.randint(cfg.ctx_lo, cfg.ctx_hi + 1, (S,), generator=gen,
-                            device=device).to("cpu", torch.int64)
+        ctx = torch.randint(cfg.ctx_lo, cfg.ctx_hi + 1, (S,), generator=gcpu,
+                            dtype=torch.int64)
     seq_lens = (ctx + 1).to(torch.int32)
     nblk = [_blocks_for(int(x), B) for x in seq_lens.tolist()]
     need = sum(nblk)
@@ -124,7 +128,7 @@ def make_decode_inputs(cfg: DecodeConfig | str, device: str = "cpu",
     else:
         nb = max(need, int(math.ceil(need * cfg.pool_slack)))
     assert nb >= need, "pool too small for the drawn lengths"
-    perm = torch.randperm(nb, generator=gen, device=device).to("cpu")
+    perm = torch.randperm(nb, generator=gcpu)
     mb = max(nblk) if nblk else 1
     tables = torch.full((S, mb), -1, dtype=torch.int32)
     off = 0
