@@ -69,9 +69,11 @@ int check_launch(cudaError_t e) {
 // that (sequences x KV heads x partitions) fills two waves of resident CTAs
 // even for the longest sequence, then capped: 2048 tokens for the
 // tensor-core kernel's shape class (group >= 2, block >= 8; two 100 KB CTAs
-// per SM) and 512 for the CUDA-core kernel (many small CTAs per SM, where
-// shorter partitions even out ragged lengths). Both caps were the fastest of
-// 512..4096 on the Llama-7B and GQA batches on GB300.
+// per SM; the fastest of 512..4096 on the GQA batch) and 256 for the
+// CUDA-core kernel (many small CTAs per SM, where short partitions even out
+// ragged lengths; the fastest of 256..1024 on Llama-7B-shape batches of 32,
+// 64 and 128 sequences: 0.99 of the copy bandwidth against 0.96 with 512 at
+// 64 sequences, equal at 128).
 // uniform = every long sequence covers about max_seq_len tokens (a sliding
 // window shorter than the longest sequence): equal work per (sequence, KV
 // head), so the partitions are sized for ONE wave of resident CTAs — the
@@ -98,7 +100,7 @@ void partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_siz
     const int g = num_q_heads / num_kv_heads;
     const bool tc = (g >= 2 && block_size >= 8) || mma_fp8;
     const int64_t per_sm = tc ? 2 : 8;
-    const int64_t cap = round_up(tc ? 2048 : 512);
+    const int64_t cap = round_up(tc ? 2048 : 256);
     const int64_t pairs = num_seqs > 0 ? (int64_t)num_seqs * num_kv_heads : 1;
     const int64_t floor_p = round_up(256);
     if (uniform) {
