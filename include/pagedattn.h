@@ -203,7 +203,8 @@ PA_API int pa_decode_attention(const void* q, const void* key_cache,
  *     launch; use pa_decode_attention with your own workspace for those.
  *   - The first call on a device looks up that device's address of the
  *     array (cudaGetSymbolAddress, with the device current); make that
- *     first call before any stream capture.
+ *     first call before any stream capture. If the lookup fails the call
+ *     returns PA_ERR_DEVICE and the next call on that device tries again.
  *   - All calls on a device share the one array and it keeps whatever the
  *     last call left in it (nothing in it needs to start at zero). Calls
  *     that may run at the same time on the GPU (different streams without
@@ -377,11 +378,11 @@ PA_API int pa_decode_attention_fp8_window(const void* q, const void* key_cache,
                                           int64_t workspace_bytes, void* stream);
 
 /*
- * pa_copy_blocks — block-level copy-on-write data movement ([P2] Figure 8:
- * "copy physical block 1's content to physical block 3"; [P4] copy-on-write
- * figure). For every pair (src, dst) in src_dst_pairs and every layer l, the
- * whole K block src of key_caches[l] is copied to block dst, and likewise for
- * value_caches[l].
+ * pa_copy_blocks — block-level copy-on-write data movement ([P2] Figure 8,
+ * the copy of the shared last block when one sharer diverges; [P4]
+ * copy-on-write figure). For every pair (src, dst) in src_dst_pairs and
+ * every layer l, the whole K block src of key_caches[l] is copied to block
+ * dst, and likewise for value_caches[l].
  *
  * key_caches, value_caches  HOST arrays of num_layers device pointers, one
  *               pool per layer, each [num_blocks][...] with block_bytes bytes

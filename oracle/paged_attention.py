@@ -170,7 +170,8 @@ def window_start(seq_len: int, window: int) -> int:
     tokens of the sequence, the new token included, so token j is attended
     iff seq_len - window <= j < seq_len. The pages name the sliding window
     only through the blocks it lets the allocator release ([P1] §3.2
-    allocate_slots, phase 1, "release blocks outside the sliding window")."""
+    allocate_slots, phase 1: blocks that fall wholly before the window are
+    freed)."""
     if window <= 0 or seq_len <= window:
         return 0
     return seq_len - window

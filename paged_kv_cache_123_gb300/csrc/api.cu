@@ -250,7 +250,8 @@ int pa_reshape_and_cache(const void* k, const void* v, int64_t num_tokens,
   if (st != PA_OK) return st;
   return check_launch(pa::launch_reshape_and_cache(
       k, v, num_tokens, num_kv_heads, head_size * eb, slot_mapping, key_cache,
-      value_cache, num_blocks, block_size, (cudaStream_t)stream, g_err_ptr[dev]));
+      value_cache, num_blocks, block_size, g_sm_count[dev], (cudaStream_t)stream,
+      g_err_ptr[dev]));
 }
 
 int pa_decode_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
@@ -464,7 +465,8 @@ int pa_reshape_and_cache_fp8(const void* k, const void* v, int64_t num_tokens, i
   if (st != PA_OK) return st;
   return check_launch(pa::launch_reshape_and_cache_fp8(
       k, v, num_tokens, num_kv_heads, head_size, dtype, slot_mapping, key_cache, value_cache,
-      num_blocks, block_size, k_scale, v_scale, (cudaStream_t)stream, g_err_ptr[dev]));
+      num_blocks, block_size, k_scale, v_scale, g_sm_count[dev], (cudaStream_t)stream,
+      g_err_ptr[dev]));
 }
 
 int pa_decode_attention_fp8(const void* q, const void* key_cache, const void* value_cache,
@@ -545,7 +547,7 @@ int pa_map_to_kernel_blocks(const int32_t* manager_table, int64_t num_rows,
   if (st != PA_OK) return st;
   return check_launch(pa::launch_map_to_kernel_blocks(
       manager_table, num_rows, manager_stride, num_cols, blocks_per_kv_block, kernel_table,
-      kernel_stride, (cudaStream_t)stream, g_err_ptr[dev]));
+      kernel_stride, g_sm_count[dev], (cudaStream_t)stream, g_err_ptr[dev]));
 }
 
 int pa_get_device_error(int* code_out, void* stream) {

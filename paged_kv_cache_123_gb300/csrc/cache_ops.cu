@@ -96,13 +96,14 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v,
                                      int64_t num_tokens, int num_kv_heads,
                                      int row_bytes, const int64_t* slots,
                                      void* kc, void* vc, int64_t num_blocks,
-                                     int block_size, cudaStream_t st, int* err) {
+                                     int block_size, int sm_count, cudaStream_t st,
+                                     int* err) {
   if (num_tokens == 0) return cudaSuccess;
   const int vpr = row_bytes / 16;
   const int64_t n = num_tokens * num_kv_heads * vpr;
   const int threads = 256;
   int64_t blocks = (n + threads - 1) / threads;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
   reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, st>>>(
       (const uint4*)k, (const uint4*)v, num_tokens, num_kv_heads, vpr, slots,
       (uint4*)kc, (uint4*)vc, num_blocks, block_size, err);
@@ -197,12 +198,12 @@ __global__ void map_to_kernel_blocks_kernel(const int32_t* __restrict__ mtab, in
 
 cudaError_t launch_map_to_kernel_blocks(const int32_t* mtab, int64_t rows, int64_t mstride,
                                         int64_t cols, int r, int32_t* ktab, int64_t kstride,
-                                        cudaStream_t st, int* err) {
+                                        int sm_count, cudaStream_t st, int* err) {
   const int64_t n = rows * cols * r;
   if (n == 0) return cudaSuccess;
   const int threads = 256;
   int64_t blocks = (n + threads - 1) / threads;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
   map_to_kernel_blocks_kernel<<<(unsigned)blocks, threads, 0, st>>>(
       mtab, rows, mstride, cols, r, ktab, kstride, err);
   return cudaGetLastError();

@@ -25,24 +25,27 @@ static __device__ __align__(256) unsigned char g_pa_static_scratch[PA_STATIC_SCR
 namespace {
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];
-int g_scratch_status[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
+void* g_scratch_addr[kMaxDevices];   // non-null once found for that device
+std::mutex g_scratch_mu;
 
-// Device address of this device's copy of the scratch array (looked up on
-// the first call made with the device current).
+// Device address of this device's copy of the scratch array, looked up with
+// the device current on the first call that succeeds. A failed lookup is not
+// remembered: the next call tries again.
 int scratch_for_current_device(void** addr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return PA_ERR_DEVICE;
-  std::call_once(g_scratch_once[dev], [dev]() {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_pa_static_scratch);
-    g_scratch_status[dev] = (e == cudaSuccess && p != nullptr) ? PA_OK : PA_ERR_DEVICE;
+    if (cudaGetSymbolAddress(&p, g_pa_static_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();   // do not leave the failure for the next call to see
+      return PA_ERR_DEVICE;
+    }
     g_scratch_addr[dev] = p;
-  });
+  }
   *addr = g_scratch_addr[dev];
-  return g_scratch_status[dev];
+  return PA_OK;
 }
 
 }  // namespace

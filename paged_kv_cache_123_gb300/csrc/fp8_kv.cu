@@ -119,12 +119,12 @@ cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, int64_t n
                                          int num_kv_heads, int head_size, int dtype,
                                          const int64_t* slots, void* kc, void* vc,
                                          int64_t num_blocks, int block_size, float k_scale,
-                                         float v_scale, cudaStream_t st, int* err) {
+                                         float v_scale, int sm_count, cudaStream_t st, int* err) {
   if (num_tokens == 0) return cudaSuccess;
   const int64_t n = num_tokens * num_kv_heads * (head_size / 8);
   const int threads = 256;
   int64_t blocks = (n + threads - 1) / threads;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
 #define PA_FP8_WRITE(TT)                                                                 \
   reshape_and_cache_fp8_kernel<TT><<<(unsigned)blocks, threads, 0, st>>>(                \
       (const TT*)k, (const TT*)v, num_tokens, num_kv_heads, head_size, slots, (uint8_t*)kc, \

@@ -1,6 +1,7 @@
 // Host-side launchers for the kernels, one per translation unit. They assume
 // the arguments were validated by the C ABI layer (api.cu) and return a
-// cudaError_t from the launch.
+// cudaError_t from the launch. `sm_count` is the device's multiprocessor
+// count; grid-stride kernels cap their grids at 16 CTAs per SM.
 #pragma once
 
 #include <cuda.h>
@@ -19,7 +20,8 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v,
                                      int64_t num_tokens, int num_kv_heads,
                                      int row_bytes, const int64_t* slots,
                                      void* kc, void* vc, int64_t num_blocks,
-                                     int block_size, cudaStream_t st, int* err);
+                                     int block_size, int sm_count, cudaStream_t st,
+                                     int* err);
 
 // Up to kCopyMaxLayers layers per launch.
 constexpr int kCopyMaxLayers = 64;
@@ -30,7 +32,7 @@ cudaError_t launch_copy_blocks(void* const* kcs, void* const* vcs,
 
 cudaError_t launch_map_to_kernel_blocks(const int32_t* mtab, int64_t rows, int64_t mstride,
                                         int64_t cols, int r, int32_t* ktab, int64_t kstride,
-                                        cudaStream_t st, int* err);
+                                        int sm_count, cudaStream_t st, int* err);
 
 struct DecodeArgs {
   const void* q;
@@ -67,7 +69,7 @@ cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, int64_t n
                                          int num_kv_heads, int head_size, int dtype,
                                          const int64_t* slots, void* kc, void* vc,
                                          int64_t num_blocks, int block_size, float k_scale,
-                                         float v_scale, cudaStream_t st, int* err);
+                                         float v_scale, int sm_count, cudaStream_t st, int* err);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, float k_scale, float v_scale,
                               cudaStream_t st);
 cudaError_t launch_decode_mma_fp8(const DecodeArgs& a, float k_scale, float v_scale,

@@ -79,16 +79,6 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int dch) {
   return base + line * 128 + (((dch & 7) ^ (line & 7)) << 4);
 }
 
-}  // namespace pa
-
-#include <cuda_fp8.h>
-
-namespace pa {
-
-}  // namespace pa
-
-namespace pa {
-
 // A pair of query values of type T as the operand type MT of the products.
 template <typename T, typename MT>
 __device__ __forceinline__ uint32_t to_mma_pair(uint32_t v) {
@@ -100,10 +90,6 @@ __device__ __forceinline__ uint32_t to_mma_pair(uint32_t v) {
     return *reinterpret_cast<const uint32_t*>(&h);
   }
 }
-
-}  // namespace pa
-
-namespace pa {
 
 // Four E4M3 codes (one 32-bit word, lowest byte first) -> two fp16 pairs,
 // exactly (every E4M3 value is an fp16 value): lo holds bytes 0 and 1 (byte 0

@@ -10,6 +10,7 @@ import oracle
 import oracle.paged_attention as opa
 import oracle.block_manager as obm
 import tests.test_oracle_attention as ta
+import tests.test_oracle_fp8 as tf
 import tests.test_oracle_pins as tp
 import tests.test_oracle_window as tw
 
@@ -128,6 +129,58 @@ def _skipped_ceil(L, W, B):
     return -(-opa.window_start(L, W) // B)             # frees a partly used block
 
 
+def _quant_multiply(x, dtype, scale):
+    x32 = opa.upcast(x, dtype).astype(np.float32)
+    return opa.e4m3_encode(x32 * np.float32(scale))         # multiplies by the scale
+
+
+def _quant_fp64(x, dtype, scale):
+    # divides and rounds in fp64: the nearest code of the unrounded quotient
+    q = opa.upcast(x, dtype) / np.float64(np.float32(scale))
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = opa.e4m3_decode(finite)
+    out = np.zeros(q.shape, dtype=np.uint8)
+    for i, v in enumerate(q.reshape(-1)):
+        d = np.abs(vals - v)
+        cand = finite[d == d.min()]
+        if len(cand) > 1:
+            cand = cand[(cand & 1) == 0]
+        if v < 0 and (cand & 0x80).all() == 0:
+            cand = cand | 0x80
+        out.reshape(-1)[i] = cand[0]
+    return out
+
+
+def _quant_scale_f64(x, dtype, scale):
+    # the scale is not rounded to fp32 first
+    q = opa.upcast(x, dtype) / float(scale)
+    return opa.e4m3_encode(q.astype(np.float32))
+
+
+class _RemoveSkippedCeil(obm.OracleBlockManager):
+    def remove_skipped(self, seq, window):
+        lo = opa.window_start(self.lens[seq], window)
+        table, gone = self.tables[seq], []
+        for i in range(-(-lo // self.block_size)):               # a partly used block too
+            if table[i] is not None:
+                gone.append(table[i])
+                self._release(table[i])
+                table[i] = None
+        return gone
+
+
+class _RemoveSkippedFreesShared(obm.OracleBlockManager):
+    def remove_skipped(self, seq, window):
+        table, gone = self.tables[seq], []
+        for i in range(opa.skipped_blocks(self.lens[seq], window, self.block_size)):
+            if table[i] is not None:
+                gone.append(table[i])
+                self.ref[table[i]] = 0                           # ignores other holders
+                self.free.append(table[i])
+                table[i] = None
+        return gone
+
+
 class _NoDecrementOnCow(obm.OracleBlockManager):
     def _release(self, b):
         pass
@@ -175,6 +228,11 @@ PIN_TESTS = [
     tw.test_window_of_one_is_the_new_value,
     tw.test_equal_keys_give_mean_of_last_w_values,
     lambda: tw.test_window_matches_masked_sdpa("f16", 8, 9),
+    tw.test_manager_releases_only_blocks_wholly_before_the_window,
+    tf.test_quantize_divides_by_the_scale,
+    tf.test_quantize_largest_code_for_448_scales,
+    tf.test_quantize_rounds_the_quotient_to_fp32_before_encoding,
+    tf.test_quantize_rounds_the_scale_to_fp32,
 ]
 
 MUTANTS = {
@@ -194,13 +252,18 @@ MUTANTS = {
     "window_one_late": [("window_start", _window_one_late)],
     "window_one_early": [("window_start", _window_one_early)],
     "skipped_ceil": [("skipped_blocks", _skipped_ceil)],
+    "quant_multiply": [("quantize_e4m3", _quant_multiply)],
+    "quant_fp64": [("quantize_e4m3", _quant_fp64)],
+    "quant_scale_f64": [("quantize_e4m3", _quant_scale_f64)],
+    "remove_skipped_ceil": [("OracleBlockManager", _RemoveSkippedCeil)],
+    "remove_skipped_frees_shared": [("OracleBlockManager", _RemoveSkippedFreesShared)],
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_planted_mistake(name, monkeypatch):
     for attr, fn in MUTANTS[name]:
-        for mod in (oracle, opa, obm, tp, tw):
+        for mod in (oracle, opa, obm, tp, tw, tf):
             if hasattr(mod, attr):
                 monkeypatch.setattr(mod, attr, fn)
     caught = []

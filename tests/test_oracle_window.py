@@ -142,3 +142,29 @@ def test_fp8_window_matches_masked_sdpa():
                 torch.from_numpy(K)[None], torch.from_numpy(V)[None],
                 attn_mask=mask[None, None, :], scale=0.088)
             assert np.allclose(got[s, kvh * g:(kvh + 1) * g], o[0].numpy(), atol=1e-12, rtol=0)
+
+
+def test_manager_releases_only_blocks_wholly_before_the_window():
+    # B = 4, one sequence of 10 tokens in blocks 5, 2, 7 (free order fixed so
+    # the ids are known). Window 7 starts at token 3 (block 0 still holds an
+    # attended token): nothing goes. Window 6 starts at token 4: block 0 (id
+    # 5) goes to the tail of the free queue and its entry is cleared. Window
+    # 1 starts at token 9: block 1 (id 2) goes too, block 2 stays.
+    m = oracle.OracleBlockManager(8, 4, free_order=[5, 2, 7, 0, 1, 3, 4, 6])
+    assert m.allocate("a", 10) == [5, 2, 7]
+    assert m.remove_skipped("a", 7) == []
+    assert m.remove_skipped("a", 6) == [5]
+    assert m.tables["a"] == [None, 2, 7] and m.ref[5] == 0 and list(m.free)[-1] == 5
+    assert m.remove_skipped("a", 1) == [2]
+    assert m.tables["a"] == [None, None, 7] and list(m.free)[-2:] == [5, 2]
+    assert m.remove_skipped("a", 1) == []                 # already released
+    # a block another sequence still references loses one reference only
+    m2 = oracle.OracleBlockManager(8, 4)
+    m2.allocate("p", 9)                                   # blocks 0, 1, 2
+    m2.fork("p", "c")
+    free_before = list(m2.free)
+    assert m2.remove_skipped("c", 1) == [0, 1]
+    assert m2.ref[:3] == [1, 1, 2] and list(m2.free) == free_before
+    assert m2.tables["p"] == [0, 1, 2] and m2.tables["c"] == [None, None, 2]
+    m2.free_seq("p")
+    assert list(m2.free)[-2:] == [0, 1] and m2.ref[:3] == [0, 0, 1]
