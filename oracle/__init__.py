@@ -23,6 +23,7 @@ from .paged_attention import (  # noqa: F401
     slots_allocated,
     fragmentation, kv_bytes_per_token, sharing_saving, map_to_kernel_blocks,
     multi_query_attention, e4m3_decode, e4m3_encode, quantize_e4m3, reshape_and_cache_fp8,
-    decode_attention_fp8, window_start, skipped_blocks,
+    decode_attention_fp8, window_start, skipped_blocks, block_scale_e4m3,
+    reshape_and_cache_fp8_block_scaled, decode_attention_fp8_block_scaled,
 )
 from .block_manager import OracleBlockManager  # noqa: F401

@@ -406,3 +406,95 @@ def decode_attention_fp8(q, key_cache8, value_cache8, block_tables, seq_lens, sc
             V = e4m3_decode(value_cache8[blk, kvh, j % block_size, :]) * np.float64(np.float32(v_scale))
             out[s, h] = decode_attention_one(q64[s, h], K, V, scale)
     return out
+
+
+# --------------------------------------------------------------------------
+# fp8 blocks that carry their own scales ([P1] §3.5 kv_quant_mode; §7.4 the
+# compression-aware block: quantisation tied to the block). Readings (the
+# pages fix no format): one scale per (physical block, KV head) for K and one
+# for V, a power of two, fixed by the KV write that stores the block's first
+# row from the largest magnitude among the tokens that this write puts into
+# that block (row 0 and the rows right after it, in consecutive slots);
+# every later write into the block quantises with the stored scale. The
+# scale 2^k is the smallest power of two with amax / 2^k <= 128, i.e.
+# k = ceil(log2(amax)) - 7, so the first tokens' largest magnitude lands in
+# (64, 128] and later tokens have 3.5x headroom before the largest finite
+# code (448). k is kept in [-126, 127] (normal fp32 powers of two); amax = 0
+# gives 1. NaN elements are left out of the maximum.
+# --------------------------------------------------------------------------
+def block_scale_e4m3(amax: float) -> float:
+    """Power-of-two scale for a block whose first tokens' largest magnitude
+    is amax (>= 0; inf allowed)."""
+    a = float(amax)
+    assert a >= 0.0
+    if a == 0.0:
+        return 1.0
+    if math.isinf(a):
+        k = 127
+    else:
+        mant, exp = math.frexp(a)          # a = mant * 2^exp, mant in [0.5, 1)
+        ceil_log2 = exp - 1 if mant == 0.5 else exp
+        k = min(max(ceil_log2 - 7, -126), 127)
+    return math.ldexp(1.0, k)
+
+
+def reshape_and_cache_fp8_block_scaled(k, v, slots, key_cache8, value_cache8, k_scales,
+                                       v_scales, block_size: int, dtype: str):
+    """KV write into e4m3 pools whose blocks carry their own scales
+    (k_scales / v_scales: float32 [num_blocks, num_kv_heads], updated in
+    place). Two passes over the call's tokens:
+      1. a token whose slot is row 0 of its block fixes that block's scales
+         from the largest |value| over it and the tokens that follow it in
+         this call in consecutive slots of the same block (at most B);
+      2. every token (slot >= 0) is quantised with its block's scale, as in
+         quantize_e4m3, at its slot."""
+    B = block_size
+    slots = np.asarray(slots, dtype=np.int64)
+    T = len(slots)
+    Hkv = key_cache8.shape[1]
+    for t in range(T):
+        s0 = int(slots[t])
+        if s0 < 0 or s0 % B != 0:
+            continue
+        n = 1
+        while n < B and t + n < T and int(slots[t + n]) == s0 + n:
+            n += 1
+        blk = s0 // B
+        for h in range(Hkv):
+            for src, dst in ((k, k_scales), (v, v_scales)):
+                run = np.abs(upcast(np.ascontiguousarray(src[t:t + n, h]), dtype))
+                amax = float(np.nanmax(run)) if not np.isnan(run).all() else 0.0
+                dst[blk, h] = block_scale_e4m3(amax)
+    for t in range(T):
+        s = int(slots[t])
+        if s < 0:
+            continue
+        blk, row = s // B, s % B
+        for h in range(Hkv):
+            key_cache8[blk, h, row] = quantize_e4m3(k[t, h], dtype, float(k_scales[blk, h]))
+            value_cache8[blk, h, row] = quantize_e4m3(v[t, h], dtype, float(v_scales[blk, h]))
+
+
+def decode_attention_fp8_block_scaled(q, key_cache8, value_cache8, k_scales, v_scales,
+                                      block_tables, seq_lens, scale: float, num_kv_heads: int,
+                                      block_size: int, dtype: str, seqs=None, heads=None,
+                                      window: int = 0) -> np.ndarray:
+    """Decode attention over e4m3 pools with per-(block, KV head) scales:
+    K_s[j] = decode(code) * k_scales[block of j, kvh], likewise V, exactly in
+    fp64; then decode_attention_one (window as in decode_attention)."""
+    S, Hq, D = q.shape
+    g = Hq // num_kv_heads
+    q64 = upcast(q, dtype)
+    out = np.zeros((S, Hq, D), dtype=np.float64)
+    for s in (range(S) if seqs is None else seqs):
+        L = int(seq_lens[s])
+        j = np.arange(window_start(L, window), L)
+        blk = np.asarray(block_tables[s], dtype=np.int64)[j // block_size]
+        for h in (range(Hq) if heads is None else heads):
+            kvh = h // g
+            ks = np.asarray(k_scales, dtype=np.float64)[blk, kvh][:, None]
+            vs = np.asarray(v_scales, dtype=np.float64)[blk, kvh][:, None]
+            K = e4m3_decode(key_cache8[blk, kvh, j % block_size, :]) * ks
+            V = e4m3_decode(value_cache8[blk, kvh, j % block_size, :]) * vs
+            out[s, h] = decode_attention_one(q64[s, h], K, V, scale)
+    return out

@@ -88,9 +88,13 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   constexpr int kSt = ring_stages<KV8>();
   static_assert(!KV8 || D == 128, "fp8 pools: head size 128 (one 128-byte line per row)");
   // fp8 pools run the products in fp16 whatever the query type: codes widen
-  // to fp16 in one conversion, and bf16 queries of ordinary magnitude
-  // ([6.1e-5, 65504]) are exact in fp16
+  // to fp16 in one conversion. A bf16 query group is first multiplied by the
+  // power of two 2^-e that puts its largest magnitude in [2^14, 2^15), which
+  // makes the fp16 conversion exact over bf16's whole range (bf16 has 8
+  // significant bits, fp16 11; only elements below 2^-28 of the group's
+  // largest reach fp16's subnormals), and 2^e goes into the logit scale.
   using MT = typename std::conditional<KV8, __half, T>::type;
+  constexpr bool kQRescale = KV8 && std::is_same<T, __nv_bfloat16>::value;
   constexpr int KSTEPS = D / 16;
   static_assert(G == 2 || G == 4 || G == 8 || (KV8 && G == 1), "group");
 
@@ -229,8 +233,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     T* out = reinterpret_cast<T*>(a.out);
     int it = 0;                                // tiles consumed so far: the ring position
     bool run = true;
-    // query fragments of item idx (its sequence and KV head)
-    auto q_frags = [&](int idx, uint32_t (&qd)[KSTEPS][2]) {
+    // query fragments of item idx (its sequence and KV head), and the factor
+    // qmul by which the products of these fragments must be multiplied
+    auto q_frags = [&](int idx, uint32_t (&qd)[KSTEPS][2], float& qmul) {
       const int kv = (idx / a.num_splits) % Hkv, sq = idx / a.num_splits / Hkv;
       const T* qb = reinterpret_cast<const T*>(a.q) + ((int64_t)sq * Hq + (int64_t)kv * G) * D;
 #pragma unroll
@@ -241,28 +246,63 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           // applied to K the same way) so a lane's codes are contiguous
           const int d0 = KV8 ? c * (D / 4) + ks * 4 : ks * 16 + 2 * c;
           const int d1 = KV8 ? d0 + 2 : d0 + 8;
-          qd[ks][0] = to_mma_pair<T, MT>(*reinterpret_cast<const uint32_t*>(qb + n * D + d0));
-          qd[ks][1] = to_mma_pair<T, MT>(*reinterpret_cast<const uint32_t*>(qb + n * D + d1));
+          qd[ks][0] = *reinterpret_cast<const uint32_t*>(qb + n * D + d0);
+          qd[ks][1] = *reinterpret_cast<const uint32_t*>(qb + n * D + d1);
         } else {
           qd[ks][0] = qd[ks][1] = 0u;
         }
+      }
+      qmul = 1.f;
+      if constexpr (kQRescale) {
+        // the lanes of the warp hold the whole group between them
+        float mx = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float2 f = MmaOps<T>::unpack(qd[ks][j]);
+            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+          }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        // e = floor(log2(mx)) - 14, kept >= -126 so 2^e and 2^-e are normal
+        // fp32 values (a group below 2^-112 only loses digits it cannot use)
+        const int e = mx > 0.f ? max(((__float_as_int(mx) >> 23) & 0xff) - 127 - 14, -126) : 0;
+        const float down = __int_as_float((127 - e) << 23);
+        qmul = __int_as_float((127 + e) << 23);
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float2 f = MmaOps<T>::unpack(qd[ks][j]);
+            qd[ks][j] = MmaOps<MT>::pack(f.x * down, f.y * down);
+          }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) qd[ks][j] = to_mma_pair<T, MT>(qd[ks][j]);
       }
     };
     // MULTI: the next item's query is loaded one item ahead, so its latency
     // hides behind the current item's tiles
     uint32_t qn[KSTEPS][2];
-    if (MULTI && (int)blockIdx.x < n_items) q_frags(blockIdx.x, qn);
+    float qmul_n = 1.f;
+    if (MULTI && (int)blockIdx.x < n_items) q_frags(blockIdx.x, qn, qmul_n);
     for (int idx = blockIdx.x; run && idx < n_items;
          idx = MULTI ? idx + (int)gridDim.x : n_items) {
     const Item im = item_at(idx);
     uint32_t qf[KSTEPS][2];
+    float qmul = 1.f;
     if (MULTI) {
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
         qf[ks][0] = qn[ks][0];
         qf[ks][1] = qn[ks][1];
       }
-      if (idx + (int)gridDim.x < n_items) q_frags(idx + (int)gridDim.x, qn);
+      qmul = qmul_n;
+      if (idx + (int)gridDim.x < n_items) q_frags(idx + (int)gridDim.x, qn, qmul_n);
     }
     if (im.zero_out) {
       if (im.L != 0 && threadIdx.x == 0) latch(a.err, PA_ERR_OUT_OF_RANGE);
@@ -278,7 +318,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     float o[KSTEPS][4];
 #pragma unroll
     for (int i = 0; i < KSTEPS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    if (!MULTI) q_frags(idx, qf);
+    if (!MULTI) q_frags(idx, qf, qmul);
+    const float sl2q = sl2 * qmul;
     bool ok = true;
     for (int i = 0; i < ntiles; ++i, ++it) {
       const int st = it % kSt;
@@ -347,10 +388,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           }
         }
         const bool okA = (okm >> n) & 1u, okB = (okm >> (n + 8)) & 1u;
-        const float x0 = okA ? sacc[0] * sl2 : kNegInfM;   // row n,   head 2c
-        const float x1 = okA ? sacc[1] * sl2 : kNegInfM;   // row n,   head 2c+1
-        const float x2 = okB ? sacc[2] * sl2 : kNegInfM;   // row n+8, head 2c
-        const float x3 = okB ? sacc[3] * sl2 : kNegInfM;   // row n+8, head 2c+1
+        const float x0 = okA ? sacc[0] * sl2q : kNegInfM;   // row n,   head 2c
+        const float x1 = okA ? sacc[1] * sl2q : kNegInfM;   // row n,   head 2c+1
+        const float x2 = okB ? sacc[2] * sl2q : kNegInfM;   // row n+8, head 2c
+        const float x3 = okB ? sacc[3] * sl2q : kNegInfM;   // row n+8, head 2c+1
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {

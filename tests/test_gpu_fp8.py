@@ -125,3 +125,34 @@ def test_fp8_partitioning_query():
     with pytest.raises(pa.PagedAttnError):
         pa.pa_decode_fp8_partitioning(64, 32, 32, 128, 16, bf, 2049, -1)
 
+
+@pytest.mark.parametrize("G", [1, 8])
+@pytest.mark.parametrize("qmul,smul,window", [(1e6, 1.0, 0), (1e6, 1.0, 300), (1e-5, 1e5, 0),
+                                              (3e30, 1e-30, 0), (1e-30, 1e30, 0)])
+def test_fp8_decode_bf16_queries_over_their_whole_range(G, qmul, smul, window):
+    # bf16 queries far outside fp16's range (1e6, 3e30: the products run in
+    # fp16 on the tensor-core path) and far below its normal range (1e-5,
+    # 1e-30), with the softmax scale adjusted so the logits stay meaningful
+    # (smul) or become one-hot (1e6); windowed and not
+    Hkv = 2
+    cfg = workloads.DecodeConfig("r8", 5, Hkv * G, Hkv, 128, 16, "bf16", seed=31 + G)
+    inp = workloads.make_decode_inputs(cfg, context_lens=[0, 15, 63, 400, 900])
+    q = (inp.q.float() * qmul).to(torch.bfloat16)
+    scale = inp.scale * smul
+    gen = torch.Generator().manual_seed(77 + G)
+    ks, vs = 1 / 48, 1 / 40
+    kc = fp8_pool((inp.num_blocks, Hkv, 16, 128), ks, gen)
+    vc = fp8_pool((inp.num_blocks, Hkv, 16, 128), vs, gen)
+    want = oracle.decode_attention_fp8(np_(q), kc.numpy(), vc.numpy(), inp.block_tables.numpy(),
+                                       inp.seq_lens.numpy(), scale, Hkv, 16, "bf16", ks, vs,
+                                       window=window)
+    args = (q.to(DEV), kc.to(DEV), vc.to(DEV), inp.block_tables.to(DEV), inp.seq_lens.to(DEV),
+            scale, Hkv, ks, vs)
+    if window:
+        out = pa.pa_decode_attention_fp8_window(*args, window, max_seq_len=inp.max_seq_len)
+    else:
+        out = pa.pa_decode_attention_fp8(*args, max_seq_len=inp.max_seq_len)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    assert max_abs_err(out, want) <= TOL["bf16"]
+    assert pa.pa_get_device_error() == 0

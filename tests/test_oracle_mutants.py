@@ -10,6 +10,7 @@ import oracle
 import oracle.paged_attention as opa
 import oracle.block_manager as obm
 import tests.test_oracle_attention as ta
+import tests.test_oracle_block_scales as tb
 import tests.test_oracle_fp8 as tf
 import tests.test_oracle_pins as tp
 import tests.test_oracle_window as tw
@@ -157,6 +158,75 @@ def _quant_scale_f64(x, dtype, scale):
     return opa.e4m3_encode(q.astype(np.float32))
 
 
+def _bs_floor(amax):
+    a = float(amax)
+    if a == 0.0:
+        return 1.0
+    if np.isinf(a):
+        return 2.0 ** 127
+    k = min(max(int(np.floor(np.log2(a))) - 7, -126), 127)   # amax lands in [128, 256)
+    return 2.0 ** k
+
+
+def _bs_write(first_only=False, one_pass=False):
+    def write(k, v, slots, kc8, vc8, ks, vs, B, dtype):
+        slots = np.asarray(slots, dtype=np.int64)
+        T, Hkv = len(slots), kc8.shape[1]
+
+        def fix(t):
+            s0 = int(slots[t])
+            n = 1
+            while not first_only and n < B and t + n < T and int(slots[t + n]) == s0 + n:
+                n += 1
+            for h in range(Hkv):
+                for src, dst in ((k, ks), (v, vs)):
+                    run = np.abs(opa.upcast(np.ascontiguousarray(src[t:t + n, h]), dtype))
+                    dst[s0 // B, h] = opa.block_scale_e4m3(float(run.max()))
+
+        def put(t):
+            s = int(slots[t])
+            for h in range(Hkv):
+                kc8[s // B, h, s % B] = opa.quantize_e4m3(k[t, h], dtype, float(ks[s // B, h]))
+                vc8[s // B, h, s % B] = opa.quantize_e4m3(v[t, h], dtype, float(vs[s // B, h]))
+
+        if one_pass:                                   # fixes and writes in call order
+            for t in range(T):
+                if slots[t] >= 0 and slots[t] % B == 0:
+                    fix(t)
+                if slots[t] >= 0:
+                    put(t)
+            return
+        for t in range(T):
+            if slots[t] >= 0 and slots[t] % B == 0:
+                fix(t)
+        for t in range(T):
+            if slots[t] >= 0:
+                put(t)
+    return write
+
+
+def _bs_attn(logical_index=False, k_for_v=False):
+    def attn(q, kc8, vc8, ks, vs, tables, lens, scale, Hkv, B, dtype, seqs=None, heads=None,
+             window=0):
+        S, Hq, D = q.shape
+        g = Hq // Hkv
+        q64 = opa.upcast(q, dtype)
+        out = np.zeros((S, Hq, D))
+        for s in range(S):
+            L = int(lens[s])
+            j = np.arange(opa.window_start(L, window), L)
+            blk = np.asarray(tables[s], dtype=np.int64)[j // B]
+            sidx = j // B if logical_index else blk           # scale of the wrong block
+            for h in range(Hq):
+                kvh = h // g
+                K = opa.e4m3_decode(kc8[blk, kvh, j % B]) * np.float64(ks)[sidx, kvh][:, None]
+                vsrc = ks if k_for_v else vs
+                V = opa.e4m3_decode(vc8[blk, kvh, j % B]) * np.float64(vsrc)[sidx, kvh][:, None]
+                out[s, h] = opa.decode_attention_one(q64[s, h], K, V, scale)
+        return out
+    return attn
+
+
 class _RemoveSkippedCeil(obm.OracleBlockManager):
     def remove_skipped(self, seq, window):
         lo = opa.window_start(self.lens[seq], window)
@@ -233,6 +303,15 @@ PIN_TESTS = [
     tf.test_quantize_largest_code_for_448_scales,
     tf.test_quantize_rounds_the_quotient_to_fp32_before_encoding,
     tf.test_quantize_rounds_the_scale_to_fp32,
+    tb.test_block_scale_closed_forms,
+    tb.test_block_scale_is_the_smallest_power_of_two_that_fits_128,
+    tb.test_decode_write_fixes_the_scale_at_row_0_and_reuses_it_later,
+    tb.test_a_run_of_consecutive_slots_fixes_the_scale_from_its_largest_value,
+    tb.test_the_run_ends_at_a_gap_and_scales_are_fixed_before_any_token_is_written,
+    lambda: tb.test_values_on_the_code_grid_round_trip_exactly("bf16"),
+    tb.test_block_scaled_attention_matches_brute_force,
+    tb.test_equal_block_scales_reduce_to_the_per_pool_scale,
+    tb.test_block_scaled_attention_is_invariant_under_relabelling,
 ]
 
 MUTANTS = {
@@ -257,13 +336,20 @@ MUTANTS = {
     "quant_scale_f64": [("quantize_e4m3", _quant_scale_f64)],
     "remove_skipped_ceil": [("OracleBlockManager", _RemoveSkippedCeil)],
     "remove_skipped_frees_shared": [("OracleBlockManager", _RemoveSkippedFreesShared)],
+    "block_scale_floor": [("block_scale_e4m3", _bs_floor)],
+    "block_scale_first_token_only": [("reshape_and_cache_fp8_block_scaled",
+                                      _bs_write(first_only=True))],
+    "block_scale_one_pass": [("reshape_and_cache_fp8_block_scaled", _bs_write(one_pass=True))],
+    "block_scale_of_logical_block": [("decode_attention_fp8_block_scaled",
+                                      _bs_attn(logical_index=True))],
+    "block_scale_k_for_v": [("decode_attention_fp8_block_scaled", _bs_attn(k_for_v=True))],
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_planted_mistake(name, monkeypatch):
     for attr, fn in MUTANTS[name]:
-        for mod in (oracle, opa, obm, tp, tw, tf):
+        for mod in (oracle, opa, obm, tp, tw, tf, tb):
             if hasattr(mod, attr):
                 monkeypatch.setattr(mod, attr, fn)
     caught = []
