@@ -311,6 +311,64 @@ PA_API int pa_decode_attention_fp8(const void* q, const void* key_cache,
                                    void* workspace, int64_t workspace_bytes, void* stream);
 
 /*
+ * fp8 blocks that carry their own scales ([P1] §3.5 kv_quant_mode and §7.4,
+ * the compression-aware block: the quantisation belongs to the block). The
+ * same E4M3 pools as above, plus two fp32 arrays k_scales, v_scales
+ * [num_blocks][num_kv_heads] (device, caller-owned, 16-byte aligned): the
+ * scale of (block b, KV head h) is a power of two,
+ *     value = code * scales[b][h].
+ * Reading taken (the pages fix no format): a block's scales are fixed by
+ * the KV write that stores its first row (row 0). That write takes the
+ * token landing there and the tokens right after it in the same call whose
+ * slots continue it inside the block (a prefill chunk fills up to
+ * block_size rows at once; a decode step writes one), and from the largest
+ * |value| amax among them (per head, K and V separately; NaN left out) sets
+ *     scale = 2^k,  k = ceil(log2(amax)) - 7 kept in [-126, 127]
+ *     (amax = 0 gives 1),
+ * so those tokens' largest magnitude lands in (64, 128] and later tokens of
+ * the block have 3.5x headroom before the largest code (448) saturates. Every
+ * token of the call is then quantised with its block's scale, as in
+ * pa_reshape_and_cache_fp8 (IEEE fp32 division, nearest even, saturated).
+ * Blocks whose first row the call does not write keep their scales. When a
+ * block is copied for copy-on-write, copy its scales with it: pa_copy_blocks
+ * on the scale arrays with block_bytes = num_kv_heads * 4.
+ *
+ * pa_reshape_and_cache_fp8_scaled — the write above: two launches on
+ * `stream` (the scales of the blocks begun in this call, then the codes).
+ * Arguments as in pa_reshape_and_cache_fp8, with k_scales / v_scales in
+ * place of the pool scales. Slots out of the pool are skipped and latch
+ * PA_ERR_OUT_OF_RANGE; two tokens of a call mapped to one slot are a caller
+ * error.
+ *
+ * pa_decode_attention_fp8_scaled — decode attention over such pools:
+ * K_s[j] = code * k_scales[b][h], V_s[j] = code * v_scales[b][h] for the
+ * block b holding token j. `window` as in pa_decode_attention_fp8_window
+ * (0 = the whole sequence); workspace sized by
+ * pa_decode_window_workspace_bytes with the same arguments; partitioning as
+ * pa_decode_fp8_partitioning reports. The tensor-core kernel multiplies each
+ * token's softmax weight by its block's V scale relative to the first
+ * attended block's before rounding it to fp16, so V scales within one
+ * sequence more than 2^16 apart saturate that weight (a precision limit, not
+ * an error).
+ */
+PA_API int pa_reshape_and_cache_fp8_scaled(const void* k, const void* v, int64_t num_tokens,
+                                           int num_kv_heads, int head_size, int dtype,
+                                           const int64_t* slot_mapping, void* key_cache,
+                                           void* value_cache, float* k_scales,
+                                           float* v_scales, int64_t num_blocks,
+                                           int block_size, void* stream);
+PA_API int pa_decode_attention_fp8_scaled(const void* q, const void* key_cache,
+                                          const void* value_cache, const float* k_scales,
+                                          const float* v_scales, const int32_t* block_tables,
+                                          int64_t block_tables_stride,
+                                          const int32_t* seq_lens, int num_seqs,
+                                          int num_q_heads, int num_kv_heads, int head_size,
+                                          int block_size, int64_t num_blocks, int dtype,
+                                          float scale, int window, int max_seq_len,
+                                          int partition_size, void* out, void* workspace,
+                                          int64_t workspace_bytes, void* stream);
+
+/*
  * Sliding-window decode. The pages name the window through the blocks the
  * allocator may release ("PagedAttention 核心创新深度分析" §3.2
  * allocate_slots, phase 1, and §3.3.1 get_num_blocks_to_allocate: skipped
@@ -394,7 +452,9 @@ PA_API int pa_decode_attention_fp8_window(const void* q, const void* key_cache,
  *               anything is launched. Without it the kernel range-checks each
  *               pair (skipping and latching PA_ERR_OUT_OF_RANGE) and aliasing
  *               is the caller's responsibility.
- * block_bytes   a positive multiple of 16.
+ * block_bytes   a positive multiple of 4 (16-byte vectors are moved when it
+ *               is a multiple of 16, 4-byte words otherwise, e.g. the
+ *               per-block scale arrays of fp8 pools: num_kv_heads * 4).
  */
 PA_API int pa_copy_blocks(void* const* key_caches, void* const* value_caches,
                    int num_layers, const int64_t* src_dst_pairs,

@@ -57,6 +57,12 @@ SIGNATURES = {
                                         _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_f,
                                         _c_f, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i64,
                                         _c_p], _c_i32),
+    "pa_reshape_and_cache_fp8_scaled": ([_c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_p, _c_p,
+                                         _c_p, _c_p, _c_p, _c_i64, _c_i32, _c_p], _c_i32),
+    "pa_decode_attention_fp8_scaled": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_p,
+                                        _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32,
+                                        _c_f, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i64, _c_p],
+                                       _c_i32),
     "pa_copy_blocks": ([_c_p, _c_p, _c_i32, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p], _c_i32),
     "pa_get_device_error": ([_c_p, _c_p], _c_i32),
     "pa_selftest_bounded_wait": ([_c_p, ctypes.c_longlong, _c_p], _c_i32),

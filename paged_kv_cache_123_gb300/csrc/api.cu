@@ -152,9 +152,9 @@ int run_decode(const void* q, const void* key_cache, const void* value_cache,
                const int32_t* block_tables, int64_t block_tables_stride,
                const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
                int head_size, int block_size, int64_t num_blocks, int dtype, float scale,
-               bool fp8, float k_scale, float v_scale, int window, int max_seq_len,
-               int partition_size, void* out, void* workspace, int64_t workspace_bytes,
-               void* stream);
+               bool fp8, float k_scale, float v_scale, const float* k_scales,
+               const float* v_scales, int window, int max_seq_len, int partition_size,
+               void* out, void* workspace, int64_t workspace_bytes, void* stream);
 
 int check_decode_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
                        int block_size, int max_seq_len) {
@@ -307,7 +307,7 @@ int pa_decode_attention(const void* q, const void* key_cache, const void* value_
                         int64_t workspace_bytes, void* stream) {
   return run_decode(q, key_cache, value_cache, block_tables, block_tables_stride, seq_lens,
                     num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
-                    dtype, scale, false, 1.f, 1.f, 0, max_seq_len, partition_size, out,
+                    dtype, scale, false, 1.f, 1.f, nullptr, nullptr, 0, max_seq_len, partition_size, out,
                     workspace, workspace_bytes, stream);
 }
 
@@ -336,7 +336,7 @@ int pa_decode_attention_window(const void* q, const void* key_cache, const void*
   if (window < 0) return PA_ERR_SHAPE;
   return run_decode(q, key_cache, value_cache, block_tables, block_tables_stride, seq_lens,
                     num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
-                    dtype, scale, false, 1.f, 1.f, window, max_seq_len, partition_size, out,
+                    dtype, scale, false, 1.f, 1.f, nullptr, nullptr, window, max_seq_len, partition_size, out,
                     workspace, workspace_bytes, stream);
 }
 
@@ -465,8 +465,32 @@ int pa_reshape_and_cache_fp8(const void* k, const void* v, int64_t num_tokens, i
   if (st != PA_OK) return st;
   return check_launch(pa::launch_reshape_and_cache_fp8(
       k, v, num_tokens, num_kv_heads, head_size, dtype, slot_mapping, key_cache, value_cache,
-      num_blocks, block_size, k_scale, v_scale, g_sm_count[dev], (cudaStream_t)stream,
-      g_err_ptr[dev]));
+      num_blocks, block_size, k_scale, v_scale, nullptr, nullptr, g_sm_count[dev],
+      (cudaStream_t)stream, g_err_ptr[dev]));
+}
+
+int pa_reshape_and_cache_fp8_scaled(const void* k, const void* v, int64_t num_tokens,
+                                    int num_kv_heads, int head_size, int dtype,
+                                    const int64_t* slot_mapping, void* key_cache,
+                                    void* value_cache, float* k_scales, float* v_scales,
+                                    int64_t num_blocks, int block_size, void* stream) {
+  if (elt_bytes(dtype) == 0) return PA_ERR_DTYPE;
+  if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks < 0 ||
+      head_size <= 0 || head_size % 16 != 0)
+    return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !key_cache || !value_cache || !k_scales || !v_scales)
+    return PA_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      !aligned16(k_scales) || !aligned16(v_scales))
+    return PA_ERR_ALIGN;
+  int dev;
+  int st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  return check_launch(pa::launch_reshape_and_cache_fp8(
+      k, v, num_tokens, num_kv_heads, head_size, dtype, slot_mapping, key_cache, value_cache,
+      num_blocks, block_size, 1.f, 1.f, k_scales, v_scales, g_sm_count[dev],
+      (cudaStream_t)stream, g_err_ptr[dev]));
 }
 
 int pa_decode_attention_fp8(const void* q, const void* key_cache, const void* value_cache,
@@ -478,8 +502,25 @@ int pa_decode_attention_fp8(const void* q, const void* key_cache, const void* va
                             int64_t workspace_bytes, void* stream) {
   return run_decode(q, key_cache, value_cache, block_tables, block_tables_stride, seq_lens,
                     num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
-                    dtype, scale, true, k_scale, v_scale, 0, max_seq_len, partition_size, out,
+                    dtype, scale, true, k_scale, v_scale, nullptr, nullptr, 0, max_seq_len, partition_size, out,
                     workspace, workspace_bytes, stream);
+}
+
+int pa_decode_attention_fp8_scaled(const void* q, const void* key_cache,
+                                   const void* value_cache, const float* k_scales,
+                                   const float* v_scales, const int32_t* block_tables,
+                                   int64_t block_tables_stride, const int32_t* seq_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_size, int block_size, int64_t num_blocks, int dtype,
+                                   float scale, int window, int max_seq_len, int partition_size,
+                                   void* out, void* workspace, int64_t workspace_bytes,
+                                   void* stream) {
+  if (window < 0) return PA_ERR_SHAPE;
+  if (num_seqs > 0 && (!k_scales || !v_scales)) return PA_ERR_NULL;
+  return run_decode(q, key_cache, value_cache, block_tables, block_tables_stride, seq_lens,
+                    num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
+                    dtype, scale, true, 1.f, 1.f, k_scales, v_scales, window, max_seq_len,
+                    partition_size, out, workspace, workspace_bytes, stream);
 }
 
 int pa_decode_attention_fp8_window(const void* q, const void* key_cache,
@@ -493,7 +534,7 @@ int pa_decode_attention_fp8_window(const void* q, const void* key_cache,
   if (window < 0) return PA_ERR_SHAPE;
   return run_decode(q, key_cache, value_cache, block_tables, block_tables_stride, seq_lens,
                     num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
-                    dtype, scale, true, k_scale, v_scale, window, max_seq_len, partition_size,
+                    dtype, scale, true, k_scale, v_scale, nullptr, nullptr, window, max_seq_len, partition_size,
                     out, workspace, workspace_bytes, stream);
 }
 
@@ -502,7 +543,7 @@ int pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_l
                    int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
                    void* stream) {
   if (num_layers < 0 || num_pairs < 0 || num_blocks < 0) return PA_ERR_SHAPE;
-  if (block_bytes <= 0 || block_bytes % 16 != 0) return PA_ERR_SHAPE;
+  if (block_bytes <= 0 || block_bytes % 4 != 0) return PA_ERR_SHAPE;
   if (num_pairs == 0 || num_layers == 0) return PA_OK;
   if (!key_caches || !value_caches || !src_dst_pairs) return PA_ERR_NULL;
   for (int l = 0; l < num_layers; ++l) {
@@ -574,9 +615,9 @@ int run_decode(const void* q, const void* key_cache, const void* value_cache,
                const int32_t* block_tables, int64_t block_tables_stride,
                const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
                int head_size, int block_size, int64_t num_blocks, int dtype, float scale,
-               bool fp8, float k_scale, float v_scale, int window, int max_seq_len,
-               int partition_size, void* out, void* workspace, int64_t workspace_bytes,
-               void* stream) {
+               bool fp8, float k_scale, float v_scale, const float* k_scales,
+               const float* v_scales, int window, int max_seq_len, int partition_size,
+               void* out, void* workspace, int64_t workspace_bytes, void* stream) {
   if (elt_bytes(dtype) == 0) return PA_ERR_DTYPE;
   int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size,
                               block_size, max_seq_len);
@@ -598,6 +639,7 @@ int run_decode(const void* q, const void* key_cache, const void* value_cache,
   a.num_seqs = num_seqs; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
   a.head_size = head_size; a.block_size = block_size; a.num_blocks = num_blocks;
   a.dtype = dtype; a.scale = scale; a.max_seq_len = max_seq_len; a.window = window;
+  a.k_scales = k_scales; a.v_scales = v_scales;
   partitioning(num_seqs, num_q_heads, num_kv_heads, block_size,
                covered_len(max_seq_len, window), partition_size, g_sm_count[dev],
                windowed(max_seq_len, window), fp8 && pa::mma_fp8_path_applies(a),

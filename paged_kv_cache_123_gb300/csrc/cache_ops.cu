@@ -116,13 +116,16 @@ struct CopyLayerPtrs {
 };
 
 // grid.z = layer * 2 + {0: K, 1: V}; grid.y strides over pairs; grid.x and
-// the threads stride over the 16-byte vectors of one block.
+// the threads stride over the 16-byte vectors of one block (W = uint4), or
+// over its 4-byte words when the block size is not a multiple of 16 (W =
+// uint32_t: the per-block scale arrays of fp8 pools).
+template <typename W>
 __global__ void copy_blocks_kernel(CopyLayerPtrs p, const int64_t* __restrict__ pairs,
                                    int64_t num_pairs, int64_t num_blocks,
                                    int64_t block_bytes, int* err) {
   const int layer = blockIdx.z >> 1;
   char* base = (blockIdx.z & 1) ? p.v[layer] : p.k[layer];
-  const int64_t nvec = block_bytes / 16;
+  const int64_t nvec = block_bytes / (int64_t)sizeof(W);
   for (int64_t pr = blockIdx.y; pr < num_pairs; pr += gridDim.y) {
     const int64_t src = pairs[2 * pr];
     const int64_t dst = pairs[2 * pr + 1];
@@ -130,11 +133,15 @@ __global__ void copy_blocks_kernel(CopyLayerPtrs p, const int64_t* __restrict__ 
       if (threadIdx.x == 0 && blockIdx.x == 0) latch(err, PA_ERR_OUT_OF_RANGE);
       continue;
     }
-    const uint4* s = reinterpret_cast<const uint4*>(base + src * block_bytes);
-    uint4* d = reinterpret_cast<uint4*>(base + dst * block_bytes);
+    const W* s = reinterpret_cast<const W*>(base + src * block_bytes);
+    W* d = reinterpret_cast<W*>(base + dst * block_bytes);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec;
-         i += (int64_t)gridDim.x * blockDim.x)
-      d[i] = ld_stream16(s + i);
+         i += (int64_t)gridDim.x * blockDim.x) {
+      if constexpr (sizeof(W) == 16)
+        d[i] = ld_stream16(s + i);
+      else
+        d[i] = __ldg(s + i);
+    }
   }
 }
 
@@ -144,7 +151,8 @@ cudaError_t launch_copy_blocks(void* const* kcs, void* const* vcs,
                                int64_t block_bytes, cudaStream_t st, int* err) {
   if (num_pairs == 0 || num_layers == 0) return cudaSuccess;
   const int threads = 256;
-  const int64_t nvec = block_bytes / 16;
+  const bool vec16 = block_bytes % 16 == 0;
+  const int64_t nvec = block_bytes / (vec16 ? 16 : 4);
   int64_t gx = (nvec + threads - 1) / threads;
   if (gx > 64) gx = 64;
   const int64_t gy = num_pairs < 65535 ? num_pairs : 65535;
@@ -156,8 +164,12 @@ cudaError_t launch_copy_blocks(void* const* kcs, void* const* vcs,
       p.v[i] = i < nl ? (char*)vcs[l0 + i] : nullptr;
     }
     dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)(2 * nl));
-    copy_blocks_kernel<<<grid, threads, 0, st>>>(p, pairs, num_pairs, num_blocks,
-                                                  block_bytes, err);
+    if (vec16)
+      copy_blocks_kernel<uint4><<<grid, threads, 0, st>>>(p, pairs, num_pairs, num_blocks,
+                                                         block_bytes, err);
+    else
+      copy_blocks_kernel<uint32_t><<<grid, threads, 0, st>>>(p, pairs, num_pairs, num_blocks,
+                                                            block_bytes, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -75,7 +75,19 @@ __device__ __forceinline__ bool consumers_bar_and(bool ok) {
 // three CTAs per SM, so more warps hide the conversion latency.
 // MULTI: each CTA walks several work items (items_per_cta > 1); the one-item
 // instantiation compiles to a single pass.
-template <typename T, int D, int G, bool KV8, bool MULTI>
+// SCALED (fp8 pools only): the blocks carry their own scales (a.k_scales /
+// a.v_scales [num_blocks][num_kv_heads]). The producer lane that loads a
+// block piece also reads its two scales and leaves them beside the stage
+// (0 for pieces it does not load). A consumer multiplies each row's logit by
+// its K scale, and its softmax weight by the ratio of its V scale to the
+// warp's reference, the largest V scale the warp has met so far, before the
+// weight is rounded to fp16 for the P*V product: the ratio is at most 1, so
+// no weight can overflow, and a weight loses no more than it would with one
+// pool-wide scale equal to the reference. When the reference grows the
+// warp's output is rescaled with the softmax's own rescale, and the warp's
+// output is multiplied by its reference when the warps merge; the
+// denominator sums the unscaled weights.
+template <typename T, int D, int G, bool KV8, bool MULTI, bool SCALED>
 __global__ void __launch_bounds__(kMmaThreads, KV8 ? 3 : 2)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, float k_scale, float v_scale) {
@@ -97,6 +109,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   constexpr bool kQRescale = KV8 && std::is_same<T, __nv_bfloat16>::value;
   constexpr int KSTEPS = D / 16;
   static_assert(G == 2 || G == 4 || G == 8 || (KV8 && G == 1), "group");
+  static_assert(!SCALED || (KV8 && !MULTI), "per-block scales: fp8 pools, one item per CTA");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -125,6 +138,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   // per-warp row maxima and sums for the merge of an item ([4][8] each)
   float* sm_m = reinterpret_cast<float*>(tile_mask + kSt);
   float* sm_l = sm_m + kMmaConsumers * 8;
+  // SCALED: K and V scale of each piece of each stage ([kSt][8] each)
+  float* st_ks = sm_l + kMmaConsumers * 8;
+  float* st_vs = st_ks + kSt * 8;
   struct Item {
     int s, kvh, split, L, lo, t0, t1, nsplit, ntiles;
     bool bad, zero_out;
@@ -192,18 +208,48 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       }
       const unsigned pm = __ballot_sync(0xffffffffu, mine);
       int ok = 1;
-      if (lane == 0) {
-        if (it >= kSt)
+      if constexpr (SCALED) {
+        // the scale loads are in flight while lane 0 waits for the stage;
+        // pieces that are not loaded get 0 (their rows are masked and take
+        // no part in the reference)
+        float ksv = 0.f, vsv = 0.f;
+        if (mine) {
+          ksv = a.k_scales[blk * Hkv + kvh];
+          vsv = a.v_scales[blk * Hkv + kvh];
+        }
+        if (lane == 0 && it >= kSt)
           ok = mbar_wait_bounded(empty_bar(st), ((it / kSt) - 1) & 1, abort_flag, kWaitCycles);
-        if (ok) {
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          run = false;
+          break;
+        }
+        if (lane < npieces) {
+          st_ks[st * 8 + lane] = ksv;
+          st_vs[st * 8 + lane] = vsv;
+        }
+        // the warp's scale stores come before lane 0's arrive (release), and
+        // the arrive before any lane's copy
+        __syncwarp();
+        if (lane == 0) {
           tile_mask[st] = pm;
           mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * IN_ROW);
         }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        run = false;
-        break;
+        __syncwarp();
+      } else {
+        if (lane == 0) {
+          if (it >= kSt)
+            ok = mbar_wait_bounded(empty_bar(st), ((it / kSt) - 1) & 1, abort_flag, kWaitCycles);
+          if (ok) {
+            tile_mask[st] = pm;
+            mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * IN_ROW);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          run = false;
+          break;
+        }
       }
       if (mine) {
         const uint32_t kdst = smem0 + st * STAGE_BYTES + lane * R * IN_ROW;
@@ -320,6 +366,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     for (int i = 0; i < KSTEPS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     if (!MULTI) q_frags(idx, qf, qmul);
     const float sl2q = sl2 * qmul;
+    // SCALED: the warp's reference V scale (0 until it meets a row) and its
+    // reciprocal
+    float vref = 0.f, inv_vref = 0.f;
     bool ok = true;
     for (int i = 0; i < ntiles; ++i, ++it) {
       const int st = it % kSt;
@@ -388,10 +437,29 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           }
         }
         const bool okA = (okm >> n) & 1u, okB = (okm >> (n + 8)) & 1u;
-        const float x0 = okA ? sacc[0] * sl2q : kNegInfM;   // row n,   head 2c
-        const float x1 = okA ? sacc[1] * sl2q : kNegInfM;   // row n,   head 2c+1
-        const float x2 = okB ? sacc[2] * sl2q : kNegInfM;   // row n+8, head 2c
-        const float x3 = okB ? sacc[3] * sl2q : kNegInfM;   // row n+8, head 2c+1
+        // SCALED: rows n and n+8 take the scales of their pieces, and the
+        // warp's reference grows to the largest V scale of its valid rows
+        float slA = sl2q, slB = sl2q, vA = 0.f, vB = 0.f, cv = 1.f;
+        if constexpr (SCALED) {
+          const int pA = (warp * 16 + n) / R, pB = (warp * 16 + n + 8) / R;
+          slA *= st_ks[st * 8 + pA];
+          slB *= st_ks[st * 8 + pB];
+          vA = okA ? st_vs[st * 8 + pA] : 0.f;
+          vB = okB ? st_vs[st * 8 + pB] : 0.f;
+          float vm = fmaxf(vA, vB);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1)
+            vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+          if (vm > vref) {               // warp-uniform
+            cv = vref / vm;              // 0 the first time: nothing to rescale
+            vref = vm;
+            inv_vref = 1.f / vm;
+          }
+        }
+        const float x0 = okA ? sacc[0] * slA : kNegInfM;   // row n,   head 2c
+        const float x1 = okA ? sacc[1] * slA : kNegInfM;   // row n,   head 2c+1
+        const float x2 = okB ? sacc[2] * slB : kNegInfM;   // row n+8, head 2c
+        const float x3 = okB ? sacc[3] * slB : kNegInfM;   // row n+8, head 2c+1
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -406,17 +474,29 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         const float p2 = live0 ? exp2f(x2 - mn0) : 0.f;
         const float p1 = live1 ? exp2f(x1 - mn1) : 0.f;
         const float p3 = live1 ? exp2f(x3 - mn1) : 0.f;
-        const uint32_t cA = MmaOps<MT>::pack(p0, p1);
-        const uint32_t cB = MmaOps<MT>::pack(p2, p3);
-        // the denominator sums the same rounded weights the MMA multiplies
-        const float2 fA = MmaOps<MT>::unpack(cA), fB = MmaOps<MT>::unpack(cB);
-        l0 = l0 * al0 + fA.x + fB.x;
-        l1 = l1 * al1 + fA.y + fB.y;
+        uint32_t cA, cB;
+        float aO0 = al0, aO1 = al1;      // rescale of the output
+        if constexpr (SCALED) {
+          const float rA = vA * inv_vref, rB = vB * inv_vref;   // <= 1
+          cA = MmaOps<MT>::pack(p0 * rA, p1 * rA);
+          cB = MmaOps<MT>::pack(p2 * rB, p3 * rB);
+          l0 = l0 * al0 + p0 + p2;
+          l1 = l1 * al1 + p1 + p3;
+          aO0 *= cv;
+          aO1 *= cv;
+        } else {
+          cA = MmaOps<MT>::pack(p0, p1);
+          cB = MmaOps<MT>::pack(p2, p3);
+          // the denominator sums the same rounded weights the MMA multiplies
+          const float2 fA = MmaOps<MT>::unpack(cA), fB = MmaOps<MT>::unpack(cB);
+          l0 = l0 * al0 + fA.x + fB.x;
+          l1 = l1 * al1 + fA.y + fB.y;
+        }
         m0 = mn0;
         m1 = mn1;
 #pragma unroll
         for (int mt = 0; mt < KSTEPS; ++mt) {
-          o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+          o[mt][0] *= aO0; o[mt][1] *= aO1; o[mt][2] *= aO0; o[mt][3] *= aO1;
         }
         const uint32_t pb0 = movmatrix_trans(cA);
         const uint32_t pb1 = movmatrix_trans(cB);
@@ -493,6 +573,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     // (16 KB of fp32 partial outputs; maxima and sums beside the barriers)
     const int st_last = (it - 1) % kSt;
     float* sm_o = reinterpret_cast<float*>(smem + st_last * STAGE_BYTES);   // [4][8][D]
+    const float ovs = SCALED ? vref : 1.f;
     {
 #pragma unroll
     for (int mt = 0; mt < KSTEPS; ++mt) {
@@ -500,10 +581,11 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       // head dim of M rows n and n+8 of m-tile mt
       const int da = KV8 ? n * 16 + mt : mt * 16 + n;
       const int db = KV8 ? n * 16 + 8 + mt : mt * 16 + n + 8;
-      base[(2 * c) * D + da] = o[mt][0];
-      base[(2 * c + 1) * D + da] = o[mt][1];
-      base[(2 * c) * D + db] = o[mt][2];
-      base[(2 * c + 1) * D + db] = o[mt][3];
+      // SCALED: back to the values' own units (vref is 1 otherwise)
+      base[(2 * c) * D + da] = o[mt][0] * ovs;
+      base[(2 * c + 1) * D + da] = o[mt][1] * ovs;
+      base[(2 * c) * D + db] = o[mt][2] * ovs;
+      base[(2 * c + 1) * D + db] = o[mt][3] * ovs;
     }
     if (n == 0) {
       sm_m[warp * 8 + 2 * c] = m0;
@@ -600,15 +682,15 @@ bool encode_pool_map_fp8(CUtensorMap* map, const void* base, const DecodeArgs& a
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool KV8>
+template <int D, bool KV8, bool SCALED>
 constexpr int mma_smem_bytes() {
   constexpr int kSt = ring_stages<KV8>();
   return 1024 + kSt * 2 * kTile * (KV8 ? D : 2 * D) + 2 * kSt * 8 + 4 + 4 * kSt +
-         2 * kMmaConsumers * 8 * 4 +
+         2 * kMmaConsumers * 8 * 4 + (SCALED ? 2 * kSt * 8 * 4 : 0) +
          16;
 }
 
-template <typename T, int D, int G, bool KV8, bool MULTI>
+template <typename T, int D, int G, bool KV8, bool MULTI, bool SCALED>
 cudaError_t launch_mma_tdgm(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
   if (!get_encode()) return cudaErrorNotSupported;
   CUtensorMap tk, tv;
@@ -616,13 +698,13 @@ cudaError_t launch_mma_tdgm(const DecodeArgs& a, float ks, float vs, cudaStream_
                       : (encode_pool_map(&tk, a.kc, MmaOps<T>::kTmaType, a) &&
                          encode_pool_map(&tv, a.vc, MmaOps<T>::kTmaType, a));
   if (!ok) return cudaErrorInvalidValue;
-  constexpr int smem = mma_smem_bytes<D, KV8>();
+  constexpr int smem = mma_smem_bytes<D, KV8, SCALED>();
   static_assert(2 * kTile * (KV8 ? D : 2 * D) >= kMmaConsumers * 8 * D * 4,
                 "an item's merge must fit in one stage");
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, []() {
-    attr_err = cudaFuncSetAttribute(decode_mma_kernel<T, D, G, KV8, MULTI>,
+    attr_err = cudaFuncSetAttribute(decode_mma_kernel<T, D, G, KV8, MULTI, SCALED>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -632,8 +714,8 @@ cudaError_t launch_mma_tdgm(const DecodeArgs& a, float ks, float vs, cudaStream_
   const int per = (MULTI && a.items_per_cta > 1) ? a.items_per_cta : 1;
   const int64_t grid = (n_items + per - 1) / per;
   if (n_items > 0x7fffffff) return cudaErrorInvalidValue;
-  decode_mma_kernel<T, D, G, KV8, MULTI><<<(unsigned)grid, kMmaThreads, smem, st>>>(a, tk, tv,
-                                                                                   ks, vs);
+  decode_mma_kernel<T, D, G, KV8, MULTI, SCALED><<<(unsigned)grid, kMmaThreads, smem, st>>>(
+      a, tk, tv, ks, vs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_combine(a, st);
@@ -642,9 +724,12 @@ cudaError_t launch_mma_tdgm(const DecodeArgs& a, float ks, float vs, cudaStream_
 template <typename T, int D, int G, bool KV8>
 cudaError_t launch_mma_tdg(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
   if constexpr (D == 128 && !KV8) {
-    if (a.items_per_cta > 1) return launch_mma_tdgm<T, D, G, KV8, true>(a, ks, vs, st);
+    if (a.items_per_cta > 1) return launch_mma_tdgm<T, D, G, KV8, true, false>(a, ks, vs, st);
   }
-  return launch_mma_tdgm<T, D, G, KV8, false>(a, ks, vs, st);
+  if constexpr (KV8) {
+    if (a.k_scales != nullptr) return launch_mma_tdgm<T, D, G, KV8, false, true>(a, 1.f, 1.f, st);
+  }
+  return launch_mma_tdgm<T, D, G, KV8, false, false>(a, ks, vs, st);
 }
 
 template <typename T, int D, bool KV8>

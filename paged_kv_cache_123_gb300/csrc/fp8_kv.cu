@@ -2,12 +2,16 @@
 // an fp8 pool.
 //
 // "PagedAttention 核心创新深度分析" §3.5 gives each attention layer's KV spec a
-// quantisation mode, and its outlook (§7) names quantisation-aware blocks; the
-// pages fix no format. This library stores OCP E4M3 codes with one fp32 scale
-// per pool (K and V): code = e4m3(x / scale), rounded to nearest even and
-// saturated to +-448 by the hardware conversion; value = code * scale. The
-// pool layout is the 16-bit one with 1-byte elements, so a slot, a block and
-// the block table mean the same thing; half the bytes per token are read.
+// quantisation mode, and its outlook (§7.4) names compression-aware blocks;
+// the pages fix no format. This library stores OCP E4M3 codes, code =
+// e4m3(x / scale) rounded to nearest even and saturated to +-448 by the
+// hardware conversion, value = code * scale, with either one fp32 scale per
+// pool (K and V), or one power-of-two scale per (block, KV head) that the
+// write storing a block's first row fixes from the largest magnitude of the
+// tokens it puts there (two passes: fix_block_scales_kernel, then the
+// quantising write). The pool layout is the 16-bit one with 1-byte elements,
+// so a slot, a block and the block table mean the same thing; half the bytes
+// per token are read.
 //
 // Attention over fp8 pools runs on the tensor-core kernel of decode_mma.cu
 // for 16-bit queries, head size 128 and blocks of at least 8 tokens (any
@@ -59,16 +63,84 @@ __device__ __forceinline__ void e4m3x8_to_f32(uint2 u, float* f) {
   }
 }
 
+// Power-of-two scale of a block whose first tokens' largest magnitude is
+// amax: 2^k with k = ceil(log2(amax)) - 7 kept in [-126, 127], so amax lands
+// in (64, 128]; 1 for amax = 0, 2^127 for an infinite amax. Integer work on
+// the fp32 encoding: the biased exponent gives floor(log2), and a nonzero
+// mantissa moves it up by one.
+__device__ __forceinline__ float block_scale_of(float amax) {
+  if (amax == 0.f) return 1.f;
+  const uint32_t b = __float_as_uint(amax);
+  const int ef = (int)(b >> 23);
+  int k;
+  if (ef == 0) {
+    k = -126;                                   // below 2^-126: clamped
+  } else if (ef == 255) {
+    k = 127;
+  } else {
+    const int c = (ef - 127) + ((b & 0x7fffffu) != 0u);
+    k = min(max(c - 7, -126), 127);
+  }
+  return __uint_as_float((uint32_t)(k + 127) << 23);
+}
+
+// First pass of the block-scaled KV write: one warp per (token, KV head)
+// whose slot is row 0 of its block. The run is that token and the tokens
+// right after it in the call whose slots continue it inside the block (at
+// most block_size); the largest |value| over the run fixes the block's K
+// (and separately V) scale. NaN values are left out of the maximum (fmaxf
+// keeps the other operand), and slots past the pool are left to the second
+// pass, which skips and reports them.
+template <typename T>
+__global__ void fix_block_scales_kernel(const T* __restrict__ k, const T* __restrict__ v,
+                                        int64_t num_tokens, int num_kv_heads, int D,
+                                        const int64_t* __restrict__ slots, int64_t num_blocks,
+                                        int block_size, float* __restrict__ k_scales,
+                                        float* __restrict__ v_scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t limit = num_blocks * block_size;
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       w < num_tokens * num_kv_heads; w += warps) {
+    const int64_t t = w / num_kv_heads;
+    const int h = (int)(w - t * num_kv_heads);
+    const int64_t s0 = slots[t];
+    if (s0 < 0 || s0 >= limit || s0 % block_size != 0) continue;
+    int n = 1;
+    while (n < block_size && t + n < num_tokens && slots[t + n] == s0 + n) ++n;
+    float ka = 0.f, va = 0.f;
+    for (int64_t e = lane; e < (int64_t)n * D; e += 32) {
+      const int64_t r = e / D;
+      const int64_t off = ((t + r) * num_kv_heads + h) * D + (e - r * D);
+      ka = fmaxf(ka, fabsf(static_cast<float>(k[off])));
+      va = fmaxf(va, fabsf(static_cast<float>(v[off])));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, o));
+      va = fmaxf(va, __shfl_xor_sync(0xffffffffu, va, o));
+    }
+    if (lane == 0) {
+      const int64_t idx = (s0 / block_size) * num_kv_heads + h;
+      k_scales[idx] = block_scale_of(ka);
+      v_scales[idx] = block_scale_of(va);
+    }
+  }
+}
+
 // One thread per 8 elements of a (token, kv head) row, K and V together:
-// widen, divide by the pool's scale (IEEE fp32), convert to E4M3 (nearest
-// even, saturating), store 8 bytes at the slot's row.
+// widen, divide by the scale (IEEE fp32), convert to E4M3 (nearest even,
+// saturating), store 8 bytes at the slot's row. The scale is the pool's
+// (k_scale, v_scale), or, when k_scales is given, the block's entry of
+// k_scales / v_scales [num_blocks][num_kv_heads].
 template <typename T>
 __global__ void reshape_and_cache_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v,
                                              int64_t num_tokens, int num_kv_heads, int D,
                                              const int64_t* __restrict__ slots,
                                              uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
                                              int64_t num_blocks, int block_size, float k_scale,
-                                             float v_scale, int* err) {
+                                             float v_scale, const float* __restrict__ k_scales,
+                                             const float* __restrict__ v_scales, int* err) {
   const int per_row = D / 8;
   const int64_t n = num_tokens * num_kv_heads * per_row;
   const int64_t limit = num_blocks * block_size;
@@ -88,6 +160,11 @@ __global__ void reshape_and_cache_fp8_kernel(const T* __restrict__ k, const T* _
     const int64_t row = slot - blk * block_size;
     const int64_t src = (t * num_kv_heads + h) * D + c * 8;
     const int64_t dst = ((blk * num_kv_heads + h) * block_size + row) * D + c * 8;
+    float ksc = k_scale, vsc = v_scale;
+    if (k_scales != nullptr) {
+      ksc = k_scales[blk * num_kv_heads + h];
+      vsc = v_scales[blk * num_kv_heads + h];
+    }
     float fk[8], fv[8];
     Wide<T>::load8(k + src, fk);
     Wide<T>::load8(v + src, fv);
@@ -99,10 +176,10 @@ __global__ void reshape_and_cache_fp8_kernel(const T* __restrict__ k, const T* _
       for (int j = 0; j < 2; ++j) {
         const int e = 4 * w + 2 * j;
         const __nv_fp8x2_storage_t pk = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(fk[e], k_scale), __fdiv_rn(fk[e + 1], k_scale)),
+            make_float2(__fdiv_rn(fk[e], ksc), __fdiv_rn(fk[e + 1], ksc)),
             __NV_SATFINITE, __NV_E4M3);
         const __nv_fp8x2_storage_t pv = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(fv[e], v_scale), __fdiv_rn(fv[e + 1], v_scale)),
+            make_float2(__fdiv_rn(fv[e], vsc), __fdiv_rn(fv[e + 1], vsc)),
             __NV_SATFINITE, __NV_E4M3);
         ak |= (uint32_t)pk << (16 * j);
         av |= (uint32_t)pv << (16 * j);
@@ -119,16 +196,36 @@ cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, int64_t n
                                          int num_kv_heads, int head_size, int dtype,
                                          const int64_t* slots, void* kc, void* vc,
                                          int64_t num_blocks, int block_size, float k_scale,
-                                         float v_scale, int sm_count, cudaStream_t st, int* err) {
+                                         float v_scale, float* k_scales, float* v_scales,
+                                         int sm_count, cudaStream_t st, int* err) {
   if (num_tokens == 0) return cudaSuccess;
-  const int64_t n = num_tokens * num_kv_heads * (head_size / 8);
   const int threads = 256;
+  if (k_scales != nullptr) {
+    // pass 1: the scales of the blocks whose first row this call writes
+    const int64_t warps = num_tokens * num_kv_heads;
+    int64_t blocks = (warps + threads / 32 - 1) / (threads / 32);
+    if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
+#define PA_FIX_SCALES(TT)                                                                \
+  fix_block_scales_kernel<TT><<<(unsigned)blocks, threads, 0, st>>>(                     \
+      (const TT*)k, (const TT*)v, num_tokens, num_kv_heads, head_size, slots, num_blocks, \
+      block_size, k_scales, v_scales)
+    switch (dtype) {
+      case PA_F32: PA_FIX_SCALES(float); break;
+      case PA_F16: PA_FIX_SCALES(__half); break;
+      case PA_BF16: PA_FIX_SCALES(__nv_bfloat16); break;
+      default: return cudaErrorInvalidValue;
+    }
+#undef PA_FIX_SCALES
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t n = num_tokens * num_kv_heads * (head_size / 8);
   int64_t blocks = (n + threads - 1) / threads;
   if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
 #define PA_FP8_WRITE(TT)                                                                 \
   reshape_and_cache_fp8_kernel<TT><<<(unsigned)blocks, threads, 0, st>>>(                \
       (const TT*)k, (const TT*)v, num_tokens, num_kv_heads, head_size, slots, (uint8_t*)kc, \
-      (uint8_t*)vc, num_blocks, block_size, k_scale, v_scale, err)
+      (uint8_t*)vc, num_blocks, block_size, k_scale, v_scale, k_scales, v_scales, err)
   switch (dtype) {
     case PA_F32: PA_FP8_WRITE(float); break;
     case PA_F16: PA_FP8_WRITE(__half); break;
@@ -144,8 +241,12 @@ constexpr int kFp8Warps = 4;
 
 // One CTA per (partition, kv head, sequence); lane groups of D/8 lanes own a
 // token row, 8 codes (8 bytes) per lane; the G query heads of the group share
-// each row read. Same online softmax and merges as decode_simt.cu.
-template <typename T, int D, int G, int U>
+// each row read. Same online softmax and merges as decode_simt.cu. SCALED:
+// the blocks carry their own scales (a.k_scales / a.v_scales), read with the
+// token's codes; a token's logit is multiplied by its block's K scale and its
+// softmax weight by its block's V scale before the weighted sum (the
+// denominator sums the weights alone).
+template <typename T, int D, int G, int U, bool SCALED>
 __global__ void __launch_bounds__(kFp8Warps * 32)
 decode_fp8_kernel(const DecodeArgs a, float k_scale, float v_scale) {
   constexpr int TPT = D / 8;
@@ -198,18 +299,24 @@ decode_fp8_kernel(const DecodeArgs a, float k_scale, float v_scale) {
   for (int base = t0 + warp * (U * TPW); base < t1; base += NW * U * TPW) {
     uint2 ku[U], vu[U];
     bool ok[U];
+    float ksu[U], vsu[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int t = base + u * TPW + grp;
       ok[u] = false;
       ku[u] = make_uint2(0, 0);
       vu[u] = ku[u];
+      ksu[u] = vsu[u] = 1.f;
       if (t >= lo && t < t1) {
         const int64_t blk = trow[t >> bshift];
         if (blk >= 0 && blk < a.num_blocks) {
           const int64_t off = ((blk * Hkv + kvh) * B + (t & (B - 1))) * D + sub * 8;
           ku[u] = __ldg(reinterpret_cast<const uint2*>(kb + off));
           vu[u] = __ldg(reinterpret_cast<const uint2*>(vb + off));
+          if (SCALED) {
+            ksu[u] = __ldg(a.k_scales + blk * Hkv + kvh);
+            vsu[u] = __ldg(a.v_scales + blk * Hkv + kvh);
+          }
           ok[u] = true;
         } else if (sub == 0) {
           latch(a.err, PA_ERR_OUT_OF_RANGE);
@@ -228,7 +335,7 @@ decode_fp8_kernel(const DecodeArgs a, float k_scale, float v_scale) {
         for (int i = 0; i < 8; ++i) d = fmaf(qf[g][i], kf[i], d);
 #pragma unroll
         for (int o = TPT / 2; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-        x[u][g] = ok[u] ? d : kNegInf8;
+        x[u][g] = ok[u] ? (SCALED ? d * ksu[u] : d) : kNegInf8;
       }
     }
 #pragma unroll
@@ -244,11 +351,12 @@ decode_fp8_kernel(const DecodeArgs a, float k_scale, float v_scale) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const float p = exp2f(x[u][g] - mx);
+        const float pv = SCALED ? p * vsu[u] : p;
         float vf[8];
         e4m3x8_to_f32(vu[u], vf);
         l[g] += p;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(p, vf[i], acc[g][i]);
+        for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pv, vf[i], acc[g][i]);
       }
       m[g] = mx;
     }
@@ -311,7 +419,10 @@ template <typename T, int D, int G>
 cudaError_t launch_fp8_tdg(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
   constexpr int U = (G <= 2) ? 4 : (G == 4 ? 2 : 1);
   dim3 grid(a.num_splits, a.num_kv_heads, a.num_seqs);
-  decode_fp8_kernel<T, D, G, U><<<grid, kFp8Warps * 32, 0, st>>>(a, ks, vs);
+  if (a.k_scales != nullptr)
+    decode_fp8_kernel<T, D, G, U, true><<<grid, kFp8Warps * 32, 0, st>>>(a, 1.f, 1.f);
+  else
+    decode_fp8_kernel<T, D, G, U, false><<<grid, kFp8Warps * 32, 0, st>>>(a, ks, vs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_combine(a, st);

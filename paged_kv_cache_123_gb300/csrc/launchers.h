@@ -50,6 +50,10 @@ struct DecodeArgs {
   int partition;     // tokens per split (multiple of max(64, block_size))
   int num_splits;    // ceil(max_seq_len / partition), >= 1
   int items_per_cta; // tensor-core decode: work items per CTA (<= 1: one each)
+  // fp8 pools whose blocks carry their own scales: [num_blocks][num_kv_heads]
+  // fp32 each (nullptr: one scale per pool)
+  const float* k_scales;
+  const float* v_scales;
   void* out;
   float* ws_acc;     // [S][Hq][num_splits][D]   (num_splits > 1)
   float* ws_ml;      // [S][Hq][num_splits][2]   (num_splits > 1)
@@ -69,7 +73,8 @@ cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, int64_t n
                                          int num_kv_heads, int head_size, int dtype,
                                          const int64_t* slots, void* kc, void* vc,
                                          int64_t num_blocks, int block_size, float k_scale,
-                                         float v_scale, int sm_count, cudaStream_t st, int* err);
+                                         float v_scale, float* k_scales, float* v_scales,
+                                         int sm_count, cudaStream_t st, int* err);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, float k_scale, float v_scale,
                               cudaStream_t st);
 cudaError_t launch_decode_mma_fp8(const DecodeArgs& a, float k_scale, float v_scale,

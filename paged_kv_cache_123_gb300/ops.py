@@ -288,6 +288,67 @@ def pa_decode_attention_fp8(q: torch.Tensor, key_cache: torch.Tensor, value_cach
     return out
 
 
+def pa_reshape_and_cache_fp8_scaled(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                                    key_cache: torch.Tensor, value_cache: torch.Tensor,
+                                    k_scales: torch.Tensor, v_scales: torch.Tensor,
+                                    stream=None) -> None:
+    """KV write into E4M3 pools whose blocks carry their own scales
+    (k_scales / v_scales: float32 [NB, Hkv], updated where this write stores
+    a block's first row)."""
+    for n, t in (("k", k), ("v", v), ("key_cache", key_cache), ("value_cache", value_cache)):
+        _dev(t, n)
+    _dev(slot_mapping, "slot_mapping", torch.int64)
+    _dev(k_scales, "k_scales", torch.float32)
+    _dev(v_scales, "v_scales", torch.float32)
+    if key_cache.dtype != torch.uint8 or value_cache.dtype != torch.uint8:
+        raise ValueError("fp8 pools are uint8 tensors of E4M3 codes")
+    NB, Hkv, B, D = key_cache.shape
+    if tuple(k_scales.shape) != (NB, Hkv) or tuple(v_scales.shape) != (NB, Hkv):
+        raise ValueError("scales must be float32 [num_blocks, num_kv_heads]")
+    check("pa_reshape_and_cache_fp8_scaled", lib().pa_reshape_and_cache_fp8_scaled(
+        ptr(k), ptr(v), k.shape[0], Hkv, D, DTYPE_CODE[k.dtype], ptr(slot_mapping),
+        ptr(key_cache), ptr(value_cache), ptr(k_scales), ptr(v_scales), NB, B,
+        stream_handle(stream)))
+
+
+def pa_decode_attention_fp8_scaled(q: torch.Tensor, key_cache: torch.Tensor,
+                                   value_cache: torch.Tensor, k_scales: torch.Tensor,
+                                   v_scales: torch.Tensor, block_tables: torch.Tensor,
+                                   seq_lens: torch.Tensor, scale: float, num_kv_heads: int,
+                                   out: Optional[torch.Tensor] = None, *, max_seq_len: int,
+                                   window: int = 0, partition_size: int = 0,
+                                   workspace: Optional[torch.Tensor] = None,
+                                   stream=None) -> torch.Tensor:
+    """Decode attention over E4M3 pools with per-(block, KV head) scales;
+    window 0 attends the whole sequence."""
+    for n, t in (("q", q), ("key_cache", key_cache), ("value_cache", value_cache)):
+        _dev(t, n)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(k_scales, "k_scales", torch.float32)
+    _dev(v_scales, "v_scales", torch.float32)
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = key_cache.shape
+    if Hkv != num_kv_heads or Dk != D or key_cache.dtype != torch.uint8:
+        raise ValueError("pools must be uint8 [NB, Hkv, B, D] matching q")
+    if tuple(k_scales.shape) != (NB, Hkv) or tuple(v_scales.shape) != (NB, Hkv):
+        raise ValueError("scales must be float32 [num_blocks, num_kv_heads]")
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out")
+    need = pa_decode_window_workspace_bytes(S, Hq, Hkv, D, B, max_seq_len, window,
+                                            partition_size)
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check("pa_decode_attention_fp8_scaled", lib().pa_decode_attention_fp8_scaled(
+        ptr(q), ptr(key_cache), ptr(value_cache), ptr(k_scales), ptr(v_scales),
+        ptr(block_tables), block_tables.shape[1], ptr(seq_lens), S, Hq, Hkv, D, B, NB,
+        DTYPE_CODE[q.dtype], float(scale), int(window), int(max_seq_len), int(partition_size),
+        ptr(out), ptr(workspace), ws_bytes, stream_handle(stream)))
+    return out
+
+
 def pa_decode_window_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int,
                                      head_size: int, block_size: int, max_seq_len: int,
                                      window: int, partition_size: int = 0) -> int:

@@ -91,7 +91,7 @@ def test_copy_blocks_host_alias_and_range_checks(lib):
     assert run([(0, 1), (2, 1)]) == -7          # repeated destination
     assert run([(0, 1), (1, 2)]) == -7          # destination is also a source
     assert run([(0, 9)]) == -5                  # outside the pool
-    assert run([(0, 1)], block_bytes=24) == -2  # not a multiple of 16
+    assert run([(0, 1)], block_bytes=26) == -2  # not a multiple of 4
     assert lib.pa_copy_blocks(arr, arr, 1, p, None, 0, 8, 256, None) == 0  # no pairs
 
 
