@@ -294,13 +294,23 @@ PA_API int pa_reshape_and_cache_fp8(const void* k, const void* v, int64_t num_to
 /*
  * pa_decode_attention_fp8 — pa_decode_attention over fp8 pools: q and out of
  * `dtype`, K = code * k_scale, V = code * v_scale. The workspace is sized by
- * pa_decode_workspace_bytes with the same arguments. The call may use fewer,
- * longer partitions than pa_decode_attention (16-bit queries, head size 128
- * and blocks of at least 8 tokens run the tensor-core kernel, which takes
- * the tensor-core partition sizes for every group size); never more, so
- * that workspace suffices. pa_decode_fp8_partitioning reports the choice.
- * k_scale and v_scale must be positive (else PA_ERR_SHAPE).
+ * pa_decode_fp8_workspace_bytes with the same arguments (window 0). The
+ * partitioning differs from pa_decode_attention's: 16-bit queries, head size
+ * 128 and blocks of at least 8 tokens run the tensor-core kernel, which
+ * takes the tensor-core partition sizes for every group size and, for a
+ * window that cuts the longest sequence, as many splits as keep its three
+ * CTAs per SM busy. pa_decode_fp8_partitioning reports the choice. k_scale
+ * and v_scale must be positive (else PA_ERR_SHAPE).
  */
+/*
+ * pa_decode_fp8_workspace_bytes — scratch for the fp8-pool decode calls
+ * (pa_decode_attention_fp8 with window 0, pa_decode_attention_fp8_window,
+ * pa_decode_attention_fp8_scaled) with the same arguments; dtype is the
+ * query type. Negative status on invalid sizes.
+ */
+PA_API int64_t pa_decode_fp8_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                             int head_size, int block_size, int dtype,
+                                             int max_seq_len, int window, int partition_size);
 PA_API int pa_decode_attention_fp8(const void* q, const void* key_cache,
                                    const void* value_cache, const int32_t* block_tables,
                                    int64_t block_tables_stride, const int32_t* seq_lens,
@@ -344,7 +354,7 @@ PA_API int pa_decode_attention_fp8(const void* q, const void* key_cache,
  * K_s[j] = code * k_scales[b][h], V_s[j] = code * v_scales[b][h] for the
  * block b holding token j. `window` as in pa_decode_attention_fp8_window
  * (0 = the whole sequence); workspace sized by
- * pa_decode_window_workspace_bytes with the same arguments; partitioning as
+ * pa_decode_fp8_workspace_bytes with the same arguments; partitioning as
  * pa_decode_fp8_partitioning reports. The tensor-core kernel multiplies each
  * token's softmax weight by its block's V scale relative to the first
  * attended block's before rounding it to fp16, so V scales within one
@@ -380,10 +390,12 @@ PA_API int pa_decode_attention_fp8_scaled(const void* q, const void* key_cache,
  * lo / block_size blocks are never read: the caller may have released those
  * blocks and left any value there (e.g. -1).
  *
- * pa_decode_window_workspace_bytes — scratch for the windowed calls with the
- * same arguments (window >= 0; returns a negative status on invalid sizes).
+ * pa_decode_window_workspace_bytes — scratch for pa_decode_attention_window
+ * with the same arguments (window >= 0; returns a negative status on
+ * invalid sizes).
  * pa_decode_attention_window — pa_decode_attention with a window.
- * pa_decode_attention_fp8_window — pa_decode_attention_fp8 with a window.
+ * pa_decode_attention_fp8_window — pa_decode_attention_fp8 with a window;
+ * its scratch comes from pa_decode_fp8_workspace_bytes.
  * Other arguments, layouts and errors as in the unwindowed calls; window < 0
  * is PA_ERR_SHAPE.
  */

@@ -50,6 +50,7 @@ SIGNATURES = {
                                  _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_f, _c_f, _c_i32,
                                  _c_i32, _c_p, _c_p, _c_i64, _c_p], _c_i32),
     "pa_decode_window_workspace_bytes": ([_c_i32] * 8, _c_i64),
+    "pa_decode_fp8_workspace_bytes": ([_c_i32] * 9, _c_i64),
     "pa_decode_attention_window": ([_c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32,
                                     _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32,
                                     _c_i32, _c_i32, _c_p, _c_p, _c_i64, _c_p], _c_i32),

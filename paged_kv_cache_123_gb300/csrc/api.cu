@@ -84,9 +84,12 @@ int check_launch(cudaError_t e) {
 // mma_fp8 = the call runs the tensor-core kernel over fp8 pools, which takes
 // the tensor-core class for every group size (group 1 included: one
 // 2,048-token partition per Llama-7B sequence ran at 0.81 of the copy
-// bandwidth, 512-token ones at 0.69). Its partitions are never shorter than
-// those of the 16-bit call with the same sizes, so the 16-bit workspace
-// query sizes its scratch too.
+// bandwidth, 512-token ones at 0.69). That kernel runs three CTAs per SM, so
+// a windowed (uniform) call sizes its one wave for three CTAs per SM; more,
+// shorter partitions were slower (each item pays its start and its merge:
+// a 4096-token window over the long-context batch ran at 0.53 of the copy
+// bandwidth with 3 splits, 0.49 with 2 and 0.50 with 7; a 1000-token window
+// over the GQA batch at 0.56 unsplit, 0.46 with 2).
 void partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
                   int max_seq_len, int partition_size, int sm_count, bool uniform,
                   bool mma_fp8, int* splits, int* tokens) {
@@ -104,7 +107,8 @@ void partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_siz
     const int64_t pairs = num_seqs > 0 ? (int64_t)num_seqs * num_kv_heads : 1;
     const int64_t floor_p = round_up(256);
     if (uniform) {
-      int64_t k = (int64_t)sm_count * per_sm / pairs;   // splits per pair in one wave
+      // splits per pair in one wave (the fp8 kernel runs three CTAs per SM)
+      int64_t k = (int64_t)sm_count * (mma_fp8 ? 3 : per_sm) / pairs;
       if (k < 1) k = 1;
       P = round_up((len + k - 1) / k);
       if (P < floor_p) P = floor_p;
@@ -282,6 +286,24 @@ int pa_decode_fp8_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, 
   return decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len,
                              window, partition_size, pa::mma_fp8_path_applies(a),
                              num_splits_out, partition_tokens_out);
+}
+
+int64_t pa_decode_fp8_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                      int head_size, int block_size, int dtype,
+                                      int max_seq_len, int window, int partition_size) {
+  if (elt_bytes(dtype) == 0) return PA_ERR_DTYPE;
+  if (window < 0 || partition_size < 0) return PA_ERR_SHAPE;
+  int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size,
+                              block_size, max_seq_len);
+  if (st != PA_OK) return st;
+  pa::DecodeArgs a{};
+  a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size; a.block_size = block_size; a.dtype = dtype;
+  int splits, tokens;
+  st = decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, window,
+                           partition_size, pa::mma_fp8_path_applies(a), &splits, &tokens);
+  if (st != PA_OK) return st;
+  return workspace_for(num_seqs, num_q_heads, head_size, splits);
 }
 
 int64_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
@@ -648,13 +670,14 @@ int run_decode(const void* q, const void* key_cache, const void* value_cache,
   // more work items than resident tensor-core CTAs, each CTA walks several
   // (its producer runs ahead into the next), so all of them run in one wave
   // instead of leaving a last, partial wave of CTAs running alone (GQA-72B
-  // batch, window 1000: 0.78 -> 0.83 of the copy bandwidth). 16-bit pools
-  // only: the fp8 kernel is bound by its widening work per CTA and needs
-  // all three CTAs per SM busy (0.59 -> 0.56 with one wave of fewer CTAs).
+  // batch, window 1000: 0.78 -> 0.83 of the copy bandwidth). fp8 pools do
+  // the same with the fp8 kernel's three CTAs per SM.
   a.items_per_cta = 1;
-  if (!fp8 && windowed(max_seq_len, window) && head_size == 128 && pa::mma_path_applies(a)) {
+  const bool multi16 = !fp8 && head_size == 128 && pa::mma_path_applies(a);
+  const bool multi8 = fp8 && pa::mma_fp8_path_applies(a);
+  if (windowed(max_seq_len, window) && (multi16 || multi8)) {
     const int64_t items = (int64_t)a.num_splits * num_kv_heads * num_seqs;
-    const int64_t slots = (int64_t)g_sm_count[dev] * 2;
+    const int64_t slots = (int64_t)g_sm_count[dev] * (multi8 ? 3 : 2);
     a.items_per_cta = (int)std::min<int64_t>(1 << 20, (items + slots - 1) / slots);
   }
   const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);

@@ -109,7 +109,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   constexpr bool kQRescale = KV8 && std::is_same<T, __nv_bfloat16>::value;
   constexpr int KSTEPS = D / 16;
   static_assert(G == 2 || G == 4 || G == 8 || (KV8 && G == 1), "group");
-  static_assert(!SCALED || (KV8 && !MULTI), "per-block scales: fp8 pools, one item per CTA");
+  static_assert(!SCALED || KV8, "per-block scales: fp8 pools");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -138,9 +138,11 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   // per-warp row maxima and sums for the merge of an item ([4][8] each)
   float* sm_m = reinterpret_cast<float*>(tile_mask + kSt);
   float* sm_l = sm_m + kMmaConsumers * 8;
-  // SCALED: K and V scale of each piece of each stage ([kSt][8] each)
+  // SCALED: per stage, each piece's K and V scale ([kSt][8] each), and the
+  // item's largest V scale up to that tile ([kSt])
   float* st_ks = sm_l + kMmaConsumers * 8;
   float* st_vs = st_ks + kSt * 8;
+  float* st_vref = st_vs + kSt * 8;
   struct Item {
     int s, kvh, split, L, lo, t0, t1, nsplit, ntiles;
     bool bad, zero_out;
@@ -189,49 +191,33 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     const int npieces = kTile / R;             // <= 8 (R >= 8)
     int it = 0;                                // tiles issued so far: the ring position
     bool run = true;
-    for (int idx = blockIdx.x; run && idx < n_items;
-         idx = MULTI ? idx + (int)gridDim.x : n_items) {
-    const Item im = item_at(idx);
-    const int kvh = im.kvh, lo = im.lo, t0 = im.t0, t1 = im.t1;
-    const int32_t* trow = a.tables + (int64_t)im.s * a.table_stride;
-    for (int i = 0; i < im.ntiles; ++i) {
+    auto in_pool = [&](int64_t b) { return b >= 0 && b < a.num_blocks; };
+    // Issue tile i of item im into the next stage: lane p loads piece p (R
+    // rows of block blk) when `need`. SCALED: ksv and rsv are the piece's K
+    // and V scales, vrt the largest V scale of the item so far (the
+    // reference the consumers' output is kept in).
+    auto issue_tile = [&](const Item& im, int i, int64_t blk, bool need, float ksv, float rsv,
+                          float vrt) -> bool {
       const int st = it % kSt;
-      const int ts = t0 + i * kTile;
-      const int te = min(t1, ts + kTile);
-      const int tok = ts + lane * R;
-      int64_t blk = -1;
-      bool mine = false;
-      if (lane < npieces && tok < te && tok + R > lo) {
-        blk = trow[tok >> bshift];
-        mine = blk >= 0 && blk < a.num_blocks;
-        if (!mine) latch(a.err, PA_ERR_OUT_OF_RANGE);
-      }
+      const int tok = im.t0 + i * kTile + lane * R;
+      const bool mine = need && in_pool(blk);
+      if (need && !mine) latch(a.err, PA_ERR_OUT_OF_RANGE);
       const unsigned pm = __ballot_sync(0xffffffffu, mine);
       int ok = 1;
       if constexpr (SCALED) {
-        // the scale loads are in flight while lane 0 waits for the stage;
-        // pieces that are not loaded get 0 (their rows are masked and take
-        // no part in the reference)
-        float ksv = 0.f, vsv = 0.f;
-        if (mine) {
-          ksv = a.k_scales[blk * Hkv + kvh];
-          vsv = a.v_scales[blk * Hkv + kvh];
-        }
         if (lane == 0 && it >= kSt)
           ok = mbar_wait_bounded(empty_bar(st), ((it / kSt) - 1) & 1, abort_flag, kWaitCycles);
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          run = false;
-          break;
-        }
+        if (!ok) return false;
         if (lane < npieces) {
           st_ks[st * 8 + lane] = ksv;
-          st_vs[st * 8 + lane] = vsv;
+          st_vs[st * 8 + lane] = rsv;
         }
         // the warp's scale stores come before lane 0's arrive (release), and
         // the arrive before any lane's copy
         __syncwarp();
         if (lane == 0) {
+          st_vref[st] = vrt;
           tile_mask[st] = pm;
           mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * IN_ROW);
         }
@@ -246,15 +232,12 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          run = false;
-          break;
-        }
+        if (!ok) return false;
       }
       if (mine) {
         const uint32_t kdst = smem0 + st * STAGE_BYTES + lane * R * IN_ROW;
         const uint32_t vdst = kdst + KV_BYTES;
-        const int z = (int)(blk * Hkv + kvh);
+        const int z = (int)(blk * Hkv + im.kvh);
         const int y = tok & (B - 1);
         if (KV8) {
           tma_load_3d(kdst, &tmK, 0, y, z, full_bar(st));
@@ -265,7 +248,95 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         }
       }
       ++it;
-    }
+      return true;
+    };
+    if constexpr (!SCALED) {
+      // the table entries of a tile are read in parallel (one lane per
+      // piece) right before its stage is awaited
+      for (int idx = blockIdx.x; run && idx < n_items;
+           idx = MULTI ? idx + (int)gridDim.x : n_items) {
+        const Item im = item_at(idx);
+        const int32_t* trow = a.tables + (int64_t)im.s * a.table_stride;
+        for (int i = 0; i < im.ntiles; ++i) {
+          const int ts = im.t0 + i * kTile;
+          const int tok = ts + lane * R;
+          const bool need = lane < npieces && tok < min(im.t1, ts + kTile) && tok + R > im.lo;
+          const int64_t blk = need ? (int64_t)trow[tok >> bshift] : -1;
+          if (!issue_tile(im, i, blk, need, 0.f, 0.f, 0.f)) {
+            run = false;
+            break;
+          }
+        }
+      }
+    } else {
+      // per-block scales: each piece's scales are read through its table
+      // entry, two dependent loads. They run ahead of the copies in a
+      // software pipeline over the CTA's tiles (cursor: item idx, tile i):
+      // while tile k is issued, the table entries of tile k+2 and the scales
+      // of tile k+1 are in flight.
+      struct Cur {
+        int idx, i;
+        Item im;
+      };
+      auto settle = [&](Cur& c) {              // skip items without tiles
+        while (c.idx < n_items && c.i >= c.im.ntiles) {
+          c.idx = MULTI ? c.idx + (int)gridDim.x : n_items;
+          c.i = 0;
+          if (c.idx < n_items) c.im = item_at(c.idx);
+        }
+      };
+      auto next = [&](Cur c) {
+        ++c.i;
+        settle(c);
+        return c;
+      };
+      auto needs = [&](const Cur& c) {
+        if (c.idx >= n_items || lane >= npieces) return false;
+        const int ts = c.im.t0 + c.i * kTile;
+        const int tok = ts + lane * R;
+        return tok < min(c.im.t1, ts + kTile) && tok + R > c.im.lo;
+      };
+      auto table_of = [&](const Cur& c) -> int64_t {
+        if (!needs(c)) return -1;
+        const int tok = c.im.t0 + c.i * kTile + lane * R;
+        return a.tables[(int64_t)c.im.s * a.table_stride + (tok >> bshift)];
+      };
+      Cur c0;
+      c0.idx = blockIdx.x;
+      c0.i = 0;
+      if (c0.idx < n_items) c0.im = item_at(c0.idx);
+      settle(c0);
+      Cur c1 = next(c0);
+      int64_t b0 = table_of(c0), b1 = table_of(c1);
+      // pieces that are not loaded get scales 0 (their rows are masked)
+      float ks0 = 0.f, vs0 = 0.f, vrun = 0.f;
+      if (in_pool(b0)) {
+        ks0 = a.k_scales[b0 * Hkv + c0.im.kvh];
+        vs0 = a.v_scales[b0 * Hkv + c0.im.kvh];
+      }
+      while (run && c0.idx < n_items) {
+        const Cur c2 = next(c1);
+        const int64_t b2 = table_of(c2);       // two tiles ahead
+        float ks1 = 0.f, vs1 = 0.f;
+        if (in_pool(b1)) {                     // one tile ahead
+          ks1 = a.k_scales[b1 * Hkv + c1.im.kvh];
+          vs1 = a.v_scales[b1 * Hkv + c1.im.kvh];
+        }
+        // the item's running maximum V scale (scales are >= 0, so their
+        // bit patterns order like the values)
+        if (c0.i == 0) vrun = 0.f;
+        vrun = fmaxf(vrun, __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(vs0))));
+        if (!issue_tile(c0.im, c0.i, b0, needs(c0), ks0, vs0, vrun)) {
+          run = false;
+          break;
+        }
+        c0 = c1;
+        c1 = c2;
+        b0 = b1;
+        b1 = b2;
+        ks0 = ks1;
+        vs0 = vs1;
+      }
     }
     // let the loads this CTA issued land before it can leave (also after a
     // timeout: this wait has its own limit and ignores the abort flag)
@@ -275,6 +346,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   } else {
     // ---------------- consumers
     const int n = lane >> 2, c = lane & 3;
+    // pieces (R rows of one block) of this lane's rows n and n+8 of the
+    // warp's 16 in every tile (R is a power of two)
+    const int rshift = __ffs(R) - 1;
+    const int pA = (warp * 16 + n) >> rshift, pB = (warp * 16 + n + 8) >> rshift;
     const float sl2 = a.scale * kLog2e * k_scale;
     T* out = reinterpret_cast<T*>(a.out);
     int it = 0;                                // tiles consumed so far: the ring position
@@ -366,8 +441,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     for (int i = 0; i < KSTEPS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     if (!MULTI) q_frags(idx, qf, qmul);
     const float sl2q = sl2 * qmul;
-    // SCALED: the warp's reference V scale (0 until it meets a row) and its
-    // reciprocal
+    // SCALED: the reference V scale the warp's output is kept in (0 until
+    // the first tile) and its reciprocal
     float vref = 0.f, inv_vref = 0.f;
     bool ok = true;
     for (int i = 0; i < ntiles; ++i, ++it) {
@@ -437,24 +512,21 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           }
         }
         const bool okA = (okm >> n) & 1u, okB = (okm >> (n + 8)) & 1u;
-        // SCALED: rows n and n+8 take the scales of their pieces, and the
-        // warp's reference grows to the largest V scale of its valid rows
-        float slA = sl2q, slB = sl2q, vA = 0.f, vB = 0.f, cv = 1.f;
+        // SCALED: rows n and n+8 take the K scales of their pieces and
+        // their V scales relative to the reference; when the reference grew,
+        // the output so far is rescaled to it
+        float slA = sl2q, slB = sl2q, rA = 0.f, rB = 0.f, cv = 1.f;
         if constexpr (SCALED) {
-          const int pA = (warp * 16 + n) / R, pB = (warp * 16 + n + 8) / R;
+          const float vr = st_vref[st];
+          if (vr != vref) {              // warp-uniform; vr > vref here
+            cv = vref / vr;              // 0 the first time: nothing to rescale
+            vref = vr;
+            inv_vref = 1.f / vr;
+          }
           slA *= st_ks[st * 8 + pA];
           slB *= st_ks[st * 8 + pB];
-          vA = okA ? st_vs[st * 8 + pA] : 0.f;
-          vB = okB ? st_vs[st * 8 + pB] : 0.f;
-          float vm = fmaxf(vA, vB);
-#pragma unroll
-          for (int off = 4; off < 32; off <<= 1)
-            vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
-          if (vm > vref) {               // warp-uniform
-            cv = vref / vm;              // 0 the first time: nothing to rescale
-            vref = vm;
-            inv_vref = 1.f / vm;
-          }
+          rA = st_vs[st * 8 + pA] * inv_vref;
+          rB = st_vs[st * 8 + pB] * inv_vref;
         }
         const float x0 = okA ? sacc[0] * slA : kNegInfM;   // row n,   head 2c
         const float x1 = okA ? sacc[1] * slA : kNegInfM;   // row n,   head 2c+1
@@ -477,8 +549,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         uint32_t cA, cB;
         float aO0 = al0, aO1 = al1;      // rescale of the output
         if constexpr (SCALED) {
-          const float rA = vA * inv_vref, rB = vB * inv_vref;   // <= 1
-          cA = MmaOps<MT>::pack(p0 * rA, p1 * rA);
+          cA = MmaOps<MT>::pack(p0 * rA, p1 * rA);     // rA, rB <= 1
           cB = MmaOps<MT>::pack(p2 * rB, p3 * rB);
           l0 = l0 * al0 + p0 + p2;
           l1 = l1 * al1 + p1 + p3;
@@ -686,7 +757,7 @@ template <int D, bool KV8, bool SCALED>
 constexpr int mma_smem_bytes() {
   constexpr int kSt = ring_stages<KV8>();
   return 1024 + kSt * 2 * kTile * (KV8 ? D : 2 * D) + 2 * kSt * 8 + 4 + 4 * kSt +
-         2 * kMmaConsumers * 8 * 4 + (SCALED ? 2 * kSt * 8 * 4 : 0) +
+         2 * kMmaConsumers * 8 * 4 + (SCALED ? 2 * kSt * 8 * 4 + kSt * 4 : 0) +
          16;
 }
 
@@ -723,8 +794,14 @@ cudaError_t launch_mma_tdgm(const DecodeArgs& a, float ks, float vs, cudaStream_
 
 template <typename T, int D, int G, bool KV8>
 cudaError_t launch_mma_tdg(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
-  if constexpr (D == 128 && !KV8) {
-    if (a.items_per_cta > 1) return launch_mma_tdgm<T, D, G, KV8, true, false>(a, ks, vs, st);
+  if constexpr (D == 128) {
+    if (a.items_per_cta > 1) {
+      if constexpr (KV8) {
+        if (a.k_scales != nullptr)
+          return launch_mma_tdgm<T, D, G, KV8, true, true>(a, 1.f, 1.f, st);
+      }
+      return launch_mma_tdgm<T, D, G, KV8, true, false>(a, ks, vs, st);
+    }
   }
   if constexpr (KV8) {
     if (a.k_scales != nullptr) return launch_mma_tdgm<T, D, G, KV8, false, true>(a, 1.f, 1.f, st);

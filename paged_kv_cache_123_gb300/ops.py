@@ -104,6 +104,19 @@ def pa_decode_fp8_partitioning(num_seqs: int, num_q_heads: int, num_kv_heads: in
     return s.value, p.value
 
 
+def pa_decode_fp8_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                  head_size: int, block_size: int, dtype: torch.dtype,
+                                  max_seq_len: int, window: int = 0,
+                                  partition_size: int = 0) -> int:
+    """Scratch bytes of the fp8-pool decode calls; dtype is the query type."""
+    n = lib().pa_decode_fp8_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                            block_size, DTYPE_CODE[dtype], max_seq_len, window,
+                                            partition_size)
+    if n < 0:
+        check("pa_decode_fp8_workspace_bytes", int(n))
+    return int(n)
+
+
 def pa_decode_attention(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
                         block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
                         num_kv_heads: int, out: Optional[torch.Tensor] = None, *,
@@ -276,7 +289,8 @@ def pa_decode_attention_fp8(q: torch.Tensor, key_cache: torch.Tensor, value_cach
     if out is None:
         out = torch.empty_like(q)
     _dev(out, "out")
-    need = pa_decode_workspace_bytes(S, Hq, Hkv, D, B, max_seq_len, partition_size)
+    need = pa_decode_fp8_workspace_bytes(S, Hq, Hkv, D, B, q.dtype, max_seq_len, 0,
+                                         partition_size)
     if need > 0 and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -336,8 +350,8 @@ def pa_decode_attention_fp8_scaled(q: torch.Tensor, key_cache: torch.Tensor,
     if out is None:
         out = torch.empty_like(q)
     _dev(out, "out")
-    need = pa_decode_window_workspace_bytes(S, Hq, Hkv, D, B, max_seq_len, window,
-                                            partition_size)
+    need = pa_decode_fp8_workspace_bytes(S, Hq, Hkv, D, B, q.dtype, max_seq_len, window,
+                                         partition_size)
     if need > 0 and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -375,8 +389,12 @@ def _window_call(name, q, key_cache, value_cache, block_tables, seq_lens, scale,
     if out is None:
         out = torch.empty_like(q)
     _dev(out, "out")
-    need = pa_decode_window_workspace_bytes(S, Hq, Hkv, D, B, max_seq_len, window,
-                                            partition_size)
+    if scales:       # fp8 pools: their own partitioning and scratch
+        need = pa_decode_fp8_workspace_bytes(S, Hq, Hkv, D, B, q.dtype, max_seq_len, window,
+                                             partition_size)
+    else:
+        need = pa_decode_window_workspace_bytes(S, Hq, Hkv, D, B, max_seq_len, window,
+                                                partition_size)
     if need > 0 and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -102,20 +102,30 @@ def test_fp8_full_step_against_oracle():
 
 def test_fp8_partitioning_query():
     """Tensor-core fp8 calls take the tensor-core partition sizes for every
-    group size (group 1 included); never more partitions than the 16-bit
-    call, whose workspace query therefore sizes the fp8 scratch too."""
+    group size (group 1 included), and windowed ones as many splits as keep
+    three CTAs per SM busy; pa_decode_fp8_workspace_bytes sizes the scratch
+    for exactly the partitioning pa_decode_fp8_partitioning reports."""
     bf = torch.bfloat16
     # Llama-7B shape over fp8 pools: one partition per sequence
     assert pa.pa_decode_fp8_partitioning(64, 32, 32, 128, 16, bf, 2000) == (1, 2048)
     assert pa.pa_decode_partitioning(64, 32, 32, 16, 2000)[0] > 1
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     for args in [(64, 32, 32, 128, 16), (128, 64, 8, 128, 16), (16, 32, 8, 128, 64),
                  (8, 8, 8, 64, 16), (8, 8, 8, 128, 4)]:
         S, Hq, Hkv, D, B = args
         for dt in (bf, torch.float16, torch.float32):
             for L, W in ((2049, 0), (8193, 0), (32768, 4096), (5000, 333)):
-                f8 = pa.pa_decode_fp8_partitioning(S, Hq, Hkv, D, B, dt, L, W)
-                sixteen = pa.pa_decode_window_partitioning(S, Hq, Hkv, B, L, W)
-                assert f8[0] <= sixteen[0], (args, dt, L, W, f8, sixteen)
+                splits, ptoks = pa.pa_decode_fp8_partitioning(S, Hq, Hkv, D, B, dt, L, W)
+                covered = min(L, W + 63) if 0 < W < L else L
+                assert splits == -(-covered // ptoks) and ptoks % max(64, B) == 0
+                ws = pa.pa_decode_fp8_workspace_bytes(S, Hq, Hkv, D, B, dt, L, W)
+                assert (ws > 0) == (splits > 1)
+                if splits > 1:
+                    assert ws >= S * Hq * splits * (D + 2) * 4
+                if dt != torch.float32 and D == 128 and B >= 8 and 0 < W < L:
+                    # windowed tensor-core fp8: as many splits as fill one
+                    # wave of three CTAs per SM, never more
+                    assert splits == 1 or splits * S * Hkv <= 3 * sms
     # the CUDA-core cases (fp32 queries, head size 64, blocks below 8) keep
     # the 16-bit call's partitioning
     assert pa.pa_decode_fp8_partitioning(64, 32, 32, 128, 16, torch.float32, 2049) == \
