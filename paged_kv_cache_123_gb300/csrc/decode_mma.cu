@@ -112,8 +112,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   static_assert(!SCALED || KV8, "per-block scales: fp8 pools");
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, reached by pointer arithmetic on the shared
+  // array itself so the compiler keeps every access in the shared space
+  // (an integer round trip would make them generic loads)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSt * STAGE_BYTES +
                                                 kMmaConsumers * PRIV_BYTES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kSt);

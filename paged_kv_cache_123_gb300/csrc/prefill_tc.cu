@@ -315,8 +315,10 @@ multi_query_tc_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensorMa
                       const __grid_constant__ CUtensorMap tmV) {
   using Ly = TcLayout<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, reached by pointer arithmetic on the shared
+  // array itself so the compiler keeps every access in the shared space
+  // (an integer round trip would make them generic loads)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t s0 = smem_u32(smem);
   const uint32_t bar = s0 + Ly::BAR_OFF;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
