@@ -81,6 +81,20 @@ def kv_read_bytes(seq_lens, num_kv_heads, head_size, elt):
     return int(sum(int(L) for L in seq_lens)) * 2 * num_kv_heads * head_size * elt
 
 
+def block_scale_bytes(seq_lens, window, block_size, num_kv_heads):
+    """Bytes of per-block fp8 scales one attention launch must read: a K and
+    a V fp32 scale for every (block, KV head) that holds an attended token
+    (tokens L - window .. L - 1 under a window, else all L)."""
+    blocks = 0
+    for L in seq_lens:
+        L = int(L)
+        if L <= 0:
+            continue
+        lo = L - window if 0 < window < L else 0
+        blocks += (L - 1) // block_size - lo // block_size + 1
+    return blocks * num_kv_heads * 2 * 4
+
+
 def kernel_sources_digest():
     """Digest of every source the library is built from (kernels, shared
     device helpers, host dispatch and partitioning) and of the workload
@@ -499,11 +513,7 @@ def ours_arm(args):
         attended = lens.tolist()
     kv_bytes = kv_read_bytes(attended, Hkv, D, elt)
     if bscaled:   # plus the K and V scale of every attended (block, KV head)
-        blocks = 0
-        for L in lens.tolist():
-            lo = (L - W) if 0 < W < L else 0
-            blocks += (L - 1) // B - lo // B + 1 if L > 0 else 0
-        kv_bytes += blocks * Hkv * 2 * 4
+        kv_bytes += block_scale_bytes(lens.tolist(), W, B, Hkv)
     tokens = int(sum(attended))
     max_len = inp.max_seq_len
     P = args.partition

@@ -677,7 +677,8 @@ int run_decode(const void* q, const void* key_cache, const void* value_cache,
   const bool multi8 = fp8 && pa::mma_fp8_path_applies(a);
   if (windowed(max_seq_len, window) && (multi16 || multi8)) {
     const int64_t items = (int64_t)a.num_splits * num_kv_heads * num_seqs;
-    const int64_t slots = (int64_t)g_sm_count[dev] * (multi8 ? 3 : 2);
+    // resident CTAs per SM: 2 (16-bit), 3 (fp8), 4 (fp8, per-block scales)
+    const int64_t slots = (int64_t)g_sm_count[dev] * (multi8 ? (k_scales ? 4 : 3) : 2);
     a.items_per_cta = (int)std::min<int64_t>(1 << 20, (items + slots - 1) / slots);
   }
   const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);

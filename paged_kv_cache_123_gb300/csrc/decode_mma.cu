@@ -41,11 +41,16 @@ namespace pa {
 constexpr int kMmaConsumers = 4;
 constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
 constexpr int kTile = 64;
-// stages of the K/V ring: four for fp8 pools (16 KB stages, three CTAs per
-// SM: 192 KB in flight per SM, as the 16-bit ring's three 32 KB stages at two
-// CTAs per SM), three for 16-bit pools
-template <bool KV8>
-constexpr int ring_stages() { return KV8 ? 4 : 3; }
+// stages of the K/V ring: four for fp8 pools with one scale per pool (16 KB
+// stages, three CTAs per SM: 192 KB in flight per SM, as the 16-bit ring's
+// three 32 KB stages at two CTAs per SM), three for 16-bit pools and for
+// fp8 pools with per-block scales, which run four CTAs per SM (more warps
+// to cover their dependent scale lookups: 0.67 -> 0.71 of the copy
+// bandwidth on the GQA batch; one-scale pools measured no better with four)
+template <bool KV8, bool SCALED>
+constexpr int ring_stages() { return (KV8 && !SCALED) ? 4 : 3; }
+template <bool KV8, bool SCALED>
+constexpr int ctas_per_sm() { return KV8 ? (SCALED ? 4 : 3) : 2; }
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 #define kNegInfM (-__int_as_float(0x7f800000))
 
@@ -72,7 +77,8 @@ __device__ __forceinline__ bool consumers_bar_and(bool ok) {
 // in fp16 without a widened copy in shared memory. k_scale / v_scale are
 // the pools' scales (1 for 16-bit pools).
 // fp8 pools: half the shared memory per stage and a register budget for
-// three CTAs per SM, so more warps hide the conversion latency.
+// three CTAs per SM (four with per-block scales), so more warps hide the
+// conversion latency.
 // MULTI: each CTA walks several work items (items_per_cta > 1); the one-item
 // instantiation compiles to a single pass.
 // SCALED (fp8 pools only): the blocks carry their own scales (a.k_scales /
@@ -88,7 +94,7 @@ __device__ __forceinline__ bool consumers_bar_and(bool ok) {
 // output is multiplied by its reference when the warps merge; the
 // denominator sums the unscaled weights.
 template <typename T, int D, int G, bool KV8, bool MULTI, bool SCALED>
-__global__ void __launch_bounds__(kMmaThreads, KV8 ? 3 : 2)
+__global__ void __launch_bounds__(kMmaThreads, ctas_per_sm<KV8, SCALED>())
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, float k_scale, float v_scale) {
   constexpr int HALVES = D / 64;                 // 128-byte lines per 16-bit token row
@@ -97,7 +103,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   constexpr int KV_BYTES = kTile * IN_ROW;       // K (or V) part of a stage
   constexpr int STAGE_BYTES = 2 * KV_BYTES;
   constexpr int PRIV_BYTES = 0;
-  constexpr int kSt = ring_stages<KV8>();
+  constexpr int kSt = ring_stages<KV8, SCALED>();
   static_assert(!KV8 || D == 128, "fp8 pools: head size 128 (one 128-byte line per row)");
   // fp8 pools run the products in fp16 whatever the query type: codes widen
   // to fp16 in one conversion. A bf16 query group is first multiplied by the
@@ -593,22 +599,29 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                 w[r][0] = w[r][1] = w[r][2] = w[r][3] = 0u;
             }
           }
-          uint32_t p01[16], p23[16];      // (token pair, head dim j) as f16x2
+          // (token pair, head dim j) as f16x2, widened half the words at a
+          // time next to the four products that use them (m-tiles 4h..4h+3
+          // take code words h and h+2), so fewer widened values are live
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const uint32_t lo01 = __byte_perm(w[0][q4], w[1][q4], 0x5140);
-            const uint32_t hi01 = __byte_perm(w[0][q4], w[1][q4], 0x7362);
-            const uint32_t lo23 = __byte_perm(w[2][q4], w[3][q4], 0x5140);
-            const uint32_t hi23 = __byte_perm(w[2][q4], w[3][q4], 0x7362);
-            e4m3x4_to_f16x2x2(lo01, p01[4 * q4 + 0], p01[4 * q4 + 1]);
-            e4m3x4_to_f16x2x2(hi01, p01[4 * q4 + 2], p01[4 * q4 + 3]);
-            e4m3x4_to_f16x2x2(lo23, p23[4 * q4 + 0], p23[4 * q4 + 1]);
-            e4m3x4_to_f16x2x2(hi23, p23[4 * q4 + 2], p23[4 * q4 + 3]);
-          }
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t p01[2][4], p23[2][4];
 #pragma unroll
-          for (int mt = 0; mt < KSTEPS; ++mt) {
-            const uint32_t af[4] = {p01[mt], p01[8 + mt], p23[mt], p23[8 + mt]};
-            MmaOps<MT>::mma(o[mt], af, pb0, pb1);
+            for (int k = 0; k < 2; ++k) {
+              const int q4 = hh + 2 * k;
+              const uint32_t lo01 = __byte_perm(w[0][q4], w[1][q4], 0x5140);
+              const uint32_t hi01 = __byte_perm(w[0][q4], w[1][q4], 0x7362);
+              const uint32_t lo23 = __byte_perm(w[2][q4], w[3][q4], 0x5140);
+              const uint32_t hi23 = __byte_perm(w[2][q4], w[3][q4], 0x7362);
+              e4m3x4_to_f16x2x2(lo01, p01[k][0], p01[k][1]);
+              e4m3x4_to_f16x2x2(hi01, p01[k][2], p01[k][3]);
+              e4m3x4_to_f16x2x2(lo23, p23[k][0], p23[k][1]);
+              e4m3x4_to_f16x2x2(hi23, p23[k][2], p23[k][3]);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t af[4] = {p01[0][j], p01[1][j], p23[0][j], p23[1][j]};
+              MmaOps<MT>::mma(o[4 * hh + j], af, pb0, pb1);
+            }
           }
         } else {
           const int j = lane >> 3;
@@ -757,7 +770,7 @@ bool encode_pool_map_fp8(CUtensorMap* map, const void* base, const DecodeArgs& a
 
 template <int D, bool KV8, bool SCALED>
 constexpr int mma_smem_bytes() {
-  constexpr int kSt = ring_stages<KV8>();
+  constexpr int kSt = ring_stages<KV8, SCALED>();
   return 1024 + kSt * 2 * kTile * (KV8 ? D : 2 * D) + 2 * kSt * 8 + 4 + 4 * kSt +
          2 * kMmaConsumers * 8 * 4 + (SCALED ? 2 * kSt * 8 * 4 + kSt * 4 : 0) +
          16;

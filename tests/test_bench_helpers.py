@@ -66,3 +66,17 @@ def test_oracle_timer_each_kind(kind, window, N):
         assert timer.unit_tok == att
         assert (f"window {window}" in desc) == bool(window)
     assert (kind == "fp8") == ("fp8" in desc)
+
+
+def test_block_scale_bytes_count_every_attended_block():
+    # brute force: the set of blocks that hold an attended token
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        B = int(rng.choice([1, 4, 16, 64]))
+        lens = rng.integers(0, 300, size=5).tolist()
+        W = int(rng.choice([0, 1, 7, 64, 250, 400]))
+        want = 0
+        for L in lens:
+            lo = L - W if 0 < W < L else 0
+            want += len({j // B for j in range(lo, L)})
+        assert bench.block_scale_bytes(lens, W, B, 3) == want * 3 * 2 * 4, (lens, W, B)
