@@ -531,6 +531,7 @@ def ours_arm(args):
                                                      max_len, P)
         splits = 1 if ws_bytes == 0 else 2
         ptoks = None
+        even_ctas = 0
     else:
         if fp8:
             splits, ptoks = pa.pa_decode_fp8_partitioning(S, cfg.num_q_heads, Hkv, D, B,
@@ -538,6 +539,13 @@ def ours_arm(args):
         else:
             splits, ptoks = pa.pa_decode_window_partitioning(S, cfg.num_q_heads, Hkv, B,
                                                              max_len, W, P)
+        # the even schedule (windowed tensor-core calls) instead of the
+        # partitions: its CTA count, and a merge launch after the attention
+        even_ctas = pa.pa_decode_even_ctas(S, cfg.num_q_heads, Hkv, D, B, inp.q.dtype,
+                                           "fp8_block_scales" if bscaled else
+                                           "fp8" if fp8 else "16bit", max_len, W, P)
+        if even_ctas:
+            splits, ptoks = None, None
         if fp8:
             ws_bytes = pa.pa_decode_fp8_workspace_bytes(S, cfg.num_q_heads, Hkv, D, B,
                                                         inp.q.dtype, max_len, W, P)
@@ -613,7 +621,8 @@ def ours_arm(args):
             if ev is not None and layer == 0:
                 ev[1].record(stream)
 
-    launches_per_step = 1 + LAYERS * (2 + (1 if bscaled else 0) + (1 if splits > 1 else 0))
+    launches_per_step = 1 + LAYERS * (2 + (1 if bscaled else 0) +
+                                      (1 if even_ctas or splits > 1 else 0))
     launch_label = (cfg.name + ("_fp8b" if bscaled else "_fp8" if fp8 else "") +
                     (f"_q{N}" if N > 1 else "") + (f"_w{W}" if W else ""))   # one attention launch
     label = launch_label + (f"_L{LAYERS}" if LAYERS > 1 else "")
@@ -810,7 +819,9 @@ def ours_arm(args):
             "context_tokens": tokens, "kv_read_bytes_per_step": LAYERS * kv_bytes,
             **({"kv_bytes_note": "codes plus 8 B of scales per attended (block, KV head)"}
                if bscaled else {}),
-            "pool_blocks": inp.num_blocks, "partitions": splits, "partition_tokens": ptoks,
+            "pool_blocks": inp.num_blocks,
+            **({"even_schedule_ctas": even_ctas} if even_ctas else
+               {"partitions": splits, "partition_tokens": ptoks}),
             "l2": ("graph-replayed steps: inputs larger than L2 (KV read per step %.2f GB, "
                    "pool %.2f GB; 129 MB L2), no flush" % (kv_bytes / 1e9,
                                                            2 * kc.numel() * elt / 1e9)

@@ -298,9 +298,9 @@ PA_API int pa_reshape_and_cache_fp8(const void* k, const void* v, int64_t num_to
  * partitioning differs from pa_decode_attention's: 16-bit queries, head size
  * 128 and blocks of at least 8 tokens run the tensor-core kernel, which
  * takes the tensor-core partition sizes for every group size and, for a
- * window that cuts the longest sequence, as many splits as keep its three
- * CTAs per SM busy. pa_decode_fp8_partitioning reports the choice. k_scale
- * and v_scale must be positive (else PA_ERR_SHAPE).
+ * window that cuts the longest sequence, one wave of three CTAs per SM
+ * (pa_decode_even_ctas). pa_decode_fp8_partitioning reports the
+ * partitions. k_scale and v_scale must be positive (else PA_ERR_SHAPE).
  */
 /*
  * pa_decode_fp8_workspace_bytes — scratch for the fp8-pool decode calls
@@ -406,8 +406,33 @@ PA_API int pa_decode_attention_fp8_scaled(const void* q, const void* key_cache,
  * window's first tile is read whole), so with partition_size == 0 the
  * partitions are sized for one wave of resident CTAs (the most splits per
  * (sequence, KV head) pair that still fit, at least 256 tokens each) rather
- * than the two waves of the unwindowed calls. window < 0 is PA_ERR_SHAPE.
+ * than the two waves of the unwindowed calls. Calls for which
+ * pa_decode_even_ctas returns a positive count do not use these partitions.
+ * window < 0 is PA_ERR_SHAPE.
+ *
+ * pa_decode_even_ctas — whether a decode call with these sizes runs the
+ * even schedule, and over how many CTAs. Calls with a window that cuts the
+ * longest sequence (0 < window < max_seq_len), partition_size == 0, head
+ * size 128, at most 8192 sequences and the tensor-core kernel (16-bit
+ * queries; 16-bit pools with groups of 2, 4 or 8, or fp8 pools with any
+ * group; blocks of at least 8 tokens) run one wave of CTAs (SMs x 2 for
+ * 16-bit pools, x 3 for fp8 pools, x 4 for fp8 pools with per-block
+ * scales). Each CTA takes whole partitions of the fixed partitioning in
+ * turn, unless whole partitions would leave the busiest CTA more than 1.25
+ * times the mean work; then the even schedule runs: the batch's 64-token
+ * tiles — those of every (sequence, KV head) pair in order, each pair from
+ * its window's first tile — are cut into C runs of equal length, one per
+ * CTA (C = the wave, fewer for small batches), and a second launch merges
+ * the pairs cut between CTAs and writes the zero outputs of empty
+ * sequences. Returns C (> 0) for such calls, 0 for calls that use the fixed
+ * partitions, a negative status on invalid sizes. kv_format: 0 = 16-bit
+ * pools, 1 = fp8 pools with one scale per pool, 2 = fp8 pools with
+ * per-block scales; dtype is the query type. The workspace queries size
+ * the scratch for either schedule.
  */
+PA_API int pa_decode_even_ctas(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+                               int block_size, int dtype, int kv_format, int max_seq_len,
+                               int window, int partition_size);
 PA_API int pa_decode_window_partitioning(int num_seqs, int num_q_heads, int num_kv_heads,
                                          int block_size, int max_seq_len, int window,
                                          int partition_size, int* num_splits_out,
@@ -415,8 +440,9 @@ PA_API int pa_decode_window_partitioning(int num_seqs, int num_q_heads, int num_
 /*
  * pa_decode_fp8_partitioning — the partition count and length that
  * pa_decode_attention_fp8 (window = 0) or pa_decode_attention_fp8_window
- * uses with the same sizes; head_size and dtype (the query type) select
- * the kernel. Either output pointer (host) may be NULL. Invalid sizes give
+ * uses with the same sizes, unless pa_decode_even_ctas reports the even
+ * schedule for them; head_size and dtype (the query type) select the
+ * kernel. Either output pointer (host) may be NULL. Invalid sizes give
  * PA_ERR_SHAPE, an unknown dtype PA_ERR_DTYPE.
  */
 PA_API int pa_decode_fp8_partitioning(int num_seqs, int num_q_heads, int num_kv_heads,

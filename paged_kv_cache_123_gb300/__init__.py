@@ -14,7 +14,7 @@ from .ops import (  # noqa: F401
     pa_reshape_and_cache_fp8, pa_decode_attention_fp8, pa_decode_window_workspace_bytes,
     pa_decode_attention_window, pa_decode_attention_fp8_window, pa_selftest_bounded_wait,
     pa_decode_window_partitioning, pa_decode_fp8_partitioning, pa_reshape_and_cache_fp8_scaled,
-    pa_decode_attention_fp8_scaled, pa_decode_fp8_workspace_bytes,
+    pa_decode_attention_fp8_scaled, pa_decode_fp8_workspace_bytes, pa_decode_even_ctas,
 )
 from ._lib import PagedAttnError, LIB_PATH, lib  # noqa: F401
 from .block_pool import BlockPool  # noqa: F401

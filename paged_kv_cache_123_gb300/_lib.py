@@ -34,6 +34,7 @@ SIGNATURES = {
     "pa_decode_partitioning": ([_c_i32] * 6 + [_c_p, _c_p], _c_i32),
     "pa_decode_window_partitioning": ([_c_i32] * 7 + [_c_p, _c_p], _c_i32),
     "pa_decode_fp8_partitioning": ([_c_i32] * 9 + [_c_p, _c_p], _c_i32),
+    "pa_decode_even_ctas": ([_c_i32] * 10, _c_i32),
     "pa_decode_attention": ([_c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32, _c_i32,
                              _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32, _c_i32, _c_p,
                              _c_p, _c_i64, _c_p], _c_i32),

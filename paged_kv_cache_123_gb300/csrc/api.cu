@@ -146,6 +146,56 @@ int covered_len(int max_seq_len, int window) {
 // covers window .. window + 63 tokens.
 bool windowed(int max_seq_len, int window) { return window > 0 && window < max_seq_len; }
 
+// Windowed tensor-core decode calls (head size 128) with automatic
+// partitioning run one wave of resident CTAs (ctas_per_sm per SM: 2 for
+// 16-bit pools, 3 for fp8 pools, 4 for fp8 pools with per-block scales).
+// A window cuts every long sequence to about the same work, and the fixed
+// partitions give items of equal length: when there are more items than
+// slots, each CTA walks several (items_per_cta, strided). Whole items rarely
+// divide evenly over the slots: with per = ceil(items / slots) items per
+// CTA, the busiest CTA does imbalance = per * slots / items times the mean
+// work. Above kEvenImbalance the even schedule takes over: the batch's
+// 64-token tiles (all (sequence, KV head) pairs in order) are cut into C
+// equal consecutive runs, one per CTA, and a merge launch combines the pairs
+// cut between CTAs. Measured on GB300: the GQA-72B batch with a 1000-token
+// window over fp8 pools (1,024 items for 456 slots, imbalance 1.34) went
+// from 0.57 to 0.63 of the copy bandwidth; at imbalance 1.19 or below (the
+// same window over 16-bit pools, the long-context batch with a 4096-token
+// window, the Llama-7B batch with a 333-token window over fp8 pools) the
+// merge launch cost as much as the balance gained or more.
+// The start of a CTA's share is found by a pass over the sequence lengths
+// in every CTA, so the even schedule is kept to batches of at most
+// kEvenMaxSeqs sequences.
+constexpr int kEvenMaxSeqs = 8192;
+constexpr double kEvenImbalance = 1.25;
+bool even_applies(int num_seqs, int head_size, int max_seq_len, int window, int partition_size,
+                  bool tc_path) {
+  return tc_path && head_size == 128 && partition_size == 0 && windowed(max_seq_len, window) &&
+         num_seqs <= kEvenMaxSeqs;
+}
+// For a call where even_applies: the items per CTA of the strided walk
+// (items_per_cta) or the CTA count of the even schedule (even_ctas > 0).
+void wave_plan(int num_seqs, int num_kv_heads, int splits, int max_seq_len, int window,
+               int sm_count, int ctas_per_sm, int* items_per_cta, int64_t* even_ctas) {
+  const int64_t items = (int64_t)splits * num_kv_heads * num_seqs;
+  const int64_t slots = (int64_t)sm_count * ctas_per_sm;
+  const int64_t per = std::max<int64_t>(1, (items + slots - 1) / slots);
+  *items_per_cta = (int)std::min<int64_t>(1 << 20, per);
+  *even_ctas = 0;
+  if (items > 0 && (double)(per * slots) > kEvenImbalance * (double)items) {
+    const int64_t tiles_per_pair = ((int64_t)covered_len(max_seq_len, window) + 63) / 64;
+    const int64_t upper = (int64_t)num_seqs * num_kv_heads * tiles_per_pair;
+    *even_ctas = std::max<int64_t>(1, std::min(slots, upper));
+    *items_per_cta = 1;
+  }
+}
+// partial outputs [C][2][G][D], maxima and sums [C][2][G][2], records [C][2]
+int64_t even_workspace(int64_t ctas, int group, int head_size) {
+  const int64_t acc = ctas * 2 * group * head_size * 4;
+  const int64_t ml = ctas * 2 * group * 2 * 4;
+  return ((acc + 255) / 256) * 256 + ((ml + 255) / 256) * 256 + ctas * 2 * 4;
+}
+
 int decode_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
                         int max_seq_len, int window, int partition_size, bool mma_fp8,
                         int* splits, int* tokens);
@@ -288,6 +338,35 @@ int pa_decode_fp8_partitioning(int num_seqs, int num_q_heads, int num_kv_heads, 
                              num_splits_out, partition_tokens_out);
 }
 
+int pa_decode_even_ctas(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+                        int block_size, int dtype, int kv_format, int max_seq_len, int window,
+                        int partition_size) {
+  if (elt_bytes(dtype) == 0) return PA_ERR_DTYPE;
+  if (kv_format < 0 || kv_format > 2 || window < 0 || partition_size < 0) return PA_ERR_SHAPE;
+  int st = check_decode_shape(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                              max_seq_len);
+  if (st != PA_OK) return st;
+  pa::DecodeArgs a{};
+  a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size; a.block_size = block_size; a.dtype = dtype;
+  const bool tc = kv_format == 0 ? pa::mma_path_applies(a) : pa::mma_fp8_path_applies(a);
+  if (num_seqs == 0 ||
+      !even_applies(num_seqs, head_size, max_seq_len, window, partition_size, tc))
+    return 0;
+  int splits, tokens;
+  st = decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, window,
+                           partition_size, kv_format != 0, &splits, &tokens);
+  if (st != PA_OK) return st;
+  int dev;
+  st = device_setup(&dev);
+  if (st != PA_OK) return st;
+  int per;
+  int64_t C;
+  wave_plan(num_seqs, num_kv_heads, splits, max_seq_len, window, g_sm_count[dev],
+            kv_format == 0 ? 2 : (kv_format == 1 ? 3 : 4), &per, &C);
+  return (int)C;
+}
+
 int64_t pa_decode_fp8_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                       int head_size, int block_size, int dtype,
                                       int max_seq_len, int window, int partition_size) {
@@ -300,10 +379,26 @@ int64_t pa_decode_fp8_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_
   a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
   a.head_size = head_size; a.block_size = block_size; a.dtype = dtype;
   int splits, tokens;
+  const bool tc8 = pa::mma_fp8_path_applies(a);
   st = decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, window,
-                           partition_size, pa::mma_fp8_path_applies(a), &splits, &tokens);
+                           partition_size, tc8, &splits, &tokens);
   if (st != PA_OK) return st;
-  return workspace_for(num_seqs, num_q_heads, head_size, splits);
+  int64_t ws = workspace_for(num_seqs, num_q_heads, head_size, splits);
+  if (even_applies(num_seqs, head_size, max_seq_len, window, partition_size, tc8)) {
+    // the even schedule, if either fp8 call (three CTAs per SM, four with
+    // per-block scales) takes it
+    int dev;
+    st = device_setup(&dev);
+    if (st != PA_OK) return st;
+    for (int per_sm = 3; per_sm <= 4; ++per_sm) {
+      int per;
+      int64_t C;
+      wave_plan(num_seqs, num_kv_heads, splits, max_seq_len, window, g_sm_count[dev], per_sm,
+                &per, &C);
+      if (C > 0) ws = std::max(ws, even_workspace(C, num_q_heads / num_kv_heads, head_size));
+    }
+  }
+  return ws;
 }
 
 int64_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
@@ -345,7 +440,24 @@ int64_t pa_decode_window_workspace_bytes(int num_seqs, int num_q_heads, int num_
   st = decode_partitioning(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, window,
                            partition_size, false, &splits, &tokens);
   if (st != PA_OK) return st;
-  return workspace_for(num_seqs, num_q_heads, head_size, splits);
+  const int64_t fixed = workspace_for(num_seqs, num_q_heads, head_size, splits);
+  // 16-bit queries of the tensor-core shape class take the even schedule,
+  // fp32 queries the partitions: enough for either
+  pa::DecodeArgs a{};
+  a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size; a.block_size = block_size; a.dtype = PA_BF16;
+  if (even_applies(num_seqs, head_size, max_seq_len, window, partition_size,
+                   pa::mma_path_applies(a))) {
+    int dev;
+    st = device_setup(&dev);
+    if (st != PA_OK) return st;
+    int per;
+    int64_t C;
+    wave_plan(num_seqs, num_kv_heads, splits, max_seq_len, window, g_sm_count[dev], 2, &per,
+              &C);
+    if (C > 0) return std::max(fixed, even_workspace(C, num_q_heads / num_kv_heads, head_size));
+  }
+  return fixed;
 }
 
 int pa_decode_attention_window(const void* q, const void* key_cache, const void* value_cache,
@@ -666,30 +778,40 @@ int run_decode(const void* q, const void* key_cache, const void* value_cache,
                covered_len(max_seq_len, window), partition_size, g_sm_count[dev],
                windowed(max_seq_len, window), fp8 && pa::mma_fp8_path_applies(a),
                &a.num_splits, &a.partition);
-  // a window cuts every long sequence to about the same work: when there are
-  // more work items than resident tensor-core CTAs, each CTA walks several
-  // (its producer runs ahead into the next), so all of them run in one wave
-  // instead of leaving a last, partial wave of CTAs running alone (GQA-72B
-  // batch, window 1000: 0.78 -> 0.83 of the copy bandwidth). fp8 pools do
-  // the same with the fp8 kernel's three CTAs per SM.
+  // a window cuts every long sequence to about the same work: one wave of
+  // tensor-core CTAs walks the items (wave_plan)
   a.items_per_cta = 1;
-  const bool multi16 = !fp8 && head_size == 128 && pa::mma_path_applies(a);
-  const bool multi8 = fp8 && pa::mma_fp8_path_applies(a);
-  if (windowed(max_seq_len, window) && (multi16 || multi8)) {
-    const int64_t items = (int64_t)a.num_splits * num_kv_heads * num_seqs;
-    // resident CTAs per SM: 2 (16-bit), 3 (fp8), 4 (fp8, per-block scales)
-    const int64_t slots = (int64_t)g_sm_count[dev] * (multi8 ? (k_scales ? 4 : 3) : 2);
-    a.items_per_cta = (int)std::min<int64_t>(1 << 20, (items + slots - 1) / slots);
-  }
-  const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);
-  a.ws_acc = nullptr; a.ws_ml = nullptr;
-  if (need > 0) {
+  a.even_ctas = 0;
+  a.ws_acc = nullptr; a.ws_ml = nullptr; a.ws_rec = nullptr;
+  const bool tc16 = !fp8 && pa::mma_path_applies(a);
+  const bool tc8 = fp8 && pa::mma_fp8_path_applies(a);
+  int64_t C = 0;
+  if (even_applies(num_seqs, head_size, max_seq_len, window, partition_size, tc16 || tc8))
+    wave_plan(num_seqs, num_kv_heads, a.num_splits, max_seq_len, window, g_sm_count[dev],
+              tc8 ? (k_scales ? 4 : 3) : 2, &a.items_per_cta, &C);
+  if (C > 0) {
+    const int group = num_q_heads / num_kv_heads;
+    const int64_t need = even_workspace(C, group, head_size);
     if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PA_ERR_ALIGN;
-    const int64_t n = (int64_t)num_seqs * num_q_heads * a.num_splits;
-    a.ws_acc = static_cast<float*>(workspace);
-    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                       ((n * head_size * 4 + 255) / 256) * 256);
+    char* w = static_cast<char*>(workspace);
+    const int64_t acc = ((C * 2 * group * head_size * 4 + 255) / 256) * 256;
+    const int64_t ml = ((C * 2 * group * 2 * 4 + 255) / 256) * 256;
+    a.even_ctas = (int)C;
+    a.num_splits = 1;
+    a.ws_acc = reinterpret_cast<float*>(w);
+    a.ws_ml = reinterpret_cast<float*>(w + acc);
+    a.ws_rec = reinterpret_cast<int*>(w + acc + ml);
+  } else {
+    const int64_t need = workspace_for(num_seqs, num_q_heads, head_size, a.num_splits);
+    if (need > 0) {
+      if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+      if (!aligned16(workspace)) return PA_ERR_ALIGN;
+      const int64_t n = (int64_t)num_seqs * num_q_heads * a.num_splits;
+      a.ws_acc = static_cast<float*>(workspace);
+      a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         ((n * head_size * 4 + 255) / 256) * 256);
+    }
   }
   a.out = out;
   a.err = g_err_ptr[dev];

@@ -18,11 +18,15 @@
 // each tile each, keep their own running softmax state (log2 domain), and
 // free the stage through an mbarrier; at the end of an item they merge in
 // the stage of its last tile and release it afterwards. A CTA takes one
-// item, or (windowed batches, where every item has about the same work)
-// several in turn, its producer running ahead into the next. Every wait is
-// bounded: a stuck barrier raises an abort flag, the CTA lets its copies in
-// flight land (with its own limit) and leaves, and PA_ERR_TIMEOUT is
-// latched.
+// item, or (MULTI: windowed batches, one wave of CTAs) several in turn, its
+// producer running ahead into the next: items blockIdx.x, blockIdx.x +
+// gridDim.x, ..., or (the even schedule) an equal share of the batch's
+// 64-token tiles: the tiles of all (sequence, KV head) pairs in order, cut
+// into gridDim.x consecutive runs, the CTA walking the segments (pieces of
+// pairs) of its run; a pair cut between CTAs leaves partial results that
+// even_merge_kernel combines. Every wait is bounded: a stuck barrier raises
+// an abort flag, the CTA lets its copies in flight land (with its own limit)
+// and leaves, and PA_ERR_TIMEOUT is latched.
 //
 // Rows past the end of the sequence (the tail of the last block, blocks not
 // loaded) are masked to -inf in S and zeroed in the V tile before the P*V
@@ -51,7 +55,17 @@ template <bool KV8, bool SCALED>
 constexpr int ring_stages() { return (KV8 && !SCALED) ? 4 : 3; }
 template <bool KV8, bool SCALED>
 constexpr int ctas_per_sm() { return KV8 ? (SCALED ? 4 : 3) : 2; }
+// MULTI: an item's query group rides in the stage of its first tile, in a
+// slot that keeps the stages 1024-byte aligned (128-byte swizzle), so the
+// consumers hold no prefetched query in registers (a one-item CTA loads it
+// from global memory while its first tile is in flight instead)
+template <typename T, int D, int G, bool MULTI>
+constexpr int q_slot_bytes() { return MULTI ? (G * D * (int)sizeof(T) + 1023) / 1024 * 1024 : 0; }
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+// even schedule: flags of a CTA's record (its last segment): it walked a
+// segment, that segment starts at its pair's first tile, ends before its
+// last, and is the CTA's only segment
+constexpr int kRecNonEmpty = 1, kRecStart0 = 2, kRecCutEnd = 4, kRecSingle = 8;
 #define kNegInfM (-__int_as_float(0x7f800000))
 
 
@@ -79,8 +93,9 @@ __device__ __forceinline__ bool consumers_bar_and(bool ok) {
 // fp8 pools: half the shared memory per stage and a register budget for
 // three CTAs per SM (four with per-block scales), so more warps hide the
 // conversion latency.
-// MULTI: each CTA walks several work items (items_per_cta > 1); the one-item
-// instantiation compiles to a single pass.
+// MULTI: the CTA walks several items (a.items_per_cta > 1: strided items;
+// a.even_ctas > 0: the segments of its even share of the batch's tiles, see
+// the top of this file); otherwise it takes work item blockIdx.x.
 // SCALED (fp8 pools only): the blocks carry their own scales (a.k_scales /
 // a.v_scales [num_blocks][num_kv_heads]). The producer lane that loads a
 // block piece also reads its two scales and leaves them beside the stage
@@ -101,7 +116,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   constexpr int ROW_BYTES = HALVES * 128;        // one 16-bit token row (D * 2 bytes)
   constexpr int IN_ROW = KV8 ? D : ROW_BYTES;    // one token row as loaded
   constexpr int KV_BYTES = kTile * IN_ROW;       // K (or V) part of a stage
-  constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  constexpr int Q_BYTES = G * D * (int)sizeof(T);
+  constexpr int STAGE_BYTES = 2 * KV_BYTES + q_slot_bytes<T, D, G, MULTI>();
   constexpr int PRIV_BYTES = 0;
   constexpr int kSt = ring_stages<KV8, SCALED>();
   static_assert(!KV8 || D == 128, "fp8 pools: head size 128 (one 128-byte line per row)");
@@ -138,11 +154,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   const int B = a.block_size;
   const int bshift = __ffs(B) - 1;
   const int R = B < kTile ? B : kTile;           // rows per TMA box
-  // work items (partition, KV head, sequence), partition fastest; a CTA
-  // takes items blockIdx.x, blockIdx.x + gridDim.x, ... (exactly one when
-  // the grid covers them all). Producer and consumers walk the same items
-  // and carry the ring position across them.
+  // work items (partition, KV head, sequence), partition fastest
   const int n_items = a.num_splits * Hkv * a.num_seqs;
+  const bool even = MULTI && a.even_ctas > 0;   // the even schedule
   // per-warp row maxima and sums for the merge of an item ([4][8] each)
   float* sm_m = reinterpret_cast<float*>(tile_mask + kSt);
   float* sm_l = sm_m + kMmaConsumers * 8;
@@ -151,9 +165,21 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   float* st_ks = sm_l + kMmaConsumers * 8;
   float* st_vs = st_ks + kSt * 8;
   float* st_vref = st_vs + kSt * 8;
+  // even schedule: the start of this CTA's share, found by all threads
+  // (per-warp sums [5], tiles g0 and g1 of the batch, the offset of g0 in its
+  // sequence's tiles; the sequence and its length)
+  long long* ev_ll = reinterpret_cast<long long*>(
+      smem + ((reinterpret_cast<uint8_t*>(st_vref + kSt) - smem + 7) & ~7));
+  int* ev_i = reinterpret_cast<int*>(ev_ll + 8);
   struct Item {
-    int s, kvh, split, L, lo, t0, t1, nsplit, ntiles;
+    int s, kvh, split, L, lo, t0, t1, ntiles;
     bool bad, zero_out;
+    bool complete;        // covers the pair's whole range: the output is final
+    bool first;           // even: the CTA's first segment (partial slot 0, else 1)
+    bool start0, cut_end; // even: starts at the pair's first tile / ends before its last
+  };
+  auto bad_len = [&](int L) {
+    return L < 0 || L > a.max_seq_len || (int64_t)L > a.table_stride * a.block_size;
   };
   auto item_at = [&](int idx) {
     Item im;
@@ -162,20 +188,110 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     im.kvh = rest % Hkv;
     im.s = rest / Hkv;
     im.L = a.seq_lens[im.s];
-    im.bad = im.L < 0 || im.L > a.max_seq_len || (int64_t)im.L > a.table_stride * a.block_size;
+    im.bad = bad_len(im.L);
     // an empty or invalid sequence: its first partition writes zeros
     im.zero_out = (im.bad || im.L == 0) && im.split == 0;
-    im.lo = 0; im.t0 = 0; im.t1 = 0; im.nsplit = 1; im.ntiles = 0;
+    im.lo = 0; im.t0 = 0; im.t1 = 0; im.ntiles = 0;
+    im.complete = true; im.first = true; im.start0 = true; im.cut_end = false;
     if (!im.bad && im.L > 0) {
       im.lo = window_lo(im.L, a.window);
       im.t0 = window_base(im.lo) + im.split * a.partition;
       if (im.t0 < im.L) {
         im.t1 = min(im.L, im.t0 + a.partition);
-        im.nsplit = (im.L - window_base(im.lo) + a.partition - 1) / a.partition;
+        im.complete = (im.L - window_base(im.lo) + a.partition - 1) / a.partition == 1;
         im.ntiles = (im.t1 - im.t0 + kTile - 1) / kTile;
       }
     }
     return im;
+  };
+  // even schedule: tiles of a sequence of length L (0 for empty or invalid lengths,
+  // whose zeros even_merge_kernel writes)
+  auto seq_tiles = [&](int L) -> int {
+    if (L <= 0 || bad_len(L)) return 0;
+    return (L - window_base(window_lo(L, a.window)) + kTile - 1) / kTile;
+  };
+  auto len_of = [&](int s) { return s < a.num_seqs ? a.seq_lens[s] : 0; };
+  // even schedule: cursor over this CTA's share: g = the batch's next tile (pair
+  // s * Hkv + kvh, tile ta of the pair's ntl), g1 = the end of the share;
+  // Ln = the next sequence's length, loaded ahead
+  struct Cursor {
+    long long g, g1;
+    int s, kvh, ta, L, ntl, Ln;
+    bool first;
+  };
+  auto cursor_item = [&](const Cursor& c) {
+    Item im;
+    im.s = c.s; im.kvh = c.kvh; im.split = 0; im.L = c.L;
+    im.bad = false; im.zero_out = false;
+    im.lo = window_lo(c.L, a.window);
+    const int base = window_base(im.lo);
+    const int tb = (int)min((long long)c.ntl, c.ta + (c.g1 - c.g));
+    im.t0 = base + c.ta * kTile;
+    im.t1 = min(c.L, base + tb * kTile);
+    im.ntiles = tb - c.ta;
+    im.first = c.first;
+    im.start0 = c.ta == 0;
+    im.cut_end = tb < c.ntl;
+    im.complete = im.start0 && !im.cut_end;
+    return im;
+  };
+  auto cursor_next = [&](Cursor& c) {
+    c.g += (int)min((long long)c.ntl, c.ta + (c.g1 - c.g)) - c.ta;
+    c.ta = 0;
+    c.first = false;
+    if (c.g >= c.g1 || ++c.kvh < Hkv) return;
+    c.kvh = 0;
+    do {                                   // the next sequence with tiles
+      if (c.s + 1 >= a.num_seqs) {         // (none: lengths inconsistent, stop)
+        c.g = c.g1;
+        return;
+      }
+      ++c.s;
+      c.L = c.Ln;
+      c.Ln = len_of(c.s + 1);
+      c.ntl = seq_tiles(c.L);
+    } while (c.ntl == 0);
+  };
+  // the CTA's items: item blockIdx.x, items blockIdx.x + k * gridDim.x
+  // (MULTI), or the segments of its even share
+  struct Iter {
+    Cursor c;
+    int idx;
+    bool done;
+  };
+  auto iter_begin = [&]() {
+    Iter w;
+    w.idx = blockIdx.x;
+    if (even) {
+      w.c.g = ev_ll[5];
+      w.c.g1 = ev_ll[6];
+      w.done = ev_i[0] < 0 || w.c.g >= w.c.g1;
+      if (!w.done) {
+        w.c.s = ev_i[0];
+        w.c.L = ev_i[1];
+        w.c.ntl = seq_tiles(w.c.L);
+        const long long off = ev_ll[7];
+        w.c.kvh = (int)(off / w.c.ntl);
+        w.c.ta = (int)(off - (long long)w.c.kvh * w.c.ntl);
+        w.c.Ln = len_of(w.c.s + 1);
+        w.c.first = true;
+      }
+    } else {
+      w.done = w.idx >= n_items;
+    }
+    return w;
+  };
+  auto iter_item = [&](const Iter& w) { return even ? cursor_item(w.c) : item_at(w.idx); };
+  auto iter_next = [&](Iter& w) {
+    if (even) {
+      cursor_next(w.c);
+      w.done = w.c.g >= w.c.g1;
+    } else if (MULTI) {
+      w.idx += gridDim.x;
+      w.done = w.idx >= n_items;
+    } else {
+      w.done = true;
+    }
   };
 
   if (threadIdx.x == 0) {
@@ -184,9 +300,62 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       mbar_init(empty_bar(st), kMmaConsumers);
     }
     *abort_flag = 0;
+    if (even) ev_i[0] = -1;
     mbar_fence_init();
   }
+  if (even) {
+    // the batch's tiles T (every thread sums a contiguous range of
+    // sequences, then an exclusive scan over the threads); this CTA's share
+    // is tiles [g0, g1) with g0 = floor(blockIdx.x * T / gridDim.x), and
+    // the thread whose sequences hold tile g0 finds its sequence
+    const int S = a.num_seqs;
+    const int K = (S + kMmaThreads - 1) / kMmaThreads;
+    const int sb = threadIdx.x * K;
+    long long mine = 0;
+    for (int j = 0; j < K; ++j)
+      if (sb + j < S) mine += seq_tiles(a.seq_lens[sb + j]);
+    long long inc = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long v = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += v;
+    }
+    if (lane == 31) ev_ll[warp] = inc;
+    __syncthreads();
+    long long before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w <= kMmaConsumers; ++w) {
+      const long long t = ev_ll[w];
+      if (w < warp) before += t;
+      total += t;
+    }
+    const long long tiles = total * Hkv, C = gridDim.x;
+    const long long g0 = (long long)blockIdx.x * tiles / C;
+    const long long g1 = ((long long)blockIdx.x + 1) * tiles / C;
+    long long cum = (before + inc - mine) * Hkv;
+    if (g0 < g1 && cum <= g0 && g0 < cum + mine * Hkv) {
+      for (int j = 0; j < K && sb + j < S; ++j) {
+        const int L = a.seq_lens[sb + j];
+        const long long t = (long long)seq_tiles(L) * Hkv;
+        if (g0 < cum + t) {
+          ev_i[0] = sb + j;
+          ev_i[1] = L;
+          ev_ll[7] = g0 - cum;
+          break;
+        }
+        cum += t;
+      }
+    }
+    __syncthreads();        // every thread has read the warp sums
+    if (threadIdx.x == 0) {
+      ev_ll[5] = g0;
+      ev_ll[6] = g1;
+    }
+  }
   __syncthreads();
+  // even schedule: the merge launch may be scheduled now; it waits for this
+  // grid to complete before it reads the partials
+  if (even) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kMmaConsumers) {
     // ---------------- producer warp: lane p owns piece p (R rows of one
@@ -200,14 +369,16 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     int it = 0;                                // tiles issued so far: the ring position
     bool run = true;
     auto in_pool = [&](int64_t b) { return b >= 0 && b < a.num_blocks; };
-    // Issue tile i of item im into the next stage: lane p loads piece p (R
-    // rows of block blk) when `need`. SCALED: ksv and rsv are the piece's K
-    // and V scales, vrt the largest V scale of the item so far (the
-    // reference the consumers' output is kept in).
-    auto issue_tile = [&](const Item& im, int i, int64_t blk, bool need, float ksv, float rsv,
-                          float vrt) -> bool {
+    // Issue the tile starting at token ts of KV head kvh into the next
+    // stage: lane p loads piece p (R rows of block blk) when `need`; the
+    // first tile of an item (qs = its sequence, else -1) also brings the
+    // item's query group. SCALED: ksv and rsv are the piece's K and V
+    // scales, vrt the largest V scale of the item so far (the reference the
+    // consumers' output is kept in).
+    auto issue_tile = [&](int ts, int kvh, int64_t blk, bool need, float ksv, float rsv,
+                          float vrt, int qs) -> bool {
       const int st = it % kSt;
-      const int tok = im.t0 + i * kTile + lane * R;
+      const int tok = ts + lane * R;
       const bool mine = need && in_pool(blk);
       if (need && !mine) latch(a.err, PA_ERR_OUT_OF_RANGE);
       const unsigned pm = __ballot_sync(0xffffffffu, mine);
@@ -227,7 +398,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
         if (lane == 0) {
           st_vref[st] = vrt;
           tile_mask[st] = pm;
-          mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * IN_ROW);
+          mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * IN_ROW +
+                                                  (qs >= 0 ? (uint32_t)Q_BYTES : 0u));
         }
         __syncwarp();
       } else {
@@ -236,16 +408,21 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
             ok = mbar_wait_bounded(empty_bar(st), ((it / kSt) - 1) & 1, abort_flag, kWaitCycles);
           if (ok) {
             tile_mask[st] = pm;
-            mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * IN_ROW);
+            mbar_arrive_expect_tx(full_bar(st), (uint32_t)__popc(pm) * 2u * R * IN_ROW +
+                                                    (qs >= 0 ? (uint32_t)Q_BYTES : 0u));
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) return false;
       }
+      if (lane == 0 && qs >= 0)
+        bulk_load(smem0 + st * STAGE_BYTES + 2 * KV_BYTES,
+                  reinterpret_cast<const T*>(a.q) + ((int64_t)qs * Hq + (int64_t)kvh * G) * D,
+                  (uint32_t)Q_BYTES, full_bar(st));
       if (mine) {
         const uint32_t kdst = smem0 + st * STAGE_BYTES + lane * R * IN_ROW;
         const uint32_t vdst = kdst + KV_BYTES;
-        const int z = (int)(blk * Hkv + im.kvh);
+        const int z = (int)(blk * Hkv + kvh);
         const int y = tok & (B - 1);
         if (KV8) {
           tma_load_3d(kdst, &tmK, 0, y, z, full_bar(st));
@@ -261,16 +438,15 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     if constexpr (!SCALED) {
       // the table entries of a tile are read in parallel (one lane per
       // piece) right before its stage is awaited
-      for (int idx = blockIdx.x; run && idx < n_items;
-           idx = MULTI ? idx + (int)gridDim.x : n_items) {
-        const Item im = item_at(idx);
+      for (Iter w = iter_begin(); run && !w.done; iter_next(w)) {
+        const Item im = iter_item(w);
         const int32_t* trow = a.tables + (int64_t)im.s * a.table_stride;
         for (int i = 0; i < im.ntiles; ++i) {
           const int ts = im.t0 + i * kTile;
           const int tok = ts + lane * R;
           const bool need = lane < npieces && tok < min(im.t1, ts + kTile) && tok + R > im.lo;
           const int64_t blk = need ? (int64_t)trow[tok >> bshift] : -1;
-          if (!issue_tile(im, i, blk, need, 0.f, 0.f, 0.f)) {
+          if (!issue_tile(ts, im.kvh, blk, need, 0.f, 0.f, 0.f, MULTI && i == 0 ? im.s : -1)) {
             run = false;
             break;
           }
@@ -279,67 +455,77 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     } else {
       // per-block scales: each piece's scales are read through its table
       // entry, two dependent loads. They run ahead of the copies in a
-      // software pipeline over the CTA's tiles (cursor: item idx, tile i):
-      // while tile k is issued, the table entries of tile k+2 and the scales
-      // of tile k+1 are in flight.
-      struct Cur {
-        int idx, i;
-        Item im;
+      // software pipeline over the CTA's tiles: while tile k is issued, the
+      // table entries of tile k+2 and the scales of tile k+1 are in flight.
+      // One cursor (gw, gim, gi) walks the items; the pipeline holds only
+      // small per-tile descriptors.
+      struct TD {
+        int s, kvh, ts;
+        bool need, first;     // this lane's piece is attended; the item's first tile
       };
-      auto settle = [&](Cur& c) {              // skip items without tiles
-        while (c.idx < n_items && c.i >= c.im.ntiles) {
-          c.idx = MULTI ? c.idx + (int)gridDim.x : n_items;
-          c.i = 0;
-          if (c.idx < n_items) c.im = item_at(c.idx);
+      Iter gw = iter_begin();
+      Item gim;
+      int gi = 0;
+      if (!gw.done) gim = iter_item(gw);
+      auto settle = [&]() {                    // skip items without tiles
+        while (!gw.done && gi >= gim.ntiles) {
+          iter_next(gw);
+          gi = 0;
+          if (!gw.done) gim = iter_item(gw);
         }
       };
-      auto next = [&](Cur c) {
-        ++c.i;
-        settle(c);
-        return c;
+      settle();
+      // the next tile's descriptor (valid = false past the last tile)
+      auto gen = [&](TD& td) -> bool {
+        if (gw.done) {
+          td.need = false;
+          td.first = false;
+          return false;
+        }
+        td.s = gim.s;
+        td.kvh = gim.kvh;
+        td.ts = gim.t0 + gi * kTile;
+        td.first = gi == 0;
+        const int tok = td.ts + lane * R;
+        td.need = lane < npieces && tok < min(gim.t1, td.ts + kTile) && tok + R > gim.lo;
+        ++gi;
+        settle();
+        return true;
       };
-      auto needs = [&](const Cur& c) {
-        if (c.idx >= n_items || lane >= npieces) return false;
-        const int ts = c.im.t0 + c.i * kTile;
-        const int tok = ts + lane * R;
-        return tok < min(c.im.t1, ts + kTile) && tok + R > c.im.lo;
+      auto table_of = [&](const TD& td) -> int64_t {
+        if (!td.need) return -1;
+        return a.tables[(int64_t)td.s * a.table_stride + ((td.ts + lane * R) >> bshift)];
       };
-      auto table_of = [&](const Cur& c) -> int64_t {
-        if (!needs(c)) return -1;
-        const int tok = c.im.t0 + c.i * kTile + lane * R;
-        return a.tables[(int64_t)c.im.s * a.table_stride + (tok >> bshift)];
-      };
-      Cur c0;
-      c0.idx = blockIdx.x;
-      c0.i = 0;
-      if (c0.idx < n_items) c0.im = item_at(c0.idx);
-      settle(c0);
-      Cur c1 = next(c0);
-      int64_t b0 = table_of(c0), b1 = table_of(c1);
+      TD d0, d1, d2;
+      bool v0 = gen(d0), v1 = gen(d1);
+      int64_t b0 = table_of(d0), b1 = table_of(d1);
       // pieces that are not loaded get scales 0 (their rows are masked)
       float ks0 = 0.f, vs0 = 0.f, vrun = 0.f;
       if (in_pool(b0)) {
-        ks0 = a.k_scales[b0 * Hkv + c0.im.kvh];
-        vs0 = a.v_scales[b0 * Hkv + c0.im.kvh];
+        ks0 = a.k_scales[b0 * Hkv + d0.kvh];
+        vs0 = a.v_scales[b0 * Hkv + d0.kvh];
       }
-      while (run && c0.idx < n_items) {
-        const Cur c2 = next(c1);
-        const int64_t b2 = table_of(c2);       // two tiles ahead
+      while (run && v0) {
+        const bool v2 = gen(d2);
+        const int64_t b2 = table_of(d2);       // two tiles ahead
         float ks1 = 0.f, vs1 = 0.f;
         if (in_pool(b1)) {                     // one tile ahead
-          ks1 = a.k_scales[b1 * Hkv + c1.im.kvh];
-          vs1 = a.v_scales[b1 * Hkv + c1.im.kvh];
+          ks1 = a.k_scales[b1 * Hkv + d1.kvh];
+          vs1 = a.v_scales[b1 * Hkv + d1.kvh];
         }
         // the item's running maximum V scale (scales are >= 0, so their
         // bit patterns order like the values)
-        if (c0.i == 0) vrun = 0.f;
+        if (d0.first) vrun = 0.f;
         vrun = fmaxf(vrun, __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(vs0))));
-        if (!issue_tile(c0.im, c0.i, b0, needs(c0), ks0, vs0, vrun)) {
+        if (!issue_tile(d0.ts, d0.kvh, b0, d0.need, ks0, vs0, vrun,
+                        MULTI && d0.first ? d0.s : -1)) {
           run = false;
           break;
         }
-        c0 = c1;
-        c1 = c2;
+        d0 = d1;
+        d1 = d2;
+        v0 = v1;
+        v1 = v2;
         b0 = b1;
         b1 = b2;
         ks0 = ks1;
@@ -362,11 +548,11 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     T* out = reinterpret_cast<T*>(a.out);
     int it = 0;                                // tiles consumed so far: the ring position
     bool run = true;
-    // query fragments of item idx (its sequence and KV head), and the factor
-    // qmul by which the products of these fragments must be multiplied
-    auto q_frags = [&](int idx, uint32_t (&qd)[KSTEPS][2], float& qmul) {
-      const int kv = (idx / a.num_splits) % Hkv, sq = idx / a.num_splits / Hkv;
-      const T* qb = reinterpret_cast<const T*>(a.q) + ((int64_t)sq * Hq + (int64_t)kv * G) * D;
+    // query fragments of an item from its query group [G][D] (q_read: in
+    // the slot of the item's first stage, or in global memory), then in the
+    // products' type with the factor qmul by which the products must be
+    // multiplied (q_finish)
+    auto q_read = [&](const T* qb, uint32_t (&qd)[KSTEPS][2]) {
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
         if (n < G) {
@@ -381,6 +567,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           qd[ks][0] = qd[ks][1] = 0u;
         }
       }
+    };
+    auto q_finish = [&](uint32_t (&qd)[KSTEPS][2], float& qmul) {
       qmul = 1.f;
       if constexpr (kQRescale) {
         // the lanes of the warp hold the whole group between them
@@ -414,25 +602,17 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           for (int j = 0; j < 2; ++j) qd[ks][j] = to_mma_pair<T, MT>(qd[ks][j]);
       }
     };
-    // MULTI: the next item's query is loaded one item ahead, so its latency
-    // hides behind the current item's tiles
-    uint32_t qn[KSTEPS][2];
-    float qmul_n = 1.f;
-    if (MULTI && (int)blockIdx.x < n_items) q_frags(blockIdx.x, qn, qmul_n);
-    for (int idx = blockIdx.x; run && idx < n_items;
-         idx = MULTI ? idx + (int)gridDim.x : n_items) {
-    const Item im = item_at(idx);
+    Iter cw = iter_begin();
+    // even schedule: the segments walked and the last one (for the merge
+    // launch)
+    int nseg = 0;
+    int last_pair = 0;
+    bool last_start0 = false, last_cut_end = false;
+    while (run && !cw.done) {
+    const Item im = iter_item(cw);
+    iter_next(cw);
     uint32_t qf[KSTEPS][2];
     float qmul = 1.f;
-    if (MULTI) {
-#pragma unroll
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-        qf[ks][0] = qn[ks][0];
-        qf[ks][1] = qn[ks][1];
-      }
-      qmul = qmul_n;
-      if (idx + (int)gridDim.x < n_items) q_frags(idx + (int)gridDim.x, qn, qmul_n);
-    }
     if (im.zero_out) {
       if (im.L != 0 && threadIdx.x == 0) latch(a.err, PA_ERR_OUT_OF_RANGE);
       for (int i = threadIdx.x; i < G * D; i += kMmaConsumers * 32)
@@ -441,14 +621,22 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     }
     if (im.ntiles == 0) continue;
     const int s = im.s, kvh = im.kvh, split = im.split, lo = im.lo;
-    const int t0 = im.t0, t1 = im.t1, nsplit = im.nsplit, ntiles = im.ntiles;
+    const int t0 = im.t0, t1 = im.t1, ntiles = im.ntiles;
+    ++nseg;
+    last_pair = s * Hkv + kvh;
+    last_start0 = im.start0;
+    last_cut_end = im.cut_end;
     // merge state, per consumer warp; heads 2c and 2c+1 of this lane
     float m0 = kNegInfM, m1 = kNegInfM, l0 = 0.f, l1 = 0.f;
     float o[KSTEPS][4];
 #pragma unroll
     for (int i = 0; i < KSTEPS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    if (!MULTI) q_frags(idx, qf, qmul);
-    const float sl2q = sl2 * qmul;
+    float sl2q = sl2;
+    if (!MULTI) {
+      q_read(reinterpret_cast<const T*>(a.q) + ((int64_t)s * Hq + (int64_t)kvh * G) * D, qf);
+      q_finish(qf, qmul);
+      sl2q = sl2 * qmul;
+    }
     // SCALED: the reference V scale the warp's output is kept in (0 until
     // the first tile) and its reciprocal
     float vref = 0.f, inv_vref = 0.f;
@@ -461,6 +649,11 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
       if (!mbar_wait_bounded(full_bar(st), (it / kSt) & 1, abort_flag, kWaitCycles)) {
         ok = false;
         break;
+      }
+      if (MULTI && i == 0) {     // the item's query group came with its first tile
+        q_read(reinterpret_cast<const T*>(smem + st * STAGE_BYTES + 2 * KV_BYTES), qf);
+        q_finish(qf, qmul);
+        sl2q = sl2 * qmul;
       }
       const int ts = t0 + i * kTile;
       const int te = min(t1, ts + kTile);
@@ -681,23 +874,42 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     }
     }
     consumers_bar();
+    // per head g (thread g): the warps' weights 2^(m_w - M) (times v_scale)
+    // replace their maxima in sm_m; sm_l keeps 1 / sum (column g of warp 0),
+    // M (warp 1) and the sum (warp 2)
+    if (threadIdx.x < G) {
+      const int g = threadIdx.x;
+      float M = kNegInfM;
+#pragma unroll
+      for (int w = 0; w < kMmaConsumers; ++w) M = fmaxf(M, sm_m[w * 8 + g]);
+      float Ls = 0.f;
+#pragma unroll
+      for (int w = 0; w < kMmaConsumers; ++w) {
+        const float mw = sm_m[w * 8 + g];
+        const float wt = (mw == kNegInfM) ? 0.f : exp2f(mw - M);
+        Ls += sm_l[w * 8 + g] * wt;
+        sm_m[w * 8 + g] = wt * v_scale;
+      }
+      sm_l[g] = Ls > 0.f ? 1.f / Ls : 0.f;
+      sm_l[8 + g] = M;
+      sm_l[16 + g] = Ls;
+    }
+    consumers_bar();
     for (int e = threadIdx.x; e < G * D; e += kMmaConsumers * 32) {
     const int g = e / D, d = e - g * D;
-    float M = kNegInfM;
+    float O = 0.f;
 #pragma unroll
-    for (int w = 0; w < kMmaConsumers; ++w) M = fmaxf(M, sm_m[w * 8 + g]);
-    float Ls = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMmaConsumers; ++w) {
-      const float mw = sm_m[w * 8 + g];
-      const float wt = (mw == kNegInfM) ? 0.f : exp2f(mw - M);
-      Ls += sm_l[w * 8 + g] * wt;
-      O += sm_o[(w * 8 + g) * D + d] * wt;
-    }
-    O *= v_scale;
+    for (int w = 0; w < kMmaConsumers; ++w) O += sm_o[(w * 8 + g) * D + d] * sm_m[w * 8 + g];
+    const float M = sm_l[8 + g], Ls = sm_l[16 + g];
     const int h = kvh * G + g;
-    if (nsplit == 1) {
-      out[((int64_t)s * Hq + h) * D + d] = Vec<T>::cvt_out(Ls > 0.f ? O / Ls : 0.f);
+    if (im.complete) {
+      out[((int64_t)s * Hq + h) * D + d] = Vec<T>::cvt_out(O * sm_l[g]);
+    } else if (even) {
+      // a pair cut between CTAs: the CTA's first segment in slot 0, its
+      // last in slot 1
+      const int64_t slot = ((int64_t)blockIdx.x * 2 + (im.first ? 0 : 1)) * G + g;
+      a.ws_acc[slot * D + d] = O;
+      if (d == 0) { a.ws_ml[2 * slot] = M; a.ws_ml[2 * slot + 1] = Ls; }
     } else {
       const int64_t slot = ((int64_t)s * Hq + h) * a.num_splits + split;
       a.ws_acc[slot * D + d] = O;
@@ -710,9 +922,139 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_bar(st_last));
     }
+    // even schedule: the record even_merge_kernel reads: the pair of the
+    // CTA's last segment and how it was cut (nothing, after a timeout)
+    if (even && threadIdx.x == 0) {
+      int flags = 0;
+      if (run && nseg > 0)
+        flags = kRecNonEmpty | (last_start0 ? kRecStart0 : 0) | (last_cut_end ? kRecCutEnd : 0) |
+                (nseg == 1 ? kRecSingle : 0);
+      a.ws_rec[2 * blockIdx.x] = last_pair;
+      a.ws_rec[2 * blockIdx.x + 1] = flags;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) latch(a.err, PA_ERR_TIMEOUT);
+}
+
+// The second launch of an even-schedule call, one CTA of kMergeThreads threads per
+// CTA of the attention launch (c = blockIdx.x, C = gridDim.x):
+//  - sequences s = c, c + C, ... that are empty or invalid get zero outputs
+//    (invalid ones also latch PA_ERR_OUT_OF_RANGE): they have no tiles, so
+//    no attention CTA visits them, and this runs before the attention
+//    launch has finished (programmatic dependent launch);
+//  - if attention CTA c holds the start of a pair that continues into the
+//    following CTAs (its last segment starts at the pair's first tile and
+//    ends before its last), this CTA merges the pair's partial results:
+//    CTA c's (slot 0 if that segment was its only one, else slot 1), then
+//    slot 0 of every following CTA with a segment up to the one where the
+//    pair ends, with the log-sum-exp weights of combine_kernel:
+//        M = max_p m_p,  w_p = 2^(m_p - M),  o = sum_p w_p acc_p / sum_p w_p l_p
+// Warp 0 reads this CTA's record and the following ones 32 at a time and
+// lists the pieces in shared memory; each thread then merges its output
+// elements four pieces at a time (online: a running maximum with rescale),
+// with all loads of a step independent of each other.
+constexpr int kMergeThreads = 256;
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kMergeThreads) even_merge_kernel(const DecodeArgs a) {
+  extern __shared__ int pieces[];          // [gridDim.x]: partial-slot indices k*2+slot
+  __shared__ int n_pieces, head_pair;
+  const int c = blockIdx.x, C = gridDim.x;
+  const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
+  T* out = reinterpret_cast<T*>(a.out);
+  for (int s = c; s < a.num_seqs; s += C) {
+    const int L = a.seq_lens[s];
+    const bool bad = L < 0 || L > a.max_seq_len || (int64_t)L > a.table_stride * a.block_size;
+    if (bad || L == 0) {
+      if (bad && threadIdx.x == 0) latch(a.err, PA_ERR_OUT_OF_RANGE);
+      for (int i = threadIdx.x; i < Hq * D; i += blockDim.x)
+        out[(int64_t)s * Hq * D + i] = Vec<T>::cvt_out(0.f);
+    }
+  }
+  // the attention launch's records and partials are complete past this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    constexpr int kHead = kRecNonEmpty | kRecStart0 | kRecCutEnd;
+    int n = 0;
+    for (int b = c; b < C; b += 32) {
+      const int k = b + lane;
+      const int2 r = k < C ? reinterpret_cast<const int2*>(a.ws_rec)[k] : make_int2(0, 0);
+      if (b == c) {
+        // this CTA's own record: does it hold the start of a cut pair?
+        const int f0 = __shfl_sync(0xffffffffu, r.y, 0);
+        if ((f0 & kHead) != kHead) break;
+        if (lane == 0) {
+          pieces[0] = 2 * c + ((f0 & kRecSingle) ? 0 : 1);
+          head_pair = r.x;
+        }
+        n = 1;
+      }
+      // the CTAs after c that hold a piece, up to the one where the pair ends
+      // (the first with a segment that is not a single segment cut at its end)
+      const bool has = k > c && (r.y & kRecNonEmpty) != 0;
+      const bool ends = has && !((r.y & kRecSingle) && (r.y & kRecCutEnd));
+      const unsigned em = __ballot_sync(0xffffffffu, ends);
+      const unsigned upto = em ? (em & (0u - em)) * 2u - 1u : 0xffffffffu;
+      const unsigned hm = __ballot_sync(0xffffffffu, has) & upto;
+      if ((hm >> lane) & 1u) pieces[n + __popc(hm & ((1u << lane) - 1u))] = 2 * k;
+      n += __popc(hm);
+      if (em) break;
+    }
+    if (lane == 0) n_pieces = n;
+  }
+  __syncthreads();
+  const int np = n_pieces, pair = head_pair;
+  if (np == 0) return;
+  const int s = pair / Hkv, kvh = pair - s * Hkv;
+  if (pair < 0 || s >= a.num_seqs) return;
+  constexpr int PER = (G * D + kMergeThreads - 1) / kMergeThreads;
+  float M[PER], Ls[PER], O[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) { M[j] = kNegInfM; Ls[j] = 0.f; O[j] = 0.f; }
+  for (int p = 0; p < np; p += 4) {
+    float mv[PER][4], lv[PER][4], av[PER][4];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = threadIdx.x + j * kMergeThreads;
+      const int g = e / D, d = e - g * D;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        mv[j][u] = kNegInfM; lv[j][u] = 0.f; av[j][u] = 0.f;
+        if (p + u < np && e < G * D) {
+          const int64_t pk = (int64_t)pieces[p + u] * G + g;
+          mv[j][u] = a.ws_ml[2 * pk];
+          lv[j][u] = a.ws_ml[2 * pk + 1];
+          av[j][u] = a.ws_acc[pk * D + d];
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      float Mn = M[j];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) Mn = fmaxf(Mn, mv[j][u]);
+      if (Mn == kNegInfM) continue;
+      const float f = M[j] == kNegInfM ? 0.f : exp2f(M[j] - Mn);
+      Ls[j] *= f;
+      O[j] *= f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float wt = mv[j][u] == kNegInfM ? 0.f : exp2f(mv[j][u] - Mn);
+        Ls[j] += lv[j][u] * wt;
+        O[j] += av[j][u] * wt;
+      }
+      M[j] = Mn;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = threadIdx.x + j * kMergeThreads;
+    if (e >= G * D) break;
+    const int g = e / D, d = e - g * D;
+    out[((int64_t)s * Hq + (int64_t)kvh * G + g) * D + d] =
+        Vec<T>::cvt_out(Ls[j] > 0.f ? O[j] / Ls[j] : 0.f);
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -768,12 +1110,15 @@ bool encode_pool_map_fp8(CUtensorMap* map, const void* base, const DecodeArgs& a
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool KV8, bool SCALED>
+template <typename T, int D, int G, bool KV8, bool MULTI, bool SCALED>
 constexpr int mma_smem_bytes() {
   constexpr int kSt = ring_stages<KV8, SCALED>();
-  return 1024 + kSt * 2 * kTile * (KV8 ? D : 2 * D) + 2 * kSt * 8 + 4 + 4 * kSt +
-         2 * kMmaConsumers * 8 * 4 + (SCALED ? 2 * kSt * 8 * 4 + kSt * 4 : 0) +
-         16;
+  // 1024-byte alignment, the ring, then barriers, abort flag, tile masks,
+  // merge maxima and sums, stage scales (SCALED), the even schedule's start
+  // (8-byte aligned: 8 long longs, 2 ints)
+  return 1024 + kSt * (2 * kTile * (KV8 ? D : 2 * D) + q_slot_bytes<T, D, G, MULTI>()) +
+         2 * kSt * 8 + 4 + 4 * kSt +
+         2 * kMmaConsumers * 8 * 4 + 2 * kSt * 8 * 4 + kSt * 4 + 8 + 8 * 8 + 2 * 4 + 16;
 }
 
 template <typename T, int D, int G, bool KV8, bool MULTI, bool SCALED>
@@ -784,7 +1129,10 @@ cudaError_t launch_mma_tdgm(const DecodeArgs& a, float ks, float vs, cudaStream_
                       : (encode_pool_map(&tk, a.kc, MmaOps<T>::kTmaType, a) &&
                          encode_pool_map(&tv, a.vc, MmaOps<T>::kTmaType, a));
   if (!ok) return cudaErrorInvalidValue;
-  constexpr int smem = mma_smem_bytes<D, KV8, SCALED>();
+  constexpr int smem = mma_smem_bytes<T, D, G, KV8, MULTI, SCALED>();
+  // the CTAs per SM the kernel is built for fit the SM's 228 KB (1 KB of
+  // each CTA's shared memory is reserved by the system)
+  static_assert(ctas_per_sm<KV8, SCALED>() * (smem + 1024) <= 228 * 1024, "shared memory");
   static_assert(2 * kTile * (KV8 ? D : 2 * D) >= kMmaConsumers * 8 * D * 4,
                 "an item's merge must fit in one stage");
   static std::once_flag attr_once;
@@ -794,23 +1142,41 @@ cudaError_t launch_mma_tdgm(const DecodeArgs& a, float ks, float vs, cudaStream_
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  // one CTA per work item, or items_per_cta items each (a CTA walks its
-  // items while its producer runs ahead into the next one)
+  // one CTA per work item, items_per_cta items each (a CTA walks its items
+  // while its producer runs ahead into the next one), or a.even_ctas CTAs
+  // sharing the batch's tiles, then the merge of the pairs cut between them
   const int64_t n_items = (int64_t)a.num_splits * a.num_kv_heads * a.num_seqs;
+  const bool even = MULTI && a.even_ctas > 0;
   const int per = (MULTI && a.items_per_cta > 1) ? a.items_per_cta : 1;
-  const int64_t grid = (n_items + per - 1) / per;
-  if (n_items > 0x7fffffff) return cudaErrorInvalidValue;
+  const int64_t grid = even ? (int64_t)a.even_ctas : (n_items + per - 1) / per;
+  if (grid > 0x7fffffff || grid < 1) return cudaErrorInvalidValue;
   decode_mma_kernel<T, D, G, KV8, MULTI, SCALED><<<(unsigned)grid, kMmaThreads, smem, st>>>(
       a, tk, tv, ks, vs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (even) {
+    // the merge launch may start while the attention CTAs finish
+    // (programmatic dependent launch: its CTAs wait in griddepcontrol.wait
+    // before reading what the attention launch wrote)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = (size_t)grid * sizeof(int);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, even_merge_kernel<T, D, G>, a);
+  }
   return launch_combine(a, st);
 }
 
 template <typename T, int D, int G, bool KV8>
 cudaError_t launch_mma_tdg(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
   if constexpr (D == 128) {
-    if (a.items_per_cta > 1) {
+    if (a.even_ctas > 0 || a.items_per_cta > 1) {
       if constexpr (KV8) {
         if (a.k_scales != nullptr)
           return launch_mma_tdgm<T, D, G, KV8, true, true>(a, 1.f, 1.f, st);

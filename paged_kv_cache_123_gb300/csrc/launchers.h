@@ -49,14 +49,19 @@ struct DecodeArgs {
   int window;        // sliding window in tokens; 0 = the whole sequence
   int partition;     // tokens per split (multiple of max(64, block_size))
   int num_splits;    // ceil(max_seq_len / partition), >= 1
-  int items_per_cta; // tensor-core decode: work items per CTA (<= 1: one each)
+  // tensor-core decode (head size 128), windowed calls: work items per CTA
+  // (<= 1: one each), or the number of CTAs of one wave that share the
+  // batch's 64-token tiles evenly (the even schedule; 0 = not used)
+  int items_per_cta;
+  int even_ctas;
   // fp8 pools whose blocks carry their own scales: [num_blocks][num_kv_heads]
   // fp32 each (nullptr: one scale per pool)
   const float* k_scales;
   const float* v_scales;
   void* out;
-  float* ws_acc;     // [S][Hq][num_splits][D]   (num_splits > 1)
-  float* ws_ml;      // [S][Hq][num_splits][2]   (num_splits > 1)
+  float* ws_acc;     // [S][Hq][num_splits][D]   (num_splits > 1); EVEN: [C][2][G][D]
+  float* ws_ml;      // [S][Hq][num_splits][2]   (num_splits > 1); EVEN: [C][2][G][2]
+  int* ws_rec;       // EVEN: [C][2] (pair of the CTA's last segment, flags)
   int* err;
 };
 

@@ -1,6 +1,6 @@
 // Blackwell asynchronous-copy and synchronisation primitives used by the
-// tensor-core decode kernel: mbarriers with bounded waits, and tiled TMA
-// loads (cp.async.bulk.tensor) into shared memory.
+// tensor-core decode kernel: mbarriers with bounded waits, tiled TMA loads
+// (cp.async.bulk.tensor) and contiguous bulk copies into shared memory.
 #pragma once
 
 #include <cuda.h>
@@ -92,6 +92,17 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4, %5}], [%6];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w),
         "r"(bar)
+      : "memory");
+}
+
+// Contiguous bulk copy (cp.async.bulk) of `bytes` from global memory into
+// shared memory, completing on `bar`: both addresses 16-byte aligned, bytes
+// a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
 

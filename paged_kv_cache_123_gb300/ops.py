@@ -104,6 +104,23 @@ def pa_decode_fp8_partitioning(num_seqs: int, num_q_heads: int, num_kv_heads: in
     return s.value, p.value
 
 
+KV_FORMAT = {"16bit": 0, "fp8": 1, "fp8_block_scales": 2}
+
+
+def pa_decode_even_ctas(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_size: int,
+                        block_size: int, dtype: torch.dtype, kv_format: str, max_seq_len: int,
+                        window: int = 0, partition_size: int = 0) -> int:
+    """CTAs of the even schedule a decode call with these sizes runs (0: it
+    uses fixed partitions); kv_format is "16bit", "fp8" or
+    "fp8_block_scales", dtype the query type."""
+    n = lib().pa_decode_even_ctas(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                                  DTYPE_CODE[dtype], KV_FORMAT[kv_format], max_seq_len, window,
+                                  partition_size)
+    if n < 0:
+        check("pa_decode_even_ctas", int(n))
+    return int(n)
+
+
 def pa_decode_fp8_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int,
                                   head_size: int, block_size: int, dtype: torch.dtype,
                                   max_seq_len: int, window: int = 0,

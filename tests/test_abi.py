@@ -124,3 +124,21 @@ def test_fp8_and_multi_query_host_checks(lib):
     assert lib.pa_multi_query_attention(*args(1, 4, 2)) == -2
     assert lib.pa_multi_query_attention(*args(1, 16, 0)) == 0
     assert lib.pa_multi_query_workspace_bytes(8, 2, 48, 3, 128, 16, 4, 100, 0) == -2
+
+
+def test_even_schedule_query_on_the_host(lib):
+    # invalid arguments are refused, and calls that cannot take the even
+    # schedule answer 0, before any device is touched
+    q = lib.pa_decode_even_ctas
+    assert q(8, 64, 8, 128, 16, 2, 3, 4000, 1000, 0) == -2       # kv_format 3
+    assert q(8, 64, 8, 128, 16, 7, 0, 4000, 1000, 0) == -3       # dtype 7
+    assert q(8, 64, 8, 96, 16, 2, 0, 4000, 1000, 0) == -2        # head size 96
+    assert q(8, 64, 8, 128, 16, 2, 0, 4000, -1, 0) == -2         # window < 0
+    assert q(8, 64, 8, 128, 16, 2, 0, 4000, 0, 0) == 0           # no window
+    assert q(8, 64, 8, 128, 16, 2, 0, 4000, 4000, 0) == 0        # window covers all
+    assert q(8, 64, 8, 128, 16, 2, 0, 4000, 1000, 256) == 0      # fixed partitions asked
+    assert q(8, 64, 8, 64, 16, 2, 0, 4000, 1000, 0) == 0         # head size 64
+    assert q(8, 64, 8, 128, 16, 0, 0, 4000, 1000, 0) == 0        # fp32 queries
+    assert q(8, 8, 8, 128, 16, 2, 0, 4000, 1000, 0) == 0         # 16-bit pools, group 1
+    assert q(8, 64, 8, 128, 4, 2, 1, 4000, 1000, 0) == 0         # blocks of 4 tokens
+    assert q(9000, 64, 8, 128, 16, 2, 0, 4000, 1000, 0) == 0     # more than 8192 sequences

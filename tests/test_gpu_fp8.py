@@ -102,9 +102,10 @@ def test_fp8_full_step_against_oracle():
 
 def test_fp8_partitioning_query():
     """Tensor-core fp8 calls take the tensor-core partition sizes for every
-    group size (group 1 included), and windowed ones as many splits as keep
-    three CTAs per SM busy; pa_decode_fp8_workspace_bytes sizes the scratch
-    for exactly the partitioning pa_decode_fp8_partitioning reports."""
+    group size (group 1 included), and windowed ones sized for one wave of
+    three CTAs per SM, or the even schedule; pa_decode_fp8_workspace_bytes
+    sizes the scratch for exactly the partitioning pa_decode_fp8_partitioning
+    reports and for the even schedule of either fp8 call where it runs."""
     bf = torch.bfloat16
     # Llama-7B shape over fp8 pools: one partition per sequence
     assert pa.pa_decode_fp8_partitioning(64, 32, 32, 128, 16, bf, 2000) == (1, 2048)
@@ -119,9 +120,19 @@ def test_fp8_partitioning_query():
                 covered = min(L, W + 63) if 0 < W < L else L
                 assert splits == -(-covered // ptoks) and ptoks % max(64, B) == 0
                 ws = pa.pa_decode_fp8_workspace_bytes(S, Hq, Hkv, D, B, dt, L, W)
-                assert (ws > 0) == (splits > 1)
-                if splits > 1:
-                    assert ws >= S * Hq * splits * (D + 2) * 4
+                fixed = 0 if splits == 1 else (-(-S * Hq * splits * D * 4 // 256) * 256 +
+                                               S * Hq * splits * 8)
+                need = fixed
+                for fmt, per in (("fp8", 3), ("fp8_block_scales", 4)):
+                    C = pa.pa_decode_even_ctas(S, Hq, Hkv, D, B, dt, fmt, L, W)
+                    if dt == torch.float32 or D != 128 or B < 8 or not 0 < W < L:
+                        assert C == 0
+                    assert 0 <= C <= per * sms
+                    if C:      # the even schedule: partials, maxima and sums, records
+                        G = Hq // Hkv
+                        need = max(need, -(-C * 2 * G * D * 4 // 256) * 256 +
+                                   -(-C * 2 * G * 2 * 4 // 256) * 256 + C * 8)
+                assert ws == need
                 if dt != torch.float32 and D == 128 and B >= 8 and 0 < W < L:
                     # windowed tensor-core fp8: as many splits as fill one
                     # wave of three CTAs per SM, never more

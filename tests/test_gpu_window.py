@@ -104,6 +104,9 @@ def test_window_workspace_and_argument_errors():
     splits, tok = pa.pa_decode_window_partitioning(16, 32, 8, 16, 32768, 4096, 0)
     assert 16 * 8 * splits <= 2 * sms and splits * tok >= 4096 + 63 and tok % 64 == 0
     assert (splits - 1) * tok < 4096 + 63
+    # these partitions give 16 x 8 x 2 items for 2 x SMs slots, close enough
+    # to one item per slot that the 16-bit call keeps them (no even schedule)
+    assert pa.pa_decode_even_ctas(16, 32, 8, 128, 16, torch.bfloat16, "16bit", 32768, 4096) == 0
     assert pa.pa_decode_window_workspace_bytes(16, 32, 8, 128, 16, 32768, 4096, 0) == (
         0 if splits == 1 else 16 * 32 * splits * (128 * 4 + 8))
     # no window, or one covering every sequence: the unwindowed partitioning
