@@ -23,8 +23,10 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ qsl, int num_req
                                     const int32_t* __restrict__ table,
                                     int64_t stride, int block_size,
                                     int64_t* __restrict__ slots, int* err) {
+  griddep_launch();
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= num_tokens) return;
+  griddep_wait();
   // lo = number of entries of qsl[0..num_reqs] that are <= t
   int lo = 0, hi = num_reqs + 1;
   while (lo < hi) {
@@ -55,9 +57,8 @@ cudaError_t launch_slot_mapping(const int32_t* qsl, int num_reqs,
   if (num_tokens == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = (num_tokens + threads - 1) / threads;
-  slot_mapping_kernel<<<(unsigned)blocks, threads, 0, st>>>(
-      qsl, num_reqs, positions, num_tokens, table, stride, block_size, slots, err);
-  return cudaGetLastError();
+  return launch_pdl(slot_mapping_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, qsl,
+                    num_reqs, positions, num_tokens, table, stride, block_size, slots, err);
 }
 
 // One thread per 16-byte vector of a (token, kv head) row, K and V together.
@@ -70,6 +71,8 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ k,
                                          uint4* __restrict__ vc,
                                          int64_t num_blocks, int block_size,
                                          int* err) {
+  griddep_launch();
+  griddep_wait();
   const int64_t n = num_tokens * num_kv_heads * vec_per_row;
   const int64_t limit = num_blocks * block_size;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -104,10 +107,9 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v,
   const int threads = 256;
   int64_t blocks = (n + threads - 1) / threads;
   if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
-  reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, st>>>(
-      (const uint4*)k, (const uint4*)v, num_tokens, num_kv_heads, vpr, slots,
-      (uint4*)kc, (uint4*)vc, num_blocks, block_size, err);
-  return cudaGetLastError();
+  return launch_pdl(reshape_and_cache_kernel, dim3((unsigned)blocks), dim3(threads), 0, st,
+                    (const uint4*)k, (const uint4*)v, num_tokens, num_kv_heads, vpr, slots,
+                    (uint4*)kc, (uint4*)vc, num_blocks, block_size, err);
 }
 
 struct CopyLayerPtrs {

@@ -75,4 +75,34 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Programmatic dependent launch. The decode step's kernels are launched with
+// launch_pdl, so a kernel's CTAs may start while the kernel before it in the
+// stream drains: each calls griddep_wait() before its first access to
+// global memory (it returns once the previous kernel has completed and its
+// writes are visible, at once for a plain launch), and griddep_launch()
+// early, which lets the next kernel start. Only shared-memory set-up runs
+// before the wait.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace pa

@@ -303,6 +303,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     if (even) ev_i[0] = -1;
     mbar_fence_init();
   }
+  griddep_wait();
   if (even) {
     // the batch's tiles T (every thread sums a contiguous range of
     // sequences, then an exclusive scan over the threads); this CTA's share
@@ -353,9 +354,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
     }
   }
   __syncthreads();
-  // even schedule: the merge launch may be scheduled now; it waits for this
-  // grid to complete before it reads the partials
-  if (even) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the next launch (the combine or merge) may be scheduled now; it waits
+  // for this grid to complete before it reads the partials
+  griddep_launch();
 
   if (warp == kMmaConsumers) {
     // ---------------- producer warp: lane p owns piece p (R rows of one
@@ -972,7 +973,7 @@ __global__ void __launch_bounds__(kMergeThreads) even_merge_kernel(const DecodeA
     }
   }
   // the attention launch's records and partials are complete past this
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  griddep_wait();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     constexpr int kHead = kRecNonEmpty | kRecStart0 | kRecCutEnd;
@@ -1150,25 +1151,15 @@ cudaError_t launch_mma_tdgm(const DecodeArgs& a, float ks, float vs, cudaStream_
   const int per = (MULTI && a.items_per_cta > 1) ? a.items_per_cta : 1;
   const int64_t grid = even ? (int64_t)a.even_ctas : (n_items + per - 1) / per;
   if (grid > 0x7fffffff || grid < 1) return cudaErrorInvalidValue;
-  decode_mma_kernel<T, D, G, KV8, MULTI, SCALED><<<(unsigned)grid, kMmaThreads, smem, st>>>(
-      a, tk, tv, ks, vs);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(decode_mma_kernel<T, D, G, KV8, MULTI, SCALED>, dim3((unsigned)grid),
+                             dim3(kMmaThreads), smem, st, a, tk, tv, ks, vs);
   if (e != cudaSuccess) return e;
   if (even) {
     // the merge launch may start while the attention CTAs finish
     // (programmatic dependent launch: its CTAs wait in griddepcontrol.wait
     // before reading what the attention launch wrote)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kMergeThreads);
-    cfg.dynamicSmemBytes = (size_t)grid * sizeof(int);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, even_merge_kernel<T, D, G>, a);
+    return launch_pdl(even_merge_kernel<T, D, G>, dim3((unsigned)grid), dim3(kMergeThreads),
+                      (size_t)grid * sizeof(int), st, a);
   }
   return launch_combine(a, st);
 }

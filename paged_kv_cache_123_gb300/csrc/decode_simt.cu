@@ -49,6 +49,8 @@ decode_simt_kernel(const DecodeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / TPT, sub = lane % TPT;
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
+  griddep_launch();
+  griddep_wait();
   const int L = a.seq_lens[s];
   if (bad_length(a, L) || L == 0) {
     if (split == 0) {
@@ -216,6 +218,8 @@ decode_simt_kernel(const DecodeArgs a) {
 template <typename T, int D>
 __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a) {
   const int s = blockIdx.y, h = blockIdx.x, d = threadIdx.x;
+  griddep_launch();
+  griddep_wait();
   const int L = a.seq_lens[s];
   if (bad_length(a, L) || L == 0) return;
   const int tb = window_base(window_lo(L, a.window));
@@ -239,8 +243,7 @@ template <typename T, int D>
 cudaError_t launch_combine_td(const DecodeArgs& a, cudaStream_t st) {
   if (a.num_splits <= 1) return cudaSuccess;
   dim3 grid(a.num_q_heads, a.num_seqs);
-  combine_kernel<T, D><<<grid, D, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel<T, D>, grid, dim3(D), 0, st, a);
 }
 
 template <typename T>
@@ -263,8 +266,8 @@ template <typename T, int D, int G>
 cudaError_t launch_simt_tg(const DecodeArgs& a, cudaStream_t st) {
   constexpr int U = (G <= 2) ? 4 : (G == 4 ? 2 : 1);
   dim3 grid(a.num_splits, a.num_kv_heads, a.num_seqs);
-  decode_simt_kernel<T, D, G, U><<<grid, kSimtWarps * 32, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(decode_simt_kernel<T, D, G, U>, grid, dim3(kSimtWarps * 32),
+                                   0, st, a);
   if (e != cudaSuccess) return e;
   return launch_combine_td<T, D>(a, st);
 }

@@ -97,6 +97,8 @@ __global__ void fix_block_scales_kernel(const T* __restrict__ k, const T* __rest
                                         const int64_t* __restrict__ slots, int64_t num_blocks,
                                         int block_size, float* __restrict__ k_scales,
                                         float* __restrict__ v_scales) {
+  griddep_launch();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t limit = num_blocks * block_size;
@@ -141,6 +143,8 @@ __global__ void reshape_and_cache_fp8_kernel(const T* __restrict__ k, const T* _
                                              int64_t num_blocks, int block_size, float k_scale,
                                              float v_scale, const float* __restrict__ k_scales,
                                              const float* __restrict__ v_scales, int* err) {
+  griddep_launch();
+  griddep_wait();
   const int per_row = D / 8;
   const int64_t n = num_tokens * num_kv_heads * per_row;
   const int64_t limit = num_blocks * block_size;
@@ -205,35 +209,35 @@ cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, int64_t n
     const int64_t warps = num_tokens * num_kv_heads;
     int64_t blocks = (warps + threads / 32 - 1) / (threads / 32);
     if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
-#define PA_FIX_SCALES(TT)                                                                \
-  fix_block_scales_kernel<TT><<<(unsigned)blocks, threads, 0, st>>>(                     \
-      (const TT*)k, (const TT*)v, num_tokens, num_kv_heads, head_size, slots, num_blocks, \
-      block_size, k_scales, v_scales)
+#define PA_FIX_SCALES(TT)                                                                  \
+  launch_pdl(fix_block_scales_kernel<TT>, dim3((unsigned)blocks), dim3(threads), 0, st,    \
+             (const TT*)k, (const TT*)v, num_tokens, num_kv_heads, head_size, slots,       \
+             num_blocks, block_size, k_scales, v_scales)
+    cudaError_t e;
     switch (dtype) {
-      case PA_F32: PA_FIX_SCALES(float); break;
-      case PA_F16: PA_FIX_SCALES(__half); break;
-      case PA_BF16: PA_FIX_SCALES(__nv_bfloat16); break;
+      case PA_F32: e = PA_FIX_SCALES(float); break;
+      case PA_F16: e = PA_FIX_SCALES(__half); break;
+      case PA_BF16: e = PA_FIX_SCALES(__nv_bfloat16); break;
       default: return cudaErrorInvalidValue;
     }
 #undef PA_FIX_SCALES
-    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   const int64_t n = num_tokens * num_kv_heads * (head_size / 8);
   int64_t blocks = (n + threads - 1) / threads;
   if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
-#define PA_FP8_WRITE(TT)                                                                 \
-  reshape_and_cache_fp8_kernel<TT><<<(unsigned)blocks, threads, 0, st>>>(                \
-      (const TT*)k, (const TT*)v, num_tokens, num_kv_heads, head_size, slots, (uint8_t*)kc, \
-      (uint8_t*)vc, num_blocks, block_size, k_scale, v_scale, k_scales, v_scales, err)
+#define PA_FP8_WRITE(TT)                                                                   \
+  launch_pdl(reshape_and_cache_fp8_kernel<TT>, dim3((unsigned)blocks), dim3(threads), 0, st, \
+             (const TT*)k, (const TT*)v, num_tokens, num_kv_heads, head_size, slots,         \
+             (uint8_t*)kc, (uint8_t*)vc, num_blocks, block_size, k_scale, v_scale, k_scales,  \
+             v_scales, err)
   switch (dtype) {
-    case PA_F32: PA_FP8_WRITE(float); break;
-    case PA_F16: PA_FP8_WRITE(__half); break;
-    case PA_BF16: PA_FP8_WRITE(__nv_bfloat16); break;
-    default: return cudaErrorInvalidValue;
+    case PA_F32: return PA_FP8_WRITE(float);
+    case PA_F16: return PA_FP8_WRITE(__half);
+    case PA_BF16: return PA_FP8_WRITE(__nv_bfloat16);
   }
 #undef PA_FP8_WRITE
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 #define kNegInf8 (-__int_as_float(0x7f800000))
@@ -256,6 +260,8 @@ decode_fp8_kernel(const DecodeArgs a, float k_scale, float v_scale) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / TPT, sub = lane % TPT;
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
+  griddep_launch();
+  griddep_wait();
   const int L = a.seq_lens[s];
   T* out = reinterpret_cast<T*>(a.out);
   if (L < 0 || L > a.max_seq_len || (int64_t)L > a.table_stride * a.block_size || L == 0) {
@@ -419,11 +425,12 @@ template <typename T, int D, int G>
 cudaError_t launch_fp8_tdg(const DecodeArgs& a, float ks, float vs, cudaStream_t st) {
   constexpr int U = (G <= 2) ? 4 : (G == 4 ? 2 : 1);
   dim3 grid(a.num_splits, a.num_kv_heads, a.num_seqs);
-  if (a.k_scales != nullptr)
-    decode_fp8_kernel<T, D, G, U, true><<<grid, kFp8Warps * 32, 0, st>>>(a, 1.f, 1.f);
-  else
-    decode_fp8_kernel<T, D, G, U, false><<<grid, kFp8Warps * 32, 0, st>>>(a, ks, vs);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      a.k_scales != nullptr
+          ? launch_pdl(decode_fp8_kernel<T, D, G, U, true>, grid, dim3(kFp8Warps * 32), 0, st, a,
+                       1.f, 1.f)
+          : launch_pdl(decode_fp8_kernel<T, D, G, U, false>, grid, dim3(kFp8Warps * 32), 0, st, a,
+                       ks, vs);
   if (e != cudaSuccess) return e;
   return launch_combine(a, st);
 }
