@@ -416,8 +416,7 @@ PA_API int pa_decode_attention_fp8_scaled(const void* q, const void* key_cache,
  * size 128, at most 8192 sequences and the tensor-core kernel (16-bit
  * queries; 16-bit pools with groups of 2, 4 or 8, or fp8 pools with any
  * group; blocks of at least 8 tokens) run one wave of CTAs (SMs x 2 for
- * 16-bit pools, x 3 for fp8 pools, x 4 for fp8 pools with per-block
- * scales). Each CTA takes whole partitions of the fixed partitioning in
+ * 16-bit pools, x 3 for fp8 pools). Each CTA takes whole partitions of the fixed partitioning in
  * turn, unless whole partitions would leave the busiest CTA more than 1.25
  * times the mean work; then the even schedule runs: the batch's 64-token
  * tiles — those of every (sequence, KV head) pair in order, each pair from

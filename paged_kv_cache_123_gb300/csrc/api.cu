@@ -147,8 +147,9 @@ int covered_len(int max_seq_len, int window) {
 bool windowed(int max_seq_len, int window) { return window > 0 && window < max_seq_len; }
 
 // Windowed tensor-core decode calls (head size 128) with automatic
-// partitioning run one wave of resident CTAs (ctas_per_sm per SM: 2 for
-// 16-bit pools, 3 for fp8 pools, 4 for fp8 pools with per-block scales).
+// partitioning run one wave of resident CTAs (2 per SM for 16-bit pools, 3
+// for fp8 pools; the kernel's CTAs that walk several items run three per
+// SM with per-block scales too).
 // A window cuts every long sequence to about the same work, and the fixed
 // partitions give items of equal length: when there are more items than
 // slots, each CTA walks several (items_per_cta, strided). Whole items rarely
@@ -363,7 +364,7 @@ int pa_decode_even_ctas(int num_seqs, int num_q_heads, int num_kv_heads, int hea
   int per;
   int64_t C;
   wave_plan(num_seqs, num_kv_heads, splits, max_seq_len, window, g_sm_count[dev],
-            kv_format == 0 ? 2 : (kv_format == 1 ? 3 : 4), &per, &C);
+            kv_format == 0 ? 2 : 3, &per, &C);
   return (int)C;
 }
 
@@ -385,18 +386,15 @@ int64_t pa_decode_fp8_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_
   if (st != PA_OK) return st;
   int64_t ws = workspace_for(num_seqs, num_q_heads, head_size, splits);
   if (even_applies(num_seqs, head_size, max_seq_len, window, partition_size, tc8)) {
-    // the even schedule, if either fp8 call (three CTAs per SM, four with
-    // per-block scales) takes it
+    // the even schedule, if the call takes it
     int dev;
     st = device_setup(&dev);
     if (st != PA_OK) return st;
-    for (int per_sm = 3; per_sm <= 4; ++per_sm) {
-      int per;
-      int64_t C;
-      wave_plan(num_seqs, num_kv_heads, splits, max_seq_len, window, g_sm_count[dev], per_sm,
-                &per, &C);
-      if (C > 0) ws = std::max(ws, even_workspace(C, num_q_heads / num_kv_heads, head_size));
-    }
+    int per;
+    int64_t C;
+    wave_plan(num_seqs, num_kv_heads, splits, max_seq_len, window, g_sm_count[dev], 3, &per,
+              &C);
+    if (C > 0) ws = std::max(ws, even_workspace(C, num_q_heads / num_kv_heads, head_size));
   }
   return ws;
 }
@@ -788,7 +786,7 @@ int run_decode(const void* q, const void* key_cache, const void* value_cache,
   int64_t C = 0;
   if (even_applies(num_seqs, head_size, max_seq_len, window, partition_size, tc16 || tc8))
     wave_plan(num_seqs, num_kv_heads, a.num_splits, max_seq_len, window, g_sm_count[dev],
-              tc8 ? (k_scales ? 4 : 3) : 2, &a.items_per_cta, &C);
+              tc8 ? 3 : 2, &a.items_per_cta, &C);
   if (C > 0) {
     const int group = num_q_heads / num_kv_heads;
     const int64_t need = even_workspace(C, group, head_size);

@@ -45,16 +45,19 @@ namespace pa {
 constexpr int kMmaConsumers = 4;
 constexpr int kMmaThreads = (kMmaConsumers + 1) * 32;
 constexpr int kTile = 64;
-// stages of the K/V ring: four for fp8 pools with one scale per pool (16 KB
-// stages, three CTAs per SM: 192 KB in flight per SM, as the 16-bit ring's
-// three 32 KB stages at two CTAs per SM), three for 16-bit pools and for
-// fp8 pools with per-block scales, which run four CTAs per SM (more warps
-// to cover their dependent scale lookups: 0.67 -> 0.71 of the copy
-// bandwidth on the GQA batch; one-scale pools measured no better with four)
-template <bool KV8, bool SCALED>
-constexpr int ring_stages() { return (KV8 && !SCALED) ? 4 : 3; }
-template <bool KV8, bool SCALED>
-constexpr int ctas_per_sm() { return KV8 ? (SCALED ? 4 : 3) : 2; }
+// stages of the K/V ring: four for fp8 pools (16 KB stages, three CTAs per
+// SM: 192 KB in flight per SM, as the 16-bit ring's three 32 KB stages at
+// two CTAs per SM), three for 16-bit pools and for one-item CTAs over fp8
+// pools with per-block scales, which run four CTAs per SM (more warps to
+// cover their dependent scale lookups: 0.67 -> 0.71 of the copy bandwidth
+// on the GQA batch; one-scale pools measured no better with four). CTAs
+// that walk several items over per-block-scale pools keep three per SM:
+// at four (96 registers) their consumers spilled (GQA batch, window 1000:
+// 71.8 us against 66.8 us at three).
+template <bool KV8, bool SCALED, bool MULTI>
+constexpr int ring_stages() { return KV8 ? (SCALED && !MULTI ? 3 : 4) : 3; }
+template <bool KV8, bool SCALED, bool MULTI>
+constexpr int ctas_per_sm() { return KV8 ? (SCALED && !MULTI ? 4 : 3) : 2; }
 // MULTI: an item's query group rides in the stage of its first tile, in a
 // slot that keeps the stages 1024-byte aligned (128-byte swizzle), so the
 // consumers hold no prefetched query in registers (a one-item CTA loads it
@@ -109,7 +112,7 @@ __device__ __forceinline__ bool consumers_bar_and(bool ok) {
 // output is multiplied by its reference when the warps merge; the
 // denominator sums the unscaled weights.
 template <typename T, int D, int G, bool KV8, bool MULTI, bool SCALED>
-__global__ void __launch_bounds__(kMmaThreads, ctas_per_sm<KV8, SCALED>())
+__global__ void __launch_bounds__(kMmaThreads, ctas_per_sm<KV8, SCALED, MULTI>())
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, float k_scale, float v_scale) {
   constexpr int HALVES = D / 64;                 // 128-byte lines per 16-bit token row
@@ -119,7 +122,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
   constexpr int Q_BYTES = G * D * (int)sizeof(T);
   constexpr int STAGE_BYTES = 2 * KV_BYTES + q_slot_bytes<T, D, G, MULTI>();
   constexpr int PRIV_BYTES = 0;
-  constexpr int kSt = ring_stages<KV8, SCALED>();
+  constexpr int kSt = ring_stages<KV8, SCALED, MULTI>();
   static_assert(!KV8 || D == 128, "fp8 pools: head size 128 (one 128-byte line per row)");
   // fp8 pools run the products in fp16 whatever the query type: codes widen
   // to fp16 in one conversion. A bf16 query group is first multiplied by the
@@ -1113,7 +1116,7 @@ bool encode_pool_map_fp8(CUtensorMap* map, const void* base, const DecodeArgs& a
 
 template <typename T, int D, int G, bool KV8, bool MULTI, bool SCALED>
 constexpr int mma_smem_bytes() {
-  constexpr int kSt = ring_stages<KV8, SCALED>();
+  constexpr int kSt = ring_stages<KV8, SCALED, MULTI>();
   // 1024-byte alignment, the ring, then barriers, abort flag, tile masks,
   // merge maxima and sums, stage scales (SCALED), the even schedule's start
   // (8-byte aligned: 8 long longs, 2 ints)
@@ -1133,7 +1136,7 @@ cudaError_t launch_mma_tdgm(const DecodeArgs& a, float ks, float vs, cudaStream_
   constexpr int smem = mma_smem_bytes<T, D, G, KV8, MULTI, SCALED>();
   // the CTAs per SM the kernel is built for fit the SM's 228 KB (1 KB of
   // each CTA's shared memory is reserved by the system)
-  static_assert(ctas_per_sm<KV8, SCALED>() * (smem + 1024) <= 228 * 1024, "shared memory");
+  static_assert(ctas_per_sm<KV8, SCALED, MULTI>() * (smem + 1024) <= 228 * 1024, "shared memory");
   static_assert(2 * kTile * (KV8 ? D : 2 * D) >= kMmaConsumers * 8 * D * 4,
                 "an item's merge must fit in one stage");
   static std::once_flag attr_once;

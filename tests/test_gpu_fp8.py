@@ -123,7 +123,7 @@ def test_fp8_partitioning_query():
                 fixed = 0 if splits == 1 else (-(-S * Hq * splits * D * 4 // 256) * 256 +
                                                S * Hq * splits * 8)
                 need = fixed
-                for fmt, per in (("fp8", 3), ("fp8_block_scales", 4)):
+                for fmt, per in (("fp8", 3), ("fp8_block_scales", 3)):
                     C = pa.pa_decode_even_ctas(S, Hq, Hkv, D, B, dt, fmt, L, W)
                     if dt == torch.float32 or D != 128 or B < 8 or not 0 < W < L:
                         assert C == 0
