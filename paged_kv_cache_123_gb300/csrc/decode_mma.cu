@@ -65,6 +65,7 @@ constexpr int ctas_per_sm() { return KV8 ? (SCALED && !MULTI ? 4 : 3) : 2; }
 template <typename T, int D, int G, bool MULTI>
 constexpr int q_slot_bytes() { return MULTI ? (G * D * (int)sizeof(T) + 1023) / 1024 * 1024 : 0; }
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr float kLazyLog2 = 8.f;   // reference maximum moves when exceeded by 2^8
 // even schedule: flags of a CTA's record (its last segment): it walked a
 // segment, that segment starts at its pair's first tile, ends before its
 // last, and is the CTA's only segment
@@ -743,14 +744,35 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const bool live0 = mn0 != kNegInfM, live1 = mn1 != kNegInfM;
-        const float al0 = live0 ? exp2f(m0 - mn0) : 1.f;
-        const float al1 = live1 ? exp2f(m1 - mn1) : 1.f;
-        const float p0 = live0 ? exp2f(x0 - mn0) : 0.f;
-        const float p2 = live0 ? exp2f(x2 - mn0) : 0.f;
-        const float p1 = live1 ? exp2f(x1 - mn1) : 0.f;
-        const float p3 = live1 ? exp2f(x3 - mn1) : 0.f;
+        // fp8 pools (ALU-bound): lazy reference: a head's reference maximum
+        // m moves (to the tile's maximum) only when the tile's maximum
+        // exceeds it by more than 2^kLazyLog2, so the weights 2^(x - m) stay
+        // below 2^8 (exact in fp16 as far as its rounding goes) and the
+        // output and sums are rescaled only on those rare tiles, in a
+        // warp-uniform branch; the final division and the merges use the
+        // same reference (GQA batch 216 -> 211 us, Llama-7B 95.6 -> 92.8 us).
+        // 16-bit pools (HBM-bound) keep the exact maximum and rescale every
+        // tile (the lazy form measured 0.6 % slower there).
+        const float lazy = KV8 ? kLazyLog2 : 0.f;
+        const bool up0 = mx0 > m0 + lazy, up1 = mx1 > m1 + lazy;
+        float al0 = 1.f, al1 = 1.f;
+        bool rescale = !KV8 || (SCALED && cv != 1.f);
+        if (!KV8 || __any_sync(0xffffffffu, up0 || up1)) {
+          if (up0) {
+            al0 = exp2f(m0 - mx0);       // 0 on the first tile (m0 = -inf)
+            m0 = mx0;
+          }
+          if (up1) {
+            al1 = exp2f(m1 - mx1);
+            m1 = mx1;
+          }
+          rescale = true;
+        }
+        const bool live0 = m0 != kNegInfM, live1 = m1 != kNegInfM;
+        const float p0 = live0 ? exp2f(x0 - m0) : 0.f;
+        const float p2 = live0 ? exp2f(x2 - m0) : 0.f;
+        const float p1 = live1 ? exp2f(x1 - m1) : 0.f;
+        const float p3 = live1 ? exp2f(x3 - m1) : 0.f;
         uint32_t cA, cB;
         float aO0 = al0, aO1 = al1;      // rescale of the output
         if constexpr (SCALED) {
@@ -768,11 +790,11 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
           l0 = l0 * al0 + fA.x + fB.x;
           l1 = l1 * al1 + fA.y + fB.y;
         }
-        m0 = mn0;
-        m1 = mn1;
+        if (rescale) {
 #pragma unroll
-        for (int mt = 0; mt < KSTEPS; ++mt) {
-          o[mt][0] *= aO0; o[mt][1] *= aO1; o[mt][2] *= aO0; o[mt][3] *= aO1;
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            o[mt][0] *= aO0; o[mt][1] *= aO1; o[mt][2] *= aO0; o[mt][3] *= aO1;
+          }
         }
         const uint32_t pb0 = movmatrix_trans(cA);
         const uint32_t pb1 = movmatrix_trans(cB);

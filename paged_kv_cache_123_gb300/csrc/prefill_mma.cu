@@ -33,6 +33,7 @@ constexpr int kMqTile = 64;        // KV tokens per stage
 constexpr int kMqStages = 3;
 constexpr long long kMqWaitCycles = 4000000000LL;
 #define kNegInfQ (-__int_as_float(0x7f800000))
+constexpr float kLazyLog2Q = 8.f;   // reference maximum moves when exceeded by 2^8
 
 // Producer warp: fill the ring with the KV tiles [0, ntiles) of (sequence,
 // kv head): lane p issues the TMA loads (whole rows, one 4-D box per block
@@ -275,25 +276,36 @@ multi_query_cols_kernel(const MultiQueryArgs a, const __grid_constant__ CUtensor
             mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
             mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
           }
-          float p[4], al[2];
+          // lazy reference (as in the decode kernel): a column's reference
+          // maximum moves to the tile's maximum only when that exceeds it
+          // by more than 2^8, so the weights stay below 2^8 and the output
+          // is rescaled only on those tiles, in a warp-uniform branch
+          float p[4], al[2] = {1.f, 1.f};
+          bool up[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) up[e] = mx[e] > m[nt][e] + kLazyLog2Q;
+          const bool rescale = __any_sync(0xffffffffu, up[0] || up[1]);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const float mn = fmaxf(m[nt][e], mx[e]);
-            const bool live = mn != kNegInfQ;
-            al[e] = live ? exp2f(m[nt][e] - mn) : 1.f;
-            p[e] = live ? exp2f(x[e] - mn) : 0.f;
-            p[e + 2] = live ? exp2f(x[e + 2] - mn) : 0.f;
-            m[nt][e] = mn;
+            if (up[e]) {
+              al[e] = exp2f(m[nt][e] - mx[e]);     // 0 on the first tile
+              m[nt][e] = mx[e];
+            }
+            const bool live = m[nt][e] != kNegInfQ;
+            p[e] = live ? exp2f(x[e] - m[nt][e]) : 0.f;
+            p[e + 2] = live ? exp2f(x[e + 2] - m[nt][e]) : 0.f;
           }
           const uint32_t cA = MmaOps<T>::pack(p[0], p[1]);
           const uint32_t cB = MmaOps<T>::pack(p[2], p[3]);
           const float2 fA = MmaOps<T>::unpack(cA), fB = MmaOps<T>::unpack(cB);
           l[nt][0] = l[nt][0] * al[0] + fA.x + fB.x;
           l[nt][1] = l[nt][1] * al[1] + fA.y + fB.y;
+          if (rescale) {
 #pragma unroll
-          for (int mt = 0; mt < KSTEPS; ++mt) {
-            o[nt][mt][0] *= al[0]; o[nt][mt][1] *= al[1];
-            o[nt][mt][2] *= al[0]; o[nt][mt][3] *= al[1];
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+              o[nt][mt][0] *= al[0]; o[nt][mt][1] *= al[1];
+              o[nt][mt][2] *= al[0]; o[nt][mt][3] *= al[1];
+            }
           }
           pb[nt][0] = movmatrix_trans(cA);
           pb[nt][1] = movmatrix_trans(cB);
