@@ -226,14 +226,33 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs a) {
   const int n = (L - tb + a.partition - 1) / a.partition;
   if (n <= 1) return;
   const int64_t base = ((int64_t)s * a.num_q_heads + h) * a.num_splits;
-  float M = kNegInf;
-  for (int p = 0; p < n; ++p) M = fmaxf(M, a.ws_ml[2 * (base + p)]);
-  float Ls = 0.f, O = 0.f;
-  for (int p = 0; p < n; ++p) {
-    const float mp = a.ws_ml[2 * (base + p)];
-    const float w = (mp == kNegInf) ? 0.f : exp2f(mp - M);
-    Ls += a.ws_ml[2 * (base + p) + 1] * w;
-    O += a.ws_acc[(base + p) * D + d] * w;
+  // one pass, four partitions at a time (their loads issued together): the
+  // running maximum M, with the sums rescaled when it grows
+  float M = kNegInf, Ls = 0.f, O = 0.f;
+  for (int p0 = 0; p0 < n; p0 += 4) {
+    float mv[4], lv[4], av[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int p = p0 + u;
+      mv[u] = kNegInf; lv[u] = 0.f; av[u] = 0.f;
+      if (p < n) {
+        mv[u] = a.ws_ml[2 * (base + p)];
+        lv[u] = a.ws_ml[2 * (base + p) + 1];
+        av[u] = a.ws_acc[(base + p) * D + d];
+      }
+    }
+    const float Mn = fmaxf(fmaxf(M, fmaxf(mv[0], mv[1])), fmaxf(mv[2], mv[3]));
+    if (Mn == kNegInf) continue;
+    const float f = (M == kNegInf) ? 0.f : exp2f(M - Mn);
+    Ls *= f;
+    O *= f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = (mv[u] == kNegInf) ? 0.f : exp2f(mv[u] - Mn);
+      Ls += lv[u] * w;
+      O += av[u] * w;
+    }
+    M = Mn;
   }
   T* out = reinterpret_cast<T*>(a.out);
   out[((int64_t)s * a.num_q_heads + h) * D + d] = Vec<T>::cvt_out(Ls > 0.f ? O / Ls : 0.f);
