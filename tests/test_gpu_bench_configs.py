@@ -1,7 +1,7 @@
 """Parity in the launch configurations bench.py times for the next rows: the
-GQA-72B-shaped prefill step (8 sequences x 512 new tokens, automatic
-partitioning, tcgen05 kernel) and the full GQA-72B decode step over fp8
-pools. The batches are built the way bench.py builds them; sampled outputs
+prefill steps (8 GQA-72B sequences x 512 new tokens, 4 long-context
+sequences x 256 new tokens; automatic partitioning, tcgen05 kernel) and the
+full GQA-72B decode step over fp8 pools. The batches are built the way bench.py builds them; sampled outputs
 are checked one by one against the oracle, every written slot and cache
 byte in full."""
 import dataclasses
@@ -19,10 +19,11 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def test_prefill_step_gqa72b_8x512():
-    N, S = 512, 8
-    base = workloads.CONFIGS["gqa72b"]
-    cfg = dataclasses.replace(base, num_seqs=S, name=f"{base.name}_s{S}")
+@pytest.mark.parametrize("name,S,N", [("gqa72b", 8, 512), ("longctx_B16", 4, 256)])
+def test_prefill_step(name, S, N):
+    base = workloads.CONFIGS[name]
+    cfg = dataclasses.replace(base, num_seqs=S, name=f"{base.name}_s{S}",
+                              ctx_fixed=None if base.ctx_fixed is None else base.ctx_fixed[:S])
     inp = workloads.make_decode_inputs(cfg, device=DEV, seed=cfg.seed)
     B, Hkv, D, Hq = cfg.block_size, cfg.num_kv_heads, cfg.head_size, cfg.num_q_heads
     gen = torch.Generator(device=DEV).manual_seed(cfg.seed + 77)
@@ -52,7 +53,7 @@ def test_prefill_step_gqa72b_8x512():
     rng = np.random.default_rng(2)
     worst = 0.0
     for s in (0, int(lens.argmax()), int(rng.integers(S))):
-        for i in (0, 127, 128, 300, N - 1):
+        for i in sorted({0, 127, 128, N // 2 + 44, N - 1}):
             t = s * N + i
             Ls = int(lens[s]) - N + i + 1
             for h in (0, 9, Hq - 1):

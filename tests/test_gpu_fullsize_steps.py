@@ -1,9 +1,10 @@
 """Full-size steps in the launch configurations bench.py times, not covered
 by the other full-size tests: 2, 4 and 8 speculative tokens per sequence of
 the GQA-72B batch (the multi-query kernels with automatic partitioning), the
-GQA-72B step over fp8 blocks that carry their own scales (the scale-fixing
-write and the scaled attention), and the Llama-7B step over fp8 pools (group
-1 on the tensor-core kernel). The batches are built the way bench.py builds
+GQA-72B, Llama-7B and long-context steps over fp8 blocks that carry their
+own scales (the scale-fixing write and the scaled attention), and the
+Llama-7B (group 1 on the tensor-core kernel) and long-context steps over fp8
+pools with one scale per pool. The batches are built the way bench.py builds
 them; every written slot, code and scale is checked in full and sampled
 outputs one by one against the oracle."""
 import numpy as np
@@ -78,9 +79,10 @@ def _block_scaled(x):
     return c_, s_.contiguous()
 
 
-def test_fp8_block_scales_step_gqa72b_full():
+@pytest.mark.parametrize("name", ["gqa72b", "llama7b", "longctx_B16"])
+def test_fp8_block_scales_step_full(name):
     pa.pa_get_device_error()
-    inp = workloads.make_decode_inputs("gqa72b", device=DEV)
+    inp = workloads.make_decode_inputs(name, device=DEV)
     cfg = inp.cfg
     kc, ks = _block_scaled(inp.key_cache)
     vc, vs = _block_scaled(inp.value_cache)
@@ -102,8 +104,9 @@ def test_fp8_block_scales_step_gqa72b_full():
     assert np.array_equal(ks.cpu().numpy(), ks_h) and np.array_equal(vs.cpu().numpy(), vs_h)
     assert np.array_equal(kc.cpu().numpy(), kc_h) and np.array_equal(vc.cpu().numpy(), vc_h)
     lens = inp.seq_lens.cpu().numpy()
-    seqs = sorted({int(lens.argmax()), int(lens.argmin()), 5, 90})
-    heads = [0, 21, cfg.num_q_heads - 1]
+    seqs = sorted({int(lens.argmax()), int(lens.argmin()), 5 % cfg.num_seqs,
+                   90 % cfg.num_seqs})
+    heads = [0, 21 % cfg.num_q_heads, cfg.num_q_heads - 1]
     want = oracle.decode_attention_fp8_block_scaled(
         np_(inp.q), kc_h, vc_h, ks_h, vs_h, inp.block_tables.cpu().numpy(), lens, inp.scale,
         cfg.num_kv_heads, cfg.block_size, cfg.dtype, seqs=seqs, heads=heads)
@@ -113,9 +116,10 @@ def test_fp8_block_scales_step_gqa72b_full():
     assert torch.isfinite(out.float()).all()
 
 
-def test_fp8_step_llama7b_full():
+@pytest.mark.parametrize("name", ["llama7b", "longctx_B16", "longctx_B128"])
+def test_fp8_step_full(name):
     pa.pa_get_device_error()
-    inp = workloads.make_decode_inputs("llama7b", device=DEV)
+    inp = workloads.make_decode_inputs(name, device=DEV)
     cfg = inp.cfg
     ks = vs = 1.0 / 48
     kc = (inp.key_cache.float() / ks).clamp_(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
@@ -134,8 +138,9 @@ def test_fp8_step_llama7b_full():
                                  vc_h, cfg.block_size, cfg.dtype, ks, vs)
     assert np.array_equal(kc.cpu().numpy(), kc_h) and np.array_equal(vc.cpu().numpy(), vc_h)
     lens = inp.seq_lens.cpu().numpy()
-    seqs = sorted({int(lens.argmax()), int(lens.argmin()), 7, 40})
-    heads = [0, 17, cfg.num_q_heads - 1]
+    seqs = sorted({int(lens.argmax()), int(lens.argmin()), 7 % cfg.num_seqs,
+                   40 % cfg.num_seqs})
+    heads = [0, 17 % cfg.num_q_heads, cfg.num_q_heads - 1]
     want = oracle.decode_attention_fp8(np_(inp.q), kc_h, vc_h, inp.block_tables.cpu().numpy(),
                                        lens, inp.scale, cfg.num_kv_heads, cfg.block_size,
                                        cfg.dtype, ks, vs, seqs=seqs, heads=heads)

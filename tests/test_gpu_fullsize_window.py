@@ -3,8 +3,9 @@ times (automatic partitioning), with the table entries of the blocks wholly
 before the window released to -1 as the host pool does: the even schedule
 (GQA-72B batch, 1000-token window, fp8 pools with one scale per pool and
 with per-block scales), the strided multi-item walk (the same window over
-16-bit pools; the Llama-7B batch with a 333-token window over fp8 pools)
-and fixed partitions (long-context batch, 4096-token window). Attention is
+16-bit pools; the Llama-7B batch with a 333-token window over fp8 pools),
+fixed partitions (long-context batch, 4096-token window) and the CUDA-core
+kernel (the Llama-7B batch with a 333-token window over 16-bit pools). Attention is
 checked element by element against the oracle on sampled (sequence, head)
 pairs that it computes one by one."""
 import numpy as np
@@ -22,7 +23,8 @@ FORMAT = {"16bit": "16bit", "fp8": "fp8", "fp8b": "fp8_block_scales"}
 # (workload, window, KV format, the schedule: even CTAs > 0, or 0)
 CASES = [("gqa72b", 1000, "fp8", True), ("gqa72b", 1000, "fp8b", True),
          ("gqa72b", 1000, "16bit", False), ("llama7b", 333, "fp8", False),
-         ("longctx_B16", 4096, "16bit", False), ("longctx_B16", 4096, "fp8", False)]
+         ("longctx_B16", 4096, "16bit", False), ("longctx_B16", 4096, "fp8", False),
+         ("llama7b", 333, "16bit", False)]
 
 
 def _codes(x, scale):
