@@ -19,6 +19,13 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream). Every call is asynchronous on that stream; a return of PA_OK
  *     means the arguments were valid and the kernels were launched.
+ *   - The decode step's kernels (slot mapping, KV writes, decode attention
+ *     and its combine or merge) are launched with programmatic dependent
+ *     launch: a kernel's blocks may be scheduled while the kernel before it
+ *     in the stream drains, but each waits for that kernel to complete, and
+ *     for its writes to be visible, before its first access to global
+ *     memory. Stream order is kept for every caller; only launch latency
+ *     and block set-up overlap.
  *   - Tensors are dense row-major in the shapes given below.
  *   - Physical KV pool layout (one pool for K, one for V):
  *         cache[num_blocks][num_kv_heads][block_size][head_size]
