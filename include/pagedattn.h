@@ -23,9 +23,9 @@
  *     and its combine or merge) are launched with programmatic dependent
  *     launch: a kernel's blocks may be scheduled while the kernel before it
  *     in the stream drains, but each waits for that kernel to complete, and
- *     for its writes to be visible, before its first access to global
- *     memory. Stream order is kept for every caller; only launch latency
- *     and block set-up overlap.
+ *     for its writes to be visible, before it touches memory that kernel
+ *     or any earlier one may write. Stream order is kept for every caller;
+ *     only launch latency and block set-up overlap.
  *   - Tensors are dense row-major in the shapes given below.
  *   - Physical KV pool layout (one pool for K, one for V):
  *         cache[num_blocks][num_kv_heads][block_size][head_size]
